@@ -1,0 +1,255 @@
+/*
+ * qmm.h -- C ABI of the GB300 group-quantized 4-bit-weight matmul library
+ * (libqmm_gb300.so, built for sm_103a).
+ *
+ * The library computes the quantized linear layer of LLM inference,
+ * y = W x, with W stored as 4-bit integers in groups of `group` consecutive
+ * inputs (k), one fp16 scale per (output row n, group g), in two variants:
+ *
+ *   QMM_W4A8   symmetric weights q in [-8, 7]. Activations are optionally
+ *              rotated by an in-group Walsh-Hadamard transform, quantized per
+ *              row and per group to int8, contracted with the weights into
+ *              exact int32 group partials, and rescaled in fp32:
+ *                  Y[m][n] = sum_g sw[n][g] * sx[m][g] * P[m][n][g]
+ *                  P[m][n][g] = sum_{k in g} q[n][k] * a[m][k]
+ *              (cactus PR #697 "SME2 acceleration for CQ4 matmul, prefill
+ *              attention, and orthogonal embeddings": Summary, "Quantized
+ *              matmul"; the per-group partials contract in its review thread;
+ *              geistlib issue #500 "native W*A8 int8 GEMM for prefill":
+ *              Design sketch.)
+ *
+ *   QMM_AFFINE unsigned weights q in [0, 15] with w = s*q + b per group. The
+ *              bias term needs the per-row group sums of X, S[m][g]:
+ *                  Y[m][n] = sum_g ( s[n][g] * sum_{k in g} q[n][k] x[m][k]
+ *                                   + b[n][g] * S[m][g] )
+ *              (TensorFold PR #3215 "simd_qmm on Metal: X's group sums and
+ *              half operands from a prepass": What this changes.)
+ *
+ * Calls:  qmm_pack_weights (once per weight) -> qmm_prep_act (per call) ->
+ *         qmm_gemv (M == 1, W4A8) or qmm_gemm (any M, both variants).
+ *
+ * Conventions for every entry point:
+ *   - All pointers named "device" are CUDA device pointers in the current
+ *     device's context; the caller allocates and owns them. The library
+ *     allocates no device memory.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream). Outputs are valid once the stream reaches that
+ *     point. Buffers passed to one call must not overlap one another.
+ *   - Argument errors are detected on the host before anything is enqueued
+ *     and returned synchronously; nothing is written in that case.
+ *   - A launch failure returns QMM_ERR_CUDA. There is no CPU fallback: a
+ *     shape or device the kernels do not cover returns an error code.
+ *   - Device pointers must be 16-byte aligned (QMM_ERR_MISALIGNED otherwise).
+ *   - Kernels are launched with programmatic dependent launch: each kernel
+ *     streams its packed weights before waiting on the previous kernel in the
+ *     stream, and waits before it reads activations or writes outputs.
+ *   - Not thread-safe per stream; distinct host threads may use distinct
+ *     streams.
+ */
+#ifndef QMM_H
+#define QMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QMM_OK = 0,
+    QMM_ERR_INVALID_ARG = 1,        /* null pointer, non-positive size, bad enum */
+    QMM_ERR_UNSUPPORTED_SHAPE = 2,  /* K % group != 0, group not supported, ... */
+    QMM_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not compute capability 10.3 */
+    QMM_ERR_MISALIGNED = 4,         /* a device pointer is not 16-byte aligned */
+    QMM_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed */
+    QMM_ERR_TIMEOUT = 6,            /* a kernel gave up a bounded wait (qmm_device_status) */
+    QMM_ERR_WORKSPACE = 7           /* workspace too small */
+} qmm_status;
+
+typedef enum { QMM_W4A8 = 0, QMM_AFFINE = 1 } qmm_variant;
+
+typedef enum { QMM_DTYPE_F32 = 0, QMM_DTYPE_F16 = 1, QMM_DTYPE_BF16 = 2 } qmm_dtype;
+
+/* Which kernel a debug call goes through. */
+typedef enum { QMM_PATH_GEMV = 0, QMM_PATH_GEMM = 1 } qmm_path;
+
+/* Kernel identifiers reported by qmm_last_kernel_id(). */
+typedef enum {
+    QMM_KERNEL_NONE = 0,
+    QMM_KERNEL_PACK = 1,
+    QMM_KERNEL_PREP_W4A8 = 2,
+    QMM_KERNEL_PREP_AFFINE = 3,
+    QMM_KERNEL_GEMV_W4A8 = 4,
+    QMM_KERNEL_GEMM_W4A8 = 5,
+    QMM_KERNEL_GEMM_AFFINE = 6
+} qmm_kernel_id;
+
+typedef void* qmm_stream; /* cudaStream_t */
+
+/* A quantized weight matrix W [N][K].
+ *   variant: QMM_W4A8 (group 64 or 128) or QMM_AFFINE (group 64).
+ *   N >= 1, K >= group, K % group == 0. */
+typedef struct {
+    int32_t variant;
+    int32_t N;
+    int32_t K;
+    int32_t group;
+} qmm_weight_desc;
+
+/*
+ * Packed weight blob ("pack once, one runtime format"; cactus PR #697:
+ * the packed weight cache is built once per weight and is the single runtime
+ * format of both engines; geistlib issue #500, Design sketch item 2: repack at
+ * resolve time).
+ *
+ * With T = ceil(N/128) row tiles, G = K/group groups and PP = group/32 pieces
+ * per group, the blob is T*G chunks of CB bytes,
+ *     CB = 64*group + 256            (QMM_W4A8)
+ *     CB = 64*group + 512            (QMM_AFFINE),
+ * chunk (t, g) at byte (t*G + g)*CB. Inside a chunk:
+ *     [0, 64*group)           nibbles: piece p (0..PP-1), row r (0..127) at
+ *                             p*2048 + r*16; 16 bytes = 32 weights of row
+ *                             n = 128t + r, k = g*group + 32p + 0..31, as four
+ *                             little-endian 32-bit words j = 0..3 covering
+ *                             k = 8j..8j+7 of the piece. In word j, nibble slot
+ *                             s (bits 4s..4s+3) holds local k = 8j + 2s for
+ *                             s < 4 and 8j + 2(s-4) + 1 for s >= 4.
+ *                             Nibble value: q + 8 (QMM_W4A8), q (QMM_AFFINE).
+ *     [64*group, +256)        scales: 128 fp16, row r at 2r (sw[n][g]).
+ *     [64*group+256, +256)    biases (QMM_AFFINE only): 128 fp16, row r at 2r.
+ * Rows n >= N of the last tile hold q = 0 and zero scales and biases.
+ * The blob depends only on the logical values of q, scales and biases.
+ */
+size_t qmm_packed_size(const qmm_weight_desc* w);
+
+/*
+ * Repack weights into the blob above (device kernel, on `stream`).
+ *   q       device, [N][K/2] bytes, row-major. Byte j of row n holds k = 2j in
+ *           its low nibble and k = 2j+1 in its high nibble (cactus PR #697,
+ *           follow-up "single runtime weight format": low nibble first).
+ *           QMM_W4A8: 4-bit two's complement q in [-8, 7]. QMM_AFFINE: q in [0, 15].
+ *   scales  device, [N][G] fp16 (sw for W4A8, s for affine).
+ *   biases  device, [N][G] fp16; QMM_AFFINE only (must be NULL for QMM_W4A8).
+ *   packed  device, qmm_packed_size(w) bytes, written entirely.
+ * K must be a multiple of 32 and of group. The sources may be freed once the
+ * stream has passed this call.
+ */
+qmm_status qmm_pack_weights(const qmm_weight_desc* w, const uint8_t* q, const uint16_t* scales,
+                            const uint16_t* biases, void* packed, qmm_stream stream);
+
+/*
+ * Activation prepass (device kernel, on `stream`).
+ *
+ * QMM_W4A8 (cactus PR #697, Summary: "phase A does parallel Hadamard + int8
+ * activation quantization"; geistlib issue #500, Design sketch item 4: one
+ * activation quantization shared by the GEMV and GEMM paths). For each row m
+ * and group g, with v = x[m][g*group .. +group) in fp32:
+ *   if hadamard == group: v <- H v, the unnormalised Sylvester-order
+ *       Walsh-Hadamard transform, butterfly stages h = 1, 2, 4, .., group/2,
+ *       each (v[i], v[i+h]) <- (v[i] + v[i+h], v[i] - v[i+h]) for (i & h) == 0,
+ *       in fp32;
+ *   amax = max |v|;  s = amax / 127 (fp32, IEEE division);
+ *   a[m][k] = clamp(rint(v / s), -127, 127) (fp32 division, ties to even);
+ *   sx[m][g] = s * c with c = fp32(1/sqrt(group)) when rotated, else 1;
+ *   amax == 0 gives a = 0 and sx = 0;
+ *   asum[m][g] = sum of the group's a.
+ *   The orthonormal rotation H/sqrt(n) is carried by the scale, so the int8
+ *   codes do not depend on its rounding.
+ * Outputs (any may be NULL except sx):
+ *   a     device int8  [M][K]   codes (GEMV operand)
+ *   a16   device fp16  [M][K]   the same codes as fp16 (exact; GEMM operand)
+ *   sx    device fp32  [M][G]
+ *   asum  device int32 [M][G]
+ * x: device [M][K], dtype x_dtype (F32, F16 or BF16; widened exactly to fp32).
+ *
+ * QMM_AFFINE (TensorFold PR #3215, What this changes: the group sums of X are
+ * written once per call by a prepass, each with the tree
+ * ((c0+c1)+(c2+c3))+((c4+c5)+(c6+c7)), c_j the left-to-right fp32 sum of
+ * inputs 8j..8j+7 of the group). group must be 64, hadamard 0.
+ *   gsum  device fp32 [M][G]    S[m][g] (required)
+ *   x16   device fp16 [M][K]    fp16 image of x (RNE) when x_dtype is F32 or
+ *                               BF16; may be NULL when x is already F16 (the
+ *                               GEMM then reads x itself).
+ *   S is summed from the fp32 values of x as given.
+ * Pointers of the other variant must be NULL.
+ */
+qmm_status qmm_prep_act(int32_t variant, int32_t M, int32_t K, int32_t group, int32_t hadamard,
+                        const void* x, int32_t x_dtype,
+                        int8_t* a, uint16_t* a16, float* sx, int32_t* asum,
+                        float* gsum, uint16_t* x16, qmm_stream stream);
+
+/*
+ * Bytes of workspace qmm_gemv wants for split-K over `w` (0 if none).
+ * The workspace must be zero-filled before its first use; every completed
+ * call leaves its counters at zero again, so it can be reused by later calls
+ * on the same stream without clearing. Calls that may run concurrently need
+ * separate workspaces.
+ */
+size_t qmm_gemv_workspace_size(const qmm_weight_desc* w);
+
+/*
+ * M = 1 decode GEMV, QMM_W4A8 (cactus PR #697, Summary: hybrid fused GEMV,
+ * "stream packed nibbles ... half the weight bytes"; the op is DRAM-bound):
+ *   y[n] = sum_g sw[n][g] * sx[g] * P[n][g],  P[n][g] = sum_{k in g} q[n][k] a[k]
+ *   packed     device blob from qmm_pack_weights
+ *   a          device int8 [K] (qmm_prep_act output a, row 0)
+ *   sx         device fp32 [G]
+ *   y          device fp32 [N]
+ *   workspace  device, >= qmm_gemv_workspace_size(w) bytes, or NULL to run
+ *              without split-K (fewer CTAs; same result bits).
+ * Results are deterministic: a fixed reduction order, no atomics on data.
+ */
+qmm_status qmm_gemv(const qmm_weight_desc* w, const void* packed, const int8_t* a, const float* sx,
+                    float* y, void* workspace, size_t workspace_bytes, qmm_stream stream);
+
+/*
+ * GEMM, any M >= 1, both variants, on the tcgen05 tensor cores
+ * (cactus PR #697, Summary: fused GEMM with raw int32 partials and a separate
+ * fp32 rescale; TensorFold PR #3215 for the affine tiles on the prepass sums).
+ *   QMM_W4A8:   act16 = qmm_prep_act a16 [M][K] fp16 codes, act_scale = sx [M][G]
+ *               Y[m][n] = sum_g sw[n][g] * sx[m][g] * P[m][n][g]
+ *   QMM_AFFINE: act16 = x as fp16 [M][K],     act_scale = S  [M][G]
+ *               Y[m][n] = sum_g ( s[n][g] * sum_{k in g} q[n][k] x[m][k] + b[n][g] * S[m][g] )
+ *   Y          device fp32 [M][N], row-major; rows m < M written, nothing else.
+ * The weight operand is expanded from the nibbles to exact fp16 integers on
+ * chip; group partials accumulate in fp32 in tensor memory (exact integers for
+ * W4A8) and are rescaled in fp32 once per group.
+ */
+qmm_status qmm_gemm(const qmm_weight_desc* w, const void* packed, int32_t M, const uint16_t* act16,
+                    const float* act_scale, float* Y, qmm_stream stream);
+
+/*
+ * Test hook (QMM_W4A8 only): run the GEMV or GEMM kernel of `path` with its
+ * epilogue replaced by a store of the raw group partials
+ *   P[m][n][g] = sum_{k in g} q[n][k] * a[m][k]   (int32, [M][N][G])
+ * (the per-group partials contract of cactus PR #697: partials_out holds raw
+ * dot products, the caller applies the scales).
+ *   path QMM_PATH_GEMV: M must be 1, act = int8 a [K].
+ *   path QMM_PATH_GEMM: act = fp16 a16 [M][K].
+ */
+qmm_status qmm_debug_partials(const qmm_weight_desc* w, const void* packed, int32_t M, int32_t path,
+                              const void* act, int32_t* P, qmm_stream stream);
+
+/* Static text for a status code. */
+const char* qmm_status_string(qmm_status s);
+
+/* The qmm_kernel_id of the last kernel this host thread enqueued (engagement check). */
+int32_t qmm_last_kernel_id(void);
+
+/*
+ * Read and clear the device error word of the current device (synchronises
+ * `stream`). Kernels that give up a bounded wait set it instead of hanging.
+ * Returns QMM_OK, QMM_ERR_TIMEOUT, or QMM_ERR_CUDA; *flags (if non-NULL)
+ * receives the raw word.
+ */
+qmm_status qmm_device_status(qmm_stream stream, int32_t* flags);
+
+/* Enable (1, default) or disable (0) programmatic dependent launch. */
+void qmm_set_pdl(int32_t enable);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMM_H */

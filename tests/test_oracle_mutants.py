@@ -1,0 +1,78 @@
+"""Planted mistakes in copies of the oracle must turn its pins red (no GPU).
+
+Each case copies ``oracle/qmm_oracle.c``, replaces one exact snippet (the
+mistake: a dropped term, a wrong sign or index, a swapped order), compiles the
+copy with gcc into a temporary directory and runs the named pins on it. The
+test passes only when at least one of those pins fails on the mutant. The real
+oracle source is never modified.
+"""
+
+import os
+
+import pytest
+
+import oracle
+from tests import oracle_pins as P
+
+MUTANTS = [
+    ("fwht_sign", "v[i + h] = lo - hi;\n            }\n}\n\n/* The same transform in fp64",
+     "v[i + h] = hi - lo;\n            }\n}\n\n/* The same transform in fp64", [P.pin_hadamard_matrix]),
+    ("fwht_f64_dropped_stage", "for (int h = 1; h < n; h <<= 1)\n        for (int i = 0; i < n; i++)\n            if ((i & h) == 0) {\n                double",
+     "for (int h = 2; h < n; h <<= 1)\n        for (int i = 0; i < n; i++)\n            if ((i & h) == 0) {\n                double",
+     [P.pin_hadamard_matrix, P.pin_rotation_invariance]),
+    ("nibble_high_first", "int u = (k & 1) ? (byte >> 4) : (byte & 0xf);",
+     "int u = (k & 1) ? (byte & 0xf) : (byte >> 4);", [P.pin_nibble_order]),
+    ("nibble_offset_binary", "q[(size_t)n * K + k] = (int8_t)(u >= 8 ? u - 16 : u);",
+     "q[(size_t)n * K + k] = (int8_t)(u - 8);", [P.pin_nibble_order, P.pin_partials_brute_force]),
+    ("round_ties_away", "float r = rintf(v[i] / s);", "float r = roundf(v[i] / s);", [P.pin_quant_fixture]),
+    ("scale_128", "float s = amax / 127.0f;", "float s = amax / 128.0f;",
+     [P.pin_quant_fixture, P.pin_quant_properties]),
+    ("missing_rotation_factor", "sx[(size_t)m * G + g] = s * c;", "sx[(size_t)m * G + g] = s;",
+     [P.pin_quant_fixture, P.pin_rotated_quant_exact, P.pin_quantized_rotation_end_to_end]),
+    ("zero_group_scale", "sx[(size_t)m * G + g] = 0.0f;", "sx[(size_t)m * G + g] = 1.0f;",
+     [P.pin_quant_fixture, P.pin_quant_properties]),
+    ("partials_group_offset", "acc += (int64_t)q[(size_t)n * K + k] * a[(size_t)m * K + k];",
+     "acc += (int64_t)q[(size_t)n * K + k] * a[(size_t)m * K + kl];", [P.pin_partials_brute_force]),
+    ("gemm_scale_index", "double t = oracle_f16_to_f64(sw[(size_t)n * G + g]) * (double)sx[(size_t)m * G + g] * (double)p;",
+     "double t = oracle_f16_to_f64(sw[(size_t)n * G + g]) * (double)sx[(size_t)m * G] * (double)p;",
+     [P.pin_gemm_w4a8_dequant]),
+    ("gemm_transposed_weight", "p += (int64_t)qrow[k] * a[(size_t)m * K + k];",
+     "p += (int64_t)qrow[K - 1 - k] * a[(size_t)m * K + k];", [P.pin_gemm_w4a8_dequant]),
+    ("tree_pairing", "S[(size_t)m * G + g] = ((c[0] + c[1]) + (c[2] + c[3])) + ((c[4] + c[5]) + (c[6] + c[7]));",
+     "S[(size_t)m * G + g] = ((c[0] + c[2]) + (c[1] + c[3])) + ((c[4] + c[6]) + (c[5] + c[7]));",
+     [P.pin_group_sum_tree_fixture]),
+    ("tree_flat", "S[(size_t)m * G + g] = ((c[0] + c[1]) + (c[2] + c[3])) + ((c[4] + c[5]) + (c[6] + c[7]));",
+     "S[(size_t)m * G + g] = (((((((c[0] + c[1]) + c[2]) + c[3]) + c[4]) + c[5]) + c[6]) + c[7]);",
+     [P.pin_group_sum_tree_fixture]),
+    ("chunk_right_to_left", "for (int i = 1; i < 8; i++) acc = acc + xg[8 * j + i];",
+     "acc = xg[8 * j + 7]; for (int i = 6; i >= 0; i--) acc = acc + xg[8 * j + i];",
+     [P.pin_group_sum_tree_fixture]),
+    ("affine_bias_dropped", "y += sv * qx + bv * sumx;", "y += sv * qx;", [P.pin_affine_dequant_and_bias]),
+    ("pack_natural_slots", "int s = (e % 2 == 0) ? e / 2 : 4 + e / 2;", "int s = e;", [P.pin_pack_positions]),
+    ("pack_no_offset", "int u = variant == ORACLE_W4A8 ? q + 8 : q;", "int u = q;",
+     [P.pin_pack_positions, P.pin_pack_roundtrip_and_invariance]),
+    ("pack_piece_stride", "return (size_t)p * 2048 + (size_t)r * 16 + 4 * j + s / 2;",
+     "return (size_t)p * 16 + (size_t)r * 32 + 4 * j + s / 2;", [P.pin_pack_positions]),
+    ("f16_exponent", "v = ldexp((double)(1024 + f), e - 25);", "v = ldexp((double)(1024 + f), e - 24);",
+     [P.pin_f16_to_f64]),
+    ("f16_round_truncate", "double q = rint(ldexp(a, 10 - E));", "double q = floor(ldexp(a, 10 - E));",
+     [P.pin_f64_to_f16]),
+]
+
+
+@pytest.mark.parametrize("name,old,new,pins", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_planted_mistake_is_caught(name, old, new, pins, tmp_path):
+    src = open(oracle.SRC).read()
+    assert src.count(old) == 1, f"snippet for {name} not found exactly once"
+    mutant_c = tmp_path / "qmm_oracle.c"
+    mutant_c.write_text(src.replace(old, new))
+    lib = oracle.compile_source(str(mutant_c), str(tmp_path / "libmutant.so"))
+    orc = oracle.Oracle(lib)
+    failures = 0
+    for pin in pins:
+        try:
+            pin(orc)
+        except (AssertionError, ValueError):
+            failures += 1
+    assert failures > 0, f"planted mistake {name} passed every pin"
+    assert os.path.getsize(oracle.SRC) == len(src.encode())
