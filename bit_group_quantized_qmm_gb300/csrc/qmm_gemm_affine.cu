@@ -1,0 +1,19 @@
+// qmm_gemm_affine.cu -- instances of the tensor-core GEMM for the affine
+// variant (group 64; weight operand in tensor or shared memory).
+#include "qmm_gemm.cuh"
+
+namespace qmm {
+
+cudaError_t launch_gemm_affine(const LaunchCtx& c, const CUtensorMap& map, const GemmShape& sh,
+                               const uint8_t* blob, const float* gsum, float* Y, bool a_in_smem)
+{
+    const bool narrow = sh.m_tile / 2 <= 32;
+    if (a_in_smem) {
+        if (narrow) return run_gemm<1, 64, false, false, 32>(c, map, sh, blob, gsum, Y, nullptr);
+        return run_gemm<1, 64, false, false, 112>(c, map, sh, blob, gsum, Y, nullptr);
+    }
+    if (narrow) return run_gemm<1, 64, true, false, 32>(c, map, sh, blob, gsum, Y, nullptr);
+    return run_gemm<1, 64, true, false, 112>(c, map, sh, blob, gsum, Y, nullptr);
+}
+
+}  // namespace qmm

@@ -1,0 +1,33 @@
+// qmm_gemm_w4a8.cu -- instances of the tensor-core GEMM for the symmetric
+// W4A8 variant (group 64 and 128, weight operand in tensor or shared memory,
+// result or raw-partials epilogue).
+#include "qmm_gemm.cuh"
+
+namespace qmm {
+
+template <int GROUP>
+static cudaError_t dispatch(const LaunchCtx& c, const CUtensorMap& map, const GemmShape& sh, const uint8_t* blob,
+                            const float* sx, float* Y, int32_t* P, bool a_in_smem)
+{
+    const bool narrow = sh.m_tile / 2 <= 32;
+    if (P) {
+        if (a_in_smem) return run_gemm<0, GROUP, false, true, 112>(c, map, sh, blob, sx, Y, P);
+        return run_gemm<0, GROUP, true, true, 112>(c, map, sh, blob, sx, Y, P);
+    }
+    if (a_in_smem) {
+        if (narrow) return run_gemm<0, GROUP, false, false, 32>(c, map, sh, blob, sx, Y, P);
+        return run_gemm<0, GROUP, false, false, 112>(c, map, sh, blob, sx, Y, P);
+    }
+    if (narrow) return run_gemm<0, GROUP, true, false, 32>(c, map, sh, blob, sx, Y, P);
+    return run_gemm<0, GROUP, true, false, 112>(c, map, sh, blob, sx, Y, P);
+}
+
+cudaError_t launch_gemm_w4a8(const LaunchCtx& c, int group, const CUtensorMap& map, const GemmShape& sh,
+                             const uint8_t* blob, const float* sx, float* Y, int32_t* P, bool a_in_smem)
+{
+    if (group == 64) return dispatch<64>(c, map, sh, blob, sx, Y, P, a_in_smem);
+    if (group == 128) return dispatch<128>(c, map, sh, blob, sx, Y, P, a_in_smem);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace qmm

@@ -1,0 +1,73 @@
+// qmm_internal.h -- launchers shared between the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <utility>
+
+namespace qmm {
+
+struct LaunchCtx {
+    cudaStream_t stream;
+    bool pdl;         // launch with programmatic stream serialization
+    int num_sms;
+    int* status;      // device error word
+};
+
+// Launch `kern` on the context's stream, with programmatic dependent launch
+// when enabled.
+template <typename... Params, typename... Args>
+cudaError_t launch(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, const LaunchCtx& c,
+                   Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = c.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = c.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+cudaError_t launch_pack(const LaunchCtx& c, int variant, int N, int K, int group, const uint8_t* q,
+                        const uint16_t* scales, const uint16_t* biases, uint8_t* blob);
+
+cudaError_t launch_prep_w4a8(const LaunchCtx& c, int M, int K, int group, int hadamard, const void* x, int x_dtype,
+                             int8_t* a, uint16_t* a16, float* sx, int32_t* asum);
+
+cudaError_t launch_prep_affine(const LaunchCtx& c, int M, int K, const void* x, int x_dtype, float* gsum,
+                               uint16_t* x16);
+
+// Number of K-slices the GEMV splits a weight into (1 = no split).
+int gemv_ksplit(int N, int K, int group);
+size_t gemv_workspace_bytes(int N, int K, int group);
+
+// y = W a (M = 1). P_debug != nullptr: write raw group partials instead.
+cudaError_t launch_gemv(const LaunchCtx& c, int N, int K, int group, const uint8_t* blob, const int8_t* a,
+                        const float* sx, float* y, int32_t* P_debug, void* ws, size_t ws_bytes);
+
+// Largest activation-row tile of the tensor-core GEMM (MMA N).
+constexpr int kMaxMTile = 224;
+
+struct GemmShape {
+    int M, N, K;
+    int m_tile;      // activation rows per tile (MMA N), multiple of 16, <= 224
+    int mt_count;    // ceil(M / m_tile)
+    int num_tiles;   // row tiles x mt_count
+    int d_stride;    // tensor-memory columns per accumulator buffer
+    int tmem_cols;   // allocated tensor-memory columns (power of two)
+};
+
+cudaError_t launch_gemm_w4a8(const LaunchCtx& c, int group, const CUtensorMap& map, const GemmShape& sh,
+                             const uint8_t* blob, const float* sx, float* Y, int32_t* P, bool a_in_smem);
+cudaError_t launch_gemm_affine(const LaunchCtx& c, const CUtensorMap& map, const GemmShape& sh,
+                               const uint8_t* blob, const float* gsum, float* Y, bool a_in_smem);
+
+}  // namespace qmm

@@ -197,8 +197,9 @@ size_t qmm_gemv_workspace_size(const qmm_weight_desc* w);
  *   sx         device fp32 [G]
  *   y          device fp32 [N]
  *   workspace  device, >= qmm_gemv_workspace_size(w) bytes, or NULL to run
- *              without split-K (fewer CTAs; same result bits).
- * Results are deterministic: a fixed reduction order, no atomics on data.
+ *              without split-K (fewer CTAs; the fp32 sum order differs).
+ * Results are deterministic for a given shape and workspace choice: a fixed
+ * reduction order, no atomics on data.
  */
 qmm_status qmm_gemv(const qmm_weight_desc* w, const void* packed, const int8_t* a, const float* sx,
                     float* y, void* workspace, size_t workspace_bytes, qmm_stream stream);
@@ -245,8 +246,15 @@ int32_t qmm_last_kernel_id(void);
  */
 qmm_status qmm_device_status(qmm_stream stream, int32_t* flags);
 
-/* Enable (1, default) or disable (0) programmatic dependent launch. */
+/* Enable (1, default) or disable (0) programmatic dependent launch for
+ * launches made after the call (process-wide). */
 void qmm_set_pdl(int32_t enable);
+
+/* Where qmm_gemm expands the 4-bit weights for the tensor cores (process-wide,
+ * launches after the call): 0 (default) into tensor memory, read by
+ * tcgen05.mma as its A operand; 1 into 128-byte-swizzled shared memory. Both
+ * give the same partials; the choice only moves on-chip traffic. */
+void qmm_set_gemm_weight_operand(int32_t in_shared_memory);
 
 #ifdef __cplusplus
 }

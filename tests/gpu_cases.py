@@ -1,0 +1,108 @@
+"""Helpers of the GPU parity tests: run one path of the library on cuda:0 and
+return numpy results, with the inputs drawn by qmm_synth."""
+
+from __future__ import annotations
+
+import numpy as np
+
+import qmm_synth
+
+W4A8, AFFINE = 0, 1
+
+
+def lib():
+    import bit_group_quantized_qmm_gb300 as q
+    return q
+
+
+def dev():
+    import torch
+    return torch.device("cuda:0")
+
+
+def t(a):
+    import torch
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev())
+
+
+def pack(variant, N, K, group, q_bytes, scales, biases=None):
+    import torch
+    q = lib()
+    d = q.weight_desc(variant, N, K, group)
+    packed = torch.empty(q.qmm_packed_size(d), dtype=torch.uint8, device=dev())
+    q.qmm_pack_weights(d, t(q_bytes), t(scales), None if biases is None else t(biases), packed)
+    assert q.qmm_last_kernel_id() == 1
+    return d, packed
+
+
+def prep_w4a8(x, group, hadamard, x_dtype=0):
+    """x: float32 [M][K] numpy (converted to x_dtype on the device)."""
+    import torch
+    q = lib()
+    M, K = x.shape
+    G = K // group
+    xt = t(x.astype(np.float32))
+    if x_dtype == 1:
+        xt = xt.to(torch.float16)
+    elif x_dtype == 2:
+        xt = xt.to(torch.bfloat16)
+    a = torch.empty((M, K), dtype=torch.int8, device=dev())
+    a16 = torch.empty((M, K), dtype=torch.float16, device=dev())
+    sx = torch.empty((M, G), dtype=torch.float32, device=dev())
+    asum = torch.empty((M, G), dtype=torch.int32, device=dev())
+    q.qmm_prep_act(W4A8, M, K, group, hadamard, xt, x_dtype, a=a, a16=a16, sx=sx, asum=asum)
+    assert q.qmm_last_kernel_id() == 2
+    return a, a16, sx, asum, xt
+
+
+def gemv(d, packed, a, sx, workspace=True):
+    import torch
+    q = lib()
+    y = torch.full((d.N,), float("nan"), dtype=torch.float32, device=dev())
+    ws = None
+    if workspace:
+        nbytes = q.qmm_gemv_workspace_size(d)
+        if nbytes:
+            ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev())
+    q.qmm_gemv(d, packed, a, sx, y, ws)
+    assert q.qmm_last_kernel_id() == 4
+    return y
+
+
+def gemm(d, packed, M, act16, act_scale):
+    import torch
+    q = lib()
+    Y = torch.full((M, d.N), float("nan"), dtype=torch.float32, device=dev())
+    q.qmm_gemm(d, packed, M, act16, act_scale, Y)
+    assert q.qmm_last_kernel_id() == (5 if d.variant == W4A8 else 6)
+    return Y
+
+
+def partials(d, packed, M, path, act):
+    import torch
+    q = lib()
+    G = d.K // d.group
+    P = torch.full((M, d.N, G), -2**31, dtype=torch.int32, device=dev())
+    q.qmm_debug_partials(d, packed, M, path, act, P)
+    return P
+
+
+def w4a8_case(seed, name, N, K, group, hadamard, M, outlier_frac=0.0):
+    lay = qmm_synth.Layer(name, W4A8, N, K, group, hadamard, outlier_frac=outlier_frac)
+    qb, sw, _ = qmm_synth.layer_weights(seed, name, lay)
+    x = qmm_synth.layer_activations(seed, name, lay, M)
+    return qb, sw, x
+
+
+def within_w4a8(y, Y, Ym):
+    err = np.abs(np.asarray(y, dtype=np.float64) - Y)
+    bound = 1e-5 * Ym + 1e-6
+    return bool(np.all(err <= bound)), float((err / bound).max())
+
+
+def within_affine(y, Y, Ym):
+    err = np.abs(np.asarray(y, dtype=np.float64) - Y)
+    bound = 2e-3 * Ym
+    return bool(np.all(err <= bound)), float((err / np.maximum(bound, 1e-300)).max())

@@ -1,0 +1,97 @@
+"""The C-ABI library on the host (no GPU needed): it builds, loads, exports
+every function include/qmm.h declares, and rejects bad arguments before it
+touches a device."""
+
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import oracle
+
+
+@pytest.fixture(scope="module")
+def q():
+    from bit_group_quantized_qmm_gb300 import build
+    build.build()
+    import bit_group_quantized_qmm_gb300 as q
+    return q
+
+
+def test_exports_every_declared_symbol(q):
+    declared = q.declared_symbols()
+    assert len(declared) >= 12
+    out = subprocess.run(["nm", "-D", "--defined-only", q.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    missing = [s for s in declared if s not in exported]
+    assert not missing, missing
+    for s in declared:
+        assert hasattr(q.library(), s)
+
+
+@pytest.mark.parametrize("variant,N,K,group", [(0, 1024, 1024, 64), (0, 1, 64, 64), (0, 130, 512, 128),
+                                               (1, 34816, 5120, 64), (0, 262144, 1536, 128), (1, 129, 192, 64)])
+def test_packed_size_matches_oracle(q, variant, N, K, group):
+    d = q.weight_desc(variant, N, K, group)
+    assert q.qmm_packed_size(d) == oracle.packed_size(variant, N, K, group)
+
+
+def test_packed_size_rejects(q):
+    assert q.qmm_packed_size(q.weight_desc(0, 128, 100, 64)) == 0     # K % group
+    assert q.qmm_packed_size(q.weight_desc(1, 128, 256, 128)) == 0    # affine group 128
+    assert q.qmm_packed_size(q.weight_desc(0, 0, 256, 64)) == 0
+    assert q.qmm_packed_size(q.weight_desc(5, 128, 256, 64)) == 0
+
+
+def test_host_validation(q):
+    L = q.library()
+    d = q.weight_desc(0, 256, 256, 64)
+    bad = q.weight_desc(0, 256, 250, 64)
+    D = ctypes.byref
+    INV, SHAPE, DEV, MIS = 1, 2, 3, 4
+    A = 1 << 20     # an aligned (never dereferenced) address
+    assert L.qmm_pack_weights(D(d), None, A, None, A, None) == INV
+    assert L.qmm_pack_weights(D(bad), A, A, None, A, None) == SHAPE
+    assert L.qmm_pack_weights(D(d), A + 1, A, None, A, None) == MIS
+    assert L.qmm_pack_weights(D(d), A, A, A, A, None) == INV          # biases for W4A8
+    assert L.qmm_prep_act(0, 0, 256, 64, 0, A, 0, A, A, A, A, None, None, None) == INV
+    assert L.qmm_prep_act(0, 1, 256, 64, 32, A, 0, A, A, A, A, None, None, None) == SHAPE
+    assert L.qmm_prep_act(0, 1, 256, 64, 0, A, 7, A, A, A, A, None, None, None) == INV
+    assert L.qmm_prep_act(0, 1, 256, 64, 0, A, 0, A, A, None, A, None, None, None) == INV   # sx required
+    assert L.qmm_prep_act(1, 1, 256, 64, 0, A, 1, None, None, None, None, None, None, None) == INV  # gsum
+    assert L.qmm_prep_act(1, 1, 256, 128, 0, A, 1, None, None, None, None, A, None, None) == SHAPE
+    assert L.qmm_gemv(D(q.weight_desc(1, 256, 256, 64)), A, A, A, A, None, 0, None) == SHAPE
+    assert L.qmm_gemv(D(d), A, A, A, A + 4, None, 0, None) == MIS
+    assert L.qmm_gemm(D(d), A, 0, A, A, A, None) == INV
+    assert L.qmm_gemm(D(d), A, 4, A, None, A, None) == INV
+    assert L.qmm_debug_partials(D(q.weight_desc(1, 256, 256, 64)), A, 1, 0, A, A, None) == SHAPE
+    assert L.qmm_debug_partials(D(d), A, 2, 0, A, A, None) == INV    # GEMV path needs M == 1
+    assert L.qmm_debug_partials(D(d), A, 1, 9, A, A, None) == INV
+
+
+def test_valid_arguments_reach_the_device_probe(q):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    L = q.library()
+    d = q.weight_desc(0, 256, 256, 64)
+    A = 1 << 20
+    assert L.qmm_pack_weights(ctypes.byref(d), A, A, None, A, None) == 3
+    assert L.qmm_gemm(ctypes.byref(d), A, 4, A, A, A, None) == 3
+
+
+def test_status_strings(q):
+    for s in range(8):
+        assert q.status_string(s) and q.status_string(s) != "unknown status"
+    assert q.status_string(99) == "unknown status"
+
+
+def test_no_cpu_fallback_in_product_path():
+    """The product package never imports the oracle."""
+    pkg = os.path.join(os.path.dirname(os.path.dirname(__file__)), "bit_group_quantized_qmm_gb300")
+    for root, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(root, f)).read()
+                assert "oracle" not in text.lower(), f

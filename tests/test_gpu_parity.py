@@ -1,0 +1,358 @@
+"""GPU parity: the CUDA path against the CPU oracle on the same seeded inputs.
+
+Bit-exact: packed bytes, int8 codes (and their fp16 image), activation
+scales, group sums of the affine prepass, int32 group partials.
+Tolerance: W4A8 fp32 outputs |d| <= 1e-5 * sum_g |sw sx P| + 1e-6;
+affine outputs |d| <= 2e-3 * sum_k |w x|.
+"""
+
+import numpy as np
+import pytest
+
+import qmm_synth
+from tests import gpu_cases as gc
+
+pytestmark = pytest.mark.gpu
+
+W4A8, AFFINE = 0, 1
+GEMV, GEMM = 0, 1
+
+
+@pytest.fixture(scope="module")
+def torch_cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import bit_group_quantized_qmm_gb300  # noqa: F401  (fails loudly when the library is missing)
+    return torch
+
+
+# ------------------------------------------------------------------ pack
+
+PACK_CASES = [
+    (W4A8, 1024, 1024, 64),
+    (W4A8, 200, 192, 64),      # ragged last row tile
+    (W4A8, 130, 512, 128),
+    (W4A8, 1, 64, 64),         # one row, one group
+    (AFFINE, 129, 256, 64),
+    (W4A8, 12288, 1536, 64),   # gate_up
+    (W4A8, 1536, 6144, 64),    # down
+]
+
+
+@pytest.mark.parametrize("variant,N,K,group", PACK_CASES)
+def test_pack_bytes(torch_cuda, orc, variant, N, K, group):
+    lay = qmm_synth.Layer("p", variant, N, K, group, 0)
+    qb, s, b = qmm_synth.layer_weights(1, f"pack/{variant}/{N}/{K}/{group}", lay)
+    _, packed = gc.pack(variant, N, K, group, qb, s, b)
+    ref = orc.pack(variant, N, K, group, qb, s, b)
+    assert np.array_equal(packed.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("variant,N,K,group", [(W4A8, 262144, 1536, 128), (AFFINE, 34816, 5120, 64)])
+def test_pack_bytes_full_size_sampled(torch_cuda, orc, variant, N, K, group):
+    """Full-size weights: the oracle packs row tiles 0, 1, a middle one and the
+    last; the GPU blob's chunks of those tiles must match byte for byte."""
+    lay = qmm_synth.Layer("p", variant, N, K, group, 0)
+    qb, s, b = qmm_synth.layer_weights(0, "full/pack", lay)
+    _, packed = gc.pack(variant, N, K, group, qb, s, b)
+    blob = packed.cpu().numpy()
+    G = K // group
+    CB = 64 * group + 256 + (256 if variant == AFFINE else 0)
+    T = (N + 127) // 128
+    for t0 in (0, 1, T // 2, T - 1):
+        rows = slice(128 * t0, min(N, 128 * (t0 + 1)))
+        ref = orc.pack(variant, rows.stop - rows.start, K, group, qb[rows], s[rows],
+                       None if b is None else b[rows])
+        assert np.array_equal(blob[t0 * G * CB:(t0 + 1) * G * CB], ref), t0
+
+
+def test_pack_control_nibble_order_is_detected(torch_cuda, orc):
+    """Control: a blob built with the nibble halves swapped differs from the
+    GPU's (the byte comparison is sensitive to the order)."""
+    N, K, g = 256, 256, 64
+    lay = qmm_synth.Layer("p", W4A8, N, K, g, 0)
+    qb, s, _ = qmm_synth.layer_weights(2, "pack/control", lay)
+    _, packed = gc.pack(W4A8, N, K, g, qb, s)
+    swapped = ((qb & 0xF) << 4) | (qb >> 4)
+    assert not np.array_equal(packed.cpu().numpy(), orc.pack(W4A8, N, K, g, swapped, s))
+
+
+# ------------------------------------------------------------------ W4A8 prep
+
+PREP_CASES = [
+    (1, 1536, 64, 64, 0.01),
+    (7, 256, 64, 0, 0.0),
+    (5, 512, 128, 128, 0.01),
+    (65, 1536, 64, 64, 0.0),
+    (1068, 1536, 64, 64, 0.0),
+    (32, 1536, 128, 128, 0.0),
+]
+
+
+def _prep_input(x, x_dtype):
+    """(device-side input tensor on CPU, float32 values the oracle sees)."""
+    import torch
+    xt = torch.from_numpy(x)
+    if x_dtype == 1:
+        xt = xt.to(torch.float16)
+    elif x_dtype == 2:
+        xt = xt.to(torch.bfloat16)
+    return xt, xt.float().numpy()
+
+
+@pytest.mark.parametrize("M,K,group,had,outl", PREP_CASES)
+@pytest.mark.parametrize("x_dtype", [0, 1, 2])
+def test_prep_w4a8_bit_exact(torch_cuda, orc, M, K, group, had, outl, x_dtype):
+    if x_dtype and M > 65:
+        pytest.skip("dtype variants on the small shapes only")
+    x = qmm_synth.activations_f32(3, f"prep/{M}/{K}", M, K, outlier_frac=outl)
+    x[0, :group] = 0.0     # an all-zero group
+    xin, xval = _prep_input(x, x_dtype)
+    q = gc.lib()
+    G = K // group
+    dev = gc.dev()
+    xt = xin.to(dev)
+    a = torch_cuda.empty((M, K), dtype=torch_cuda.int8, device=dev)
+    a16 = torch_cuda.empty((M, K), dtype=torch_cuda.float16, device=dev)
+    sx = torch_cuda.empty((M, G), dtype=torch_cuda.float32, device=dev)
+    asum = torch_cuda.empty((M, G), dtype=torch_cuda.int32, device=dev)
+    q.qmm_prep_act(W4A8, M, K, group, had, xt, x_dtype, a=a, a16=a16, sx=sx, asum=asum)
+    ra, rsx, rsum = orc.prep_w4a8(xval, group, had)
+    assert np.array_equal(a.cpu().numpy(), ra)
+    assert np.array_equal(a16.cpu().numpy(), ra.astype(np.float16))
+    assert np.array_equal(sx.cpu().numpy().view(np.uint32), rsx.view(np.uint32))
+    assert np.array_equal(asum.cpu().numpy(), rsum)
+
+
+def test_prep_control_rotation_is_detected(torch_cuda, orc):
+    """Control: codes of the rotated prepass differ from unrotated ones."""
+    x = qmm_synth.activations_f32(4, "prep/control", 4, 512)
+    a, _, _, _, _ = gc.prep_w4a8(x, 64, 64)
+    ra, _, _ = orc.prep_w4a8(x, 64, 0)
+    assert not np.array_equal(a.cpu().numpy(), ra)
+
+
+# ------------------------------------------------------------------ affine prep
+
+@pytest.mark.parametrize("M,K,x_dtype", [(1, 64, 1), (65, 5120, 1), (3, 640, 0), (9, 192, 2), (128, 5120, 1)])
+def test_prep_affine_group_sums_bit_exact(torch_cuda, orc, M, K, x_dtype):
+    import torch
+    q = gc.lib()
+    dev = gc.dev()
+    x = qmm_synth.normal(5, f"aff/{M}/{K}", M * K).astype(np.float32).reshape(M, K)
+    xin, xval = _prep_input(x, x_dtype)
+    G = K // 64
+    S = torch.empty((M, G), dtype=torch.float32, device=dev)
+    x16 = torch.empty((M, K), dtype=torch.float16, device=dev) if x_dtype != 1 else None
+    q.qmm_prep_act(AFFINE, M, K, 64, 0, xin.to(dev), x_dtype, gsum=S, x16=x16)
+    assert q.qmm_last_kernel_id() == 3
+    ref = orc.group_sums_affine(xval)
+    assert np.array_equal(S.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    if x16 is not None:
+        assert np.array_equal(x16.cpu().numpy().view(np.uint16), xval.astype(np.float16).view(np.uint16))
+
+
+def test_prep_affine_tree_fixture(torch_cuda):
+    """The page's summation tree on the GPU, on the hand-worked fixture."""
+    import torch
+    from tests import oracle_pins
+    q = gc.lib()
+    cases = oracle_pins.read_cases("group_sum_tree.txt")
+    x = np.array([c["chunk"] for c in cases], dtype=np.float32).reshape(len(cases), 64)
+    S = torch.empty((len(cases), 1), dtype=torch.float32, device=gc.dev())
+    q.qmm_prep_act(AFFINE, len(cases), 64, 64, 0, torch.from_numpy(x).to(gc.dev()), 0, gsum=S)
+    expect = np.array([float(c["expect"]) for c in cases], dtype=np.float32)
+    assert np.array_equal(S.cpu().numpy()[:, 0], expect)
+
+
+# ------------------------------------------------------------------ GEMV
+
+GEMV_CASES = [
+    (1024, 1024, 64, 0, 0.0),     # the K = N = 1024 GEMV
+    (200, 192, 64, 64, 0.0),      # ragged rows
+    (256, 512, 128, 128, 0.0),
+    (128, 64, 64, 0, 0.0),        # one group
+    (12288, 1536, 64, 64, 0.01),  # gate_up
+    (1536, 6144, 64, 64, 0.01),   # down
+    (2048, 1536, 64, 64, 0.01),   # q
+    (1536, 2048, 64, 64, 0.01),   # o
+]
+
+
+@pytest.mark.parametrize("N,K,group,had,outl", GEMV_CASES)
+def test_gemv_partials_bit_exact(torch_cuda, orc, N, K, group, had, outl):
+    qb, sw, x = gc.w4a8_case(6, f"gemv/{N}/{K}", N, K, group, had, 1, outl)
+    d, packed = gc.pack(W4A8, N, K, group, qb, sw)
+    a, _, sx, _, _ = gc.prep_w4a8(x, group, had)
+    P = gc.partials(d, packed, 1, GEMV, a)
+    ra, _, _ = orc.prep_w4a8(x, group, had)
+    assert np.array_equal(P.cpu().numpy(), orc.partials_w4a8(qb, ra, group))
+
+
+@pytest.mark.parametrize("N,K,group,had,outl", GEMV_CASES)
+@pytest.mark.parametrize("workspace", [True, False])
+def test_gemv_output(torch_cuda, orc, N, K, group, had, outl, workspace):
+    qb, sw, x = gc.w4a8_case(7, f"gemv/{N}/{K}", N, K, group, had, 1, outl)
+    d, packed = gc.pack(W4A8, N, K, group, qb, sw)
+    a, _, sx, _, _ = gc.prep_w4a8(x, group, had)
+    y1 = gc.gemv(d, packed, a, sx, workspace).cpu().numpy()
+    y2 = gc.gemv(d, packed, a, sx, workspace).cpu().numpy()
+    assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32)), "not deterministic"
+    ra, rsx, _ = orc.prep_w4a8(x, group, had)
+    Y, Ym = orc.gemm_w4a8(qb, sw, ra, rsx, group)
+    ok, worst = gc.within_w4a8(y1[None, :], Y, Ym)
+    assert ok, f"worst error / bound = {worst}"
+
+
+# ------------------------------------------------------------------ GEMM
+
+GEMM_CASES = [
+    (1, 256, 256, 64, 64),
+    (16, 256, 512, 64, 64),
+    (17, 200, 192, 64, 0),       # ragged rows and columns
+    (65, 384, 1024, 64, 64),
+    (130, 128, 256, 128, 128),
+    (240, 256, 512, 64, 64),     # two activation tiles
+    (32, 512, 1536, 128, 128),
+]
+
+
+@pytest.mark.parametrize("M,N,K,group,had", GEMM_CASES)
+@pytest.mark.parametrize("operand_in_smem", [False, True])
+def test_gemm_partials_bit_exact(torch_cuda, orc, M, N, K, group, had, operand_in_smem):
+    q = gc.lib()
+    qb, sw, x = gc.w4a8_case(8, f"gemm/{M}/{N}/{K}", N, K, group, had, M)
+    d, packed = gc.pack(W4A8, N, K, group, qb, sw)
+    _, a16, sx, _, _ = gc.prep_w4a8(x, group, had)
+    q.qmm_set_gemm_weight_operand(operand_in_smem)
+    try:
+        P = gc.partials(d, packed, M, GEMM, a16)
+    finally:
+        q.qmm_set_gemm_weight_operand(False)
+    ra, _, _ = orc.prep_w4a8(x, group, had)
+    assert np.array_equal(P.cpu().numpy(), orc.partials_w4a8(qb, ra, group))
+
+
+@pytest.mark.parametrize("M,N,K,group,had", GEMM_CASES)
+@pytest.mark.parametrize("operand_in_smem", [False, True])
+def test_gemm_output(torch_cuda, orc, M, N, K, group, had, operand_in_smem):
+    q = gc.lib()
+    qb, sw, x = gc.w4a8_case(9, f"gemm/{M}/{N}/{K}", N, K, group, had, M)
+    d, packed = gc.pack(W4A8, N, K, group, qb, sw)
+    _, a16, sx, _, _ = gc.prep_w4a8(x, group, had)
+    q.qmm_set_gemm_weight_operand(operand_in_smem)
+    try:
+        Yg = gc.gemm(d, packed, M, a16, sx).cpu().numpy()
+    finally:
+        q.qmm_set_gemm_weight_operand(False)
+    ra, rsx, _ = orc.prep_w4a8(x, group, had)
+    Y, Ym = orc.gemm_w4a8(qb, sw, ra, rsx, group)
+    ok, worst = gc.within_w4a8(Yg, Y, Ym)
+    assert ok, f"worst error / bound = {worst}"
+
+
+def _sample_rows(N, n=48):
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, N - 1], np.linspace(0, N - 1, n).astype(np.int64)]))
+    return rows.astype(np.int32)
+
+
+@pytest.mark.parametrize("M", [16, 64, 128, 512, 1068])
+def test_gemm_prefill_full_size_sampled(torch_cuda, orc, M):
+    """K=1536, N=12288, group 64, Hadamard-64: every row m on sampled columns n."""
+    N, K, g = 12288, 1536, 64
+    qb, sw, x = gc.w4a8_case(0, "prefill_gemm", N, K, g, g, M)
+    d, packed = gc.pack(W4A8, N, K, g, qb, sw)
+    _, a16, sx, _, _ = gc.prep_w4a8(x, g, g)
+    Yg = gc.gemm(d, packed, M, a16, sx).cpu().numpy()
+    assert not np.isnan(Yg).any()
+    ra, rsx, _ = orc.prep_w4a8(x, g, g)
+    rows = _sample_rows(N)
+    Y, Ym = orc.gemm_w4a8(qb, sw, ra, rsx, g, rows=rows)
+    ok, worst = gc.within_w4a8(Yg[:, rows], Y, Ym)
+    assert ok, f"worst error / bound = {worst}"
+
+
+@pytest.fixture(scope="module")
+def lm_head(torch_cuda):
+    N, K, g = 262144, 1536, 128
+    lay = qmm_synth.Layer("lm_head", W4A8, N, K, g, g)
+    qb, sw, _ = qmm_synth.layer_weights(0, "lm_head", lay)
+    d, packed = gc.pack(W4A8, N, K, g, qb, sw)
+    return lay, qb, sw, d, packed
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16, 32])
+def test_lm_head_full_size_sampled(lm_head, orc, M):
+    lay, qb, sw, d, packed = lm_head
+    g = lay.group
+    x = qmm_synth.layer_activations(0, f"lm_head/x{M}", lay, M)
+    a, a16, sx, _, _ = gc.prep_w4a8(x, g, g)
+    Yg = gc.gemm(d, packed, M, a16, sx).cpu().numpy()
+    ra, rsx, _ = orc.prep_w4a8(x, g, g)
+    rows = _sample_rows(lay.N)
+    Y, Ym = orc.gemm_w4a8(qb, sw, ra, rsx, g, rows=rows)
+    ok, worst = gc.within_w4a8(Yg[:, rows], Y, Ym)
+    assert ok, f"GEMM worst error / bound = {worst}"
+    if M == 1:
+        y = gc.gemv(d, packed, a, sx).cpu().numpy()
+        ok, worst = gc.within_w4a8(y[None, rows], Y, Ym)
+        assert ok, f"GEMV worst error / bound = {worst}"
+
+
+# ------------------------------------------------------------------ affine GEMM
+
+AFF_CASES = [(1, 128, 64), (33, 256, 256), (65, 200, 320), (128, 384, 1024), (240, 128, 512)]
+
+
+def _affine_run(M, N, K, seed, name, zero_sums=False):
+    import torch
+    q = gc.lib()
+    lay = qmm_synth.Layer(name, AFFINE, N, K, 64, 0)
+    qb, s, b = qmm_synth.layer_weights(seed, name, lay)
+    x16 = qmm_synth.layer_activations(seed, name, lay, M)
+    d, packed = gc.pack(AFFINE, N, K, 64, qb, s, b)
+    xt = gc.t(x16).view(torch.float16)
+    S = torch.empty((M, K // 64), dtype=torch.float32, device=gc.dev())
+    q.qmm_prep_act(AFFINE, M, K, 64, 0, xt, 1, gsum=S)
+    if zero_sums:
+        S.zero_()
+    Yg = gc.gemm(d, packed, M, xt, S).cpu().numpy()
+    return qb, s, b, x16, Yg
+
+
+@pytest.mark.parametrize("M,N,K", AFF_CASES)
+@pytest.mark.parametrize("operand_in_smem", [False, True])
+def test_affine_gemm_output(torch_cuda, orc, M, N, K, operand_in_smem):
+    q = gc.lib()
+    q.qmm_set_gemm_weight_operand(operand_in_smem)
+    try:
+        qb, s, b, x16, Yg = _affine_run(M, N, K, 10, f"aff/{M}/{N}/{K}")
+    finally:
+        q.qmm_set_gemm_weight_operand(False)
+    Y, Ym = orc.gemm_affine(qb, s, b, x16)
+    ok, worst = gc.within_affine(Yg, Y, Ym)
+    assert ok, f"worst error / bound = {worst}"
+
+
+def test_affine_control_zero_sums_is_detected(torch_cuda, orc):
+    """Control: leaving the prepass's group sums at zero must break the tolerance."""
+    qb, s, b, x16, Yg = _affine_run(33, 256, 256, 11, "aff/control", zero_sums=True)
+    Y, Ym = orc.gemm_affine(qb, s, b, x16)
+    ok, _ = gc.within_affine(Yg, Y, Ym)
+    assert not ok
+
+
+@pytest.mark.parametrize("M", [64, 65, 128])
+def test_affine_full_size_sampled(torch_cuda, orc, M):
+    """K=5120, N=34816 (fused gate_up): every row m on sampled columns n."""
+    N, K = 34816, 5120
+    qb, s, b, x16, Yg = _affine_run(M, N, K, 0, "affine_gemm")
+    rows = _sample_rows(N)
+    Y, Ym = orc.gemm_affine(qb, s, b, x16, rows=rows)
+    ok, worst = gc.within_affine(Yg[:, rows], Y, Ym)
+    assert ok, f"worst error / bound = {worst}"
+
+
+def test_device_status_clean(torch_cuda):
+    assert gc.lib().qmm_device_status() == 0
