@@ -13,8 +13,8 @@ import oracle
 
 @pytest.fixture(scope="module")
 def q():
-    from bit_group_quantized_qmm_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__._build_module().build()
     import bit_group_quantized_qmm_gb300 as q
     return q
 
