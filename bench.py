@@ -1,0 +1,614 @@
+#!/usr/bin/env python3
+"""Benchmark of the group-quantized 4-bit matmul library on GB300.
+
+Headline workload (one line of JSON on rank 0): the M = 1 decode projections of
+a Gemma-shaped decoder (gate_up 1536->12288, down 6144->1536, q 1536->2048,
+o 2048->1536), W4A8 with group 64, 64-wide Hadamard rotation of the
+activations, x ~ N(0,1) with 1% +-20 outliers. One step is one decode pass
+over LAYERS layers with their own weights: for each projection the activation
+prepass and the GEMV. The metric is weight+scale bytes streamed per second.
+The per-step weights (> 2x L2) are larger than L2, so no flush is needed.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--no-sweep]
+
+The step is captured once in a CUDA graph (the kernels are launched with
+programmatic dependent launch, so each GEMV streams its weights while the
+previous kernel drains) and replayed K times between CUDA events. Under
+torchrun each rank runs its own replica (weak scaling); the time is the max
+over ranks. ``--impl reference`` times the CPU oracle on the host instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import qmm_synth  # noqa: E402
+
+LAYERS = 32
+PROJ = [("gate_up", 12288, 1536), ("down", 1536, 6144), ("q", 2048, 1536), ("o", 1536, 2048)]
+GROUP = 64
+W4A8, AFFINE = 0, 1
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "gemv_w4a8_gemma_decode.txt")
+GEMV_SOURCE = os.path.join(ROOT, "bit_group_quantized_qmm_gb300", "csrc", "qmm_gemv.cu")
+
+
+# ------------------------------------------------------------------ plumbing
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--layers", type=int, default=LAYERS)
+    p.add_argument("--no-sweep", action="store_true", help="skip the other workloads' extra figures")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world, use_cuda):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend="nccl" if use_cuda else "gloo")
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Largest value of x over all ranks (x itself when world == 1)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 100 ms while running."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        rows = []
+        if self.path and os.path.exists(self.path):
+            with open(self.path) as f:
+                for ln in f:
+                    parts = [p.strip() for p in ln.split(",")]
+                    if len(parts) >= 10:
+                        rows.append(parts)
+            os.unlink(self.path)
+        return rows
+
+    @staticmethod
+    def summarize(rows):
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        smax = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for name, val in zip(names, r[6:10]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        power = [float(r[4]) for r in rows if r[4].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_median": statistics.median(power) if power else None}
+
+
+# ------------------------------------------------------------------ workload
+
+def layer_inputs(seed, rank, layer, name, N, K):
+    prefix = f"gemma_decode/r{rank}/l{layer}/{name}"
+    lay = qmm_synth.Layer(name, W4A8, N, K, GROUP, GROUP, outlier_frac=0.01)
+    qb, sw, _ = qmm_synth.layer_weights(seed, prefix, lay)
+    x = qmm_synth.layer_activations(seed, prefix, lay, 1)
+    return lay, qb, sw, x
+
+
+class DecodeModel:
+    """Packed weights and per-projection buffers of LAYERS decoder layers."""
+
+    def __init__(self, layers, rank, keep_host=False):
+        import torch
+        import bit_group_quantized_qmm_gb300 as q
+        self.q = q
+        dev = torch.device("cuda", torch.cuda.current_device())
+        self.projs = []
+        self.host = []
+        xs, ys = [], []
+        x_off = y_off = 0
+        for l in range(layers):
+            for name, N, K in PROJ:
+                lay, qb, sw, x = layer_inputs(0, rank, l, name, N, K)
+                d = q.weight_desc(W4A8, N, K, GROUP)
+                packed = torch.empty(q.qmm_packed_size(d), dtype=torch.uint8, device=dev)
+                q.qmm_pack_weights(d, torch.from_numpy(qb).to(dev), torch.from_numpy(sw.view(np.int16)).to(dev),
+                                   None, packed)
+                self.projs.append(dict(name=name, N=N, K=K, d=d, packed=packed, x_off=x_off, y_off=y_off))
+                if keep_host:
+                    self.host.append((qb, sw, x))
+                xs.append(x.reshape(-1))
+                x_off += K
+                y_off += N
+        torch.cuda.synchronize()
+        self.x_host = torch.from_numpy(np.concatenate(xs)).pin_memory()
+        self.x = self.x_host.to(dev)
+        self.y = torch.zeros(y_off, dtype=torch.float32, device=dev)
+        self.y_host = torch.empty(y_off, dtype=torch.float32).pin_memory()
+        kmax = max(K for _, _, K in PROJ)
+        self.a = [torch.empty(K, dtype=torch.int8, device=dev) for _, _, K in PROJ]
+        self.sx = [torch.empty(K // GROUP, dtype=torch.float32, device=dev) for _, _, K in PROJ]
+        ws_bytes = max(q.qmm_gemv_workspace_size(p["d"]) for p in self.projs)
+        self.ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+        self.ws_bytes = ws_bytes
+        self.kmax = kmax
+        # bytes
+        self.weight_bytes = sum(q.qmm_packed_size(p["d"]) for p in self.projs)
+        self.act_bytes = sum(p["K"] * 1 + (p["K"] // GROUP) * 4 + p["N"] * 4 for p in self.projs)
+        self.h2d_bytes = self.x.numel() * 4
+        self.d2h_bytes = self.y.numel() * 4
+
+    def enqueue_step(self):
+        """One decode pass: prepass + GEMV for every projection of every layer."""
+        q = self.q
+        for i, p in enumerate(self.projs):
+            j = i % len(PROJ)
+            x = self.x[p["x_off"]:p["x_off"] + p["K"]]
+            q.qmm_prep_act(W4A8, 1, p["K"], GROUP, GROUP, x, 0, a=self.a[j], sx=self.sx[j])
+            q.qmm_gemv(p["d"], p["packed"], self.a[j], self.sx[j], self.y[p["y_off"]:p["y_off"] + p["N"]],
+                       self.ws, self.ws_bytes)
+
+    def enqueue_gemvs(self):
+        """The step's GEMV launches alone (activations already prepared)."""
+        q = self.q
+        for i, p in enumerate(self.projs):
+            j = i % len(PROJ)
+            q.qmm_gemv(p["d"], p["packed"], self.a[j], self.sx[j], self.y[p["y_off"]:p["y_off"] + p["N"]],
+                       self.ws, self.ws_bytes)
+
+    def gemv_algorithmic_bytes(self):
+        """Per step: packed nibbles + scales, int8 codes, fp32 scales, fp32 output."""
+        return self.weight_bytes + self.act_bytes
+
+
+def capture(fn):
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()          # eager warm-up: first-call set-up happens outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(g, steps, warmup, world):
+    """Seconds for `steps` replays, CUDA events on the replay stream, max over ranks."""
+    import torch
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    return e0.elapsed_time(e1) / 1e3
+
+
+def gemv_traffic_per_step(model):
+    """DRAM bytes of the GEMV launches of one step, from the committed ncu
+    summary, or None when the kernel changed since it was taken."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    src_hash = hashlib.sha256(open(GEMV_SOURCE, "rb").read()).hexdigest()[:16]
+    vals = {}
+    with open(PROFILE_TRAFFIC) as f:
+        for ln in f:
+            if ":" in ln and not ln.startswith("#"):
+                k, _, v = ln.partition(":")
+                vals[k.strip()] = v.strip()
+    if vals.get("gemv_source_sha256_16") != src_hash:
+        return None
+    try:
+        per_weight_byte = float(vals["dram_bytes_per_weight_byte"])
+    except (KeyError, ValueError):
+        return None
+    return per_weight_byte * model.weight_bytes
+
+
+# ------------------------------------------------------------------ CPU baseline (oracle)
+
+def cpu_oracle_rate(host, seconds, rows_cap=None):
+    """Oracle (single-threaded C) on the decode projections, cycling through
+    them until `seconds` pass: prepass of x, then the outputs of the sampled
+    rows. Returns (weight+scale bytes per second, description)."""
+    import oracle
+    orc = oracle.default()
+    t0 = time.perf_counter()
+    done_bytes = 0
+    n_proj = 0
+    while True:
+        for qb, sw, x in host:
+            N, K = qb.shape[0], qb.shape[1] * 2
+            rows = None
+            nr = N
+            if rows_cap and rows_cap < N:
+                rows = np.arange(0, N, max(1, N // rows_cap), dtype=np.int32)[:rows_cap]
+                nr = rows.size
+            a, sx, _ = orc.prep_w4a8(x, GROUP, GROUP)
+            orc.gemm_w4a8(qb, sw, a, sx, GROUP, rows=rows)
+            done_bytes += nr * (K // 2 + 2 * (K // GROUP))
+            n_proj += 1
+            if time.perf_counter() - t0 >= seconds:
+                el = time.perf_counter() - t0
+                return done_bytes / el / 1e9, n_proj, el
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle, as it stands, on the host cores."""
+    if rank != 0:
+        return      # rank 0 alone times the oracle; the other ranks exit without work
+    host = []
+    for l in range(2):
+        for name, N, K in PROJ:
+            _, qb, sw, x = layer_inputs(0, 0, l, name, N, K)
+            host.append((qb, sw, x))
+    import oracle
+    orc = oracle.default()
+    # one step = the prepass and 64 sampled output rows of one projection
+    rows_per_step = 64
+    times, nbytes = [], 0
+    total = args.warmup + args.steps
+    t_budget = 150.0
+    t_start = time.perf_counter()
+    for s in range(total):
+        qb, sw, x = host[s % len(host)]
+        N, K = qb.shape[0], qb.shape[1] * 2
+        rows = np.linspace(0, N - 1, rows_per_step).astype(np.int32)
+        t0 = time.perf_counter()
+        a, sx, _ = orc.prep_w4a8(x, GROUP, GROUP)
+        orc.gemm_w4a8(qb, sw, a, sx, GROUP, rows=rows)
+        dt = time.perf_counter() - t0
+        if s >= args.warmup:
+            times.append(dt)
+            nbytes += rows_per_step * (K // 2 + 2 * (K // GROUP))
+        if time.perf_counter() - t_start > t_budget:
+            break
+    el = sum(times) if times else float("nan")
+    value = nbytes / el / 1e9 if times else None
+    line = {
+        "impl": "reference", "metric": "GEMV weight GB/s (decode projections, M=1)", "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": len(times), "warmup": args.warmup,
+        "ms_per_step": 1e3 * el / max(1, len(times)), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "config": {"workload": "gemma_decode (sampled rows)", "sample": f"{rows_per_step} output rows per step"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"prepass + {rows_per_step} sampled rows of one projection per step, "
+                                   f"cycling through 8 projections"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ sweep of the other workloads
+
+def sweep(world):
+    """Extra figures for the other workloads (not the headline): GEMV at
+    K = N = 1024, prefill GEMM TOPS vs M, affine GEMM, lm_head sweep. Each
+    call rotates over enough weight copies to exceed L2 twice."""
+    import torch
+    import bit_group_quantized_qmm_gb300 as q
+    dev = torch.device("cuda", torch.cuda.current_device())
+    out = {}
+    pool_bytes = 320 << 20
+
+    def pack_pool(variant, N, K, group, name):
+        lay = qmm_synth.Layer(name, variant, N, K, group, group if variant == W4A8 else 0)
+        qb, s, b = qmm_synth.layer_weights(0, name, lay)
+        d = q.weight_desc(variant, N, K, group)
+        size = q.qmm_packed_size(d)
+        copies = max(2, math.ceil(pool_bytes / size))
+        first = torch.empty(size, dtype=torch.uint8, device=dev)
+        q.qmm_pack_weights(d, torch.from_numpy(qb).to(dev), torch.from_numpy(s.view(np.int16)).to(dev),
+                           None if b is None else torch.from_numpy(b.view(np.int16)).to(dev), first)
+        pool = [first] + [first.clone() for _ in range(copies - 1)]
+        return lay, d, pool, size
+
+    def timed(fn, iters=20, warm=3):
+        g = capture(fn)
+        return time_graph(g, iters, warm, 1) / iters
+
+    # K = N = 1024 GEMV
+    lay, d, pool, size = pack_pool(W4A8, 1024, 1024, 64, "gemv_k1024_n1024")
+    x = torch.from_numpy(qmm_synth.layer_activations(0, "gemv_k1024_n1024", lay, 1)).to(dev)
+    a = torch.empty(1024, dtype=torch.int8, device=dev)
+    sx = torch.empty(16, dtype=torch.float32, device=dev)
+    y = torch.empty(1024, dtype=torch.float32, device=dev)
+    ws = torch.zeros(max(16, q.qmm_gemv_workspace_size(d)), dtype=torch.uint8, device=dev)
+    q.qmm_prep_act(W4A8, 1, 1024, 64, 0, x, 0, a=a, sx=sx)
+
+    def gemv_pool():
+        for p in pool:
+            q.qmm_gemv(d, p, a, sx, y, ws, ws.numel())
+    t = timed(gemv_pool) / len(pool)
+    out["gemv_k1024_n1024"] = {"us_per_call": t * 1e6, "weight_GBps": size / t / 1e9}
+    del pool
+
+    # prefill GEMM K=1536 N=12288 vs M
+    lay, d, pool, size = pack_pool(W4A8, 12288, 1536, 64, "prefill_gemm")
+    res = {}
+    for M in (16, 64, 128, 512, 1068):
+        x = torch.from_numpy(qmm_synth.layer_activations(0, f"prefill_gemm/x{M}", lay, M)).to(dev)
+        a16 = torch.empty((M, 1536), dtype=torch.float16, device=dev)
+        sxm = torch.empty((M, 24), dtype=torch.float32, device=dev)
+        Y = torch.empty((M, 12288), dtype=torch.float32, device=dev)
+        q.qmm_prep_act(W4A8, M, 1536, 64, 64, x, 0, a16=a16, sx=sxm)
+        use = pool[:max(2, min(len(pool), 8))]
+
+        def gemm_pool():
+            for p in use:
+                q.qmm_gemm(d, p, M, a16, sxm, Y)
+        t = timed(gemm_pool) / len(use)
+        res[str(M)] = {"us_per_call": t * 1e6, "TOPS": 2 * M * 12288 * 1536 / t / 1e12,
+                       "weight_GBps": size / t / 1e9}
+    out["prefill_gemm"] = res
+    del pool
+
+    # affine GEMM K=5120 N=34816
+    lay, d, pool, size = pack_pool(AFFINE, 34816, 5120, 64, "affine_gemm")
+    res = {}
+    for M in (64, 65, 128):
+        x16 = torch.from_numpy(qmm_synth.layer_activations(0, f"affine_gemm/x{M}", lay, M).view(np.float16)).to(dev)
+        S = torch.empty((M, 80), dtype=torch.float32, device=dev)
+        Y = torch.empty((M, 34816), dtype=torch.float32, device=dev)
+        q.qmm_prep_act(AFFINE, M, 5120, 64, 0, x16, 1, gsum=S)
+
+        def aff_pool():
+            for p in pool:
+                q.qmm_gemm(d, p, M, x16, S, Y)
+        t = timed(aff_pool) / len(pool)
+        res[str(M)] = {"us_per_call": t * 1e6, "TFLOPS": 2 * M * 34816 * 5120 / t / 1e12,
+                       "weight_GBps": size / t / 1e9}
+    out["affine_gemm"] = res
+    del pool
+
+    # lm_head sweep K=1536 N=262144 group 128
+    lay, d, pool, size = pack_pool(W4A8, 262144, 1536, 128, "lm_head")
+    res = {}
+    for M in (1, 2, 4, 8, 16, 32):
+        x = torch.from_numpy(qmm_synth.layer_activations(0, f"lm_head/x{M}", lay, M)).to(dev)
+        a = torch.empty((M, 1536), dtype=torch.int8, device=dev)
+        a16 = torch.empty((M, 1536), dtype=torch.float16, device=dev)
+        sxm = torch.empty((M, 12), dtype=torch.float32, device=dev)
+        Y = torch.empty((M, 262144), dtype=torch.float32, device=dev)
+        q.qmm_prep_act(W4A8, M, 1536, 128, 128, x, 0, a=a, a16=a16, sx=sxm)
+        entry = {}
+
+        def gemm_pool():
+            for p in pool:
+                q.qmm_gemm(d, p, M, a16, sxm, Y)
+        t = timed(gemm_pool) / len(pool)
+        entry["gemm"] = {"us_per_call": t * 1e6, "weight_GBps": size / t / 1e9}
+        if M == 1:
+            ws1 = torch.zeros(max(16, q.qmm_gemv_workspace_size(d)), dtype=torch.uint8, device=dev)
+
+            def gemv_pool2():
+                for p in pool:
+                    q.qmm_gemv(d, p, a, sxm, Y, ws1, ws1.numel())
+            t = timed(gemv_pool2) / len(pool)
+            entry["gemv"] = {"us_per_call": t * 1e6, "weight_GBps": size / t / 1e9}
+        res[str(M)] = entry
+    out["lm_head"] = res
+    del pool
+    torch.cuda.empty_cache()
+    return out
+
+
+# ------------------------------------------------------------------ main
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device for the library arm (use --impl reference for the oracle)")
+    torch.cuda.set_device(local)
+    dist_init(world, use_cuda=True)
+    import bit_group_quantized_qmm_gb300 as q
+
+    hbm_peak, bf16_peak, peak_kind = measured_peaks()
+    model = DecodeModel(args.layers, rank, keep_host=(rank == 0 and world == 1))
+    g_step = capture(model.enqueue_step)
+    g_gemv = capture(model.enqueue_gemvs)
+    n_kernels_per_step = 2 * len(model.projs)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_step = time_graph(g_step, args.steps, args.warmup, world)
+    clock_rows = sampler.stop()
+    t_step = max_over_ranks(t_step, world)
+
+    # the dominant kernel alone: the step's GEMV launches back to back
+    gemv_iters = max(10, min(args.steps, 2000))
+    t_gemv = time_graph(g_gemv, gemv_iters, 3, world)
+    t_gemv = max_over_ranks(t_gemv, world)
+    gemv_launch_s = t_gemv / (gemv_iters * len(model.projs))
+
+    # end to end: pinned host x in, graph, y out, every step
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_steps = max(10, min(args.steps, 2000))
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        model.x.copy_(model.x_host, non_blocking=True)
+        g_step.replay()
+        model.y_host.copy_(model.y, non_blocking=True)
+    torch.cuda.synchronize()
+    t_e2e = time.perf_counter() - t0
+    barrier(world)
+    t_e2e = max_over_ranks(t_e2e, world)
+
+    total_weight = sum_over_ranks(model.weight_bytes * args.steps, world)
+    value = total_weight / t_step / 1e9
+    e2e_value = sum_over_ranks(model.weight_bytes * e2e_steps, world) / t_e2e / 1e9
+    gemv_bytes = model.gemv_algorithmic_bytes() / len(model.projs)
+    achieved = gemv_bytes / gemv_launch_s / 1e9
+    traffic = gemv_traffic_per_step(model)
+    status = q.qmm_device_status()
+
+    sweep_out = None
+    if not args.no_sweep and rank == 0:
+        sweep_out = sweep(1 if world == 1 else world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, nproj, el = cpu_oracle_rate(model.host[:8], args.cpu_seconds)
+        cpu = {"value": rate, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{nproj} projection passes (prepass + all output rows) of the first two layers, "
+                         f"{el:.1f} s, single-threaded C"}
+
+    if rank == 0:
+        clocks = ClockSampler.summarize(clock_rows)
+        line = {
+            "metric": "GEMV weight GB/s (decode projections, M=1)",
+            "value": value,
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": 1e3 * t_step / args.steps,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "int8",
+            "data": "synthetic",
+            "config": {
+                "workload": f"gemma_decode: {args.layers} layers x (gate_up 1536->12288, down 6144->1536, "
+                            "q 1536->2048, o 2048->1536), M=1, W4A8 group 64, Hadamard-64, "
+                            "x N(0,1) + 1% +-20 outliers, seed 0",
+                "layers": args.layers,
+                "weight_bytes_per_step": model.weight_bytes,
+                "l2": "per-step weights larger than L2 (no flush)",
+                "launch": "CUDA graph of the step; programmatic dependent launch",
+                "parallelism": f"replicas x{world}",
+            },
+            "roofline": {
+                "kernel": "gemv_kernel (W4A8, M=1)",
+                "bound": "hbm",
+                "achieved": achieved,
+                "peak": hbm_peak,
+                "unit": "GB/s",
+                "frac": achieved / hbm_peak,
+                "peak_kind": f"{peak_kind} copy bandwidth",
+                "traffic": None if traffic is None else traffic / len(model.projs),
+                "algorithmic_bytes_per_launch": gemv_bytes,
+                "avg_launch_us": gemv_launch_s * 1e6,
+                "frac_of_8TBps": achieved / 8000.0,
+            },
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": model.h2d_bytes,
+                    "d2h_bytes_per_step": model.d2h_bytes, "steps": e2e_steps},
+            "gpu_launches": n_kernels_per_step * args.steps,
+            "clocks": clocks,
+            "device_status": status,
+            "sweep": sweep_out,
+        }
+        print(json.dumps(line), flush=True)
+    barrier(world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
