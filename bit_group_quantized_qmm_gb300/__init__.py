@@ -51,6 +51,7 @@ def _load():
         "qmm_prep_act": (I32, [I32, I32, I32, I32, I32, P, I32, P, P, P, P, P, P, P]),
         "qmm_gemv_workspace_size": (SZ, [D]),
         "qmm_gemv": (I32, [D, P, P, P, P, P, SZ, P]),
+        "qmm_gemv_static_scratch": (I32, [D, P, P, P, P, P]),
         "qmm_gemm": (I32, [D, P, I32, P, P, P, P]),
         "qmm_debug_partials": (I32, [D, P, I32, I32, P, P, P]),
         "qmm_status_string": (ctypes.c_char_p, [I32]),
@@ -141,6 +142,12 @@ def qmm_gemv(desc, packed, a, sx, y, workspace=None, workspace_bytes=0, stream=N
         workspace_bytes = workspace.numel() * workspace.element_size()
     _check(_L.qmm_gemv(ctypes.byref(desc), _ptr(packed), _ptr(a), _ptr(sx), _ptr(y), _ptr(workspace),
                        workspace_bytes, _stream(stream)), "qmm_gemv")
+
+
+def qmm_gemv_static_scratch(desc, packed, a, sx, y, stream=None):
+    """qmm_gemv with the library's own fixed scratch (allocates nothing)."""
+    _check(_L.qmm_gemv_static_scratch(ctypes.byref(desc), _ptr(packed), _ptr(a), _ptr(sx), _ptr(y),
+                                      _stream(stream)), "qmm_gemv_static_scratch")
 
 
 def qmm_gemm(desc, packed, M, act16, act_scale, Y, stream=None):

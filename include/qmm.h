@@ -205,6 +205,29 @@ qmm_status qmm_gemv(const qmm_weight_desc* w, const void* packed, const int8_t* 
                     float* y, void* workspace, size_t workspace_bytes, qmm_stream stream);
 
 /*
+ * M = 1 GEMV for callers that cannot allocate device memory. The pages have no
+ * counterpart: it exists for code that runs inside a host program that owns
+ * every device allocation and does not let it allocate, or on a latency-critical
+ * path that must never reach cudaMalloc (which can synchronise the device).
+ * Arguments, results and errors are those of qmm_gemv; instead of a caller's
+ * workspace the split-K scratch is a fixed array inside the library of
+ * QMM_GEMV_STATIC_SCRATCH_BYTES (1 MiB), held on every device that loads the
+ * library until the process exits. A weight whose qmm_gemv_workspace_size
+ * exceeds it is rejected with QMM_ERR_WORKSPACE. The call allocates nothing.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call shares the array and finds the last call's contents in it; the
+ *     call clears the part that must start at zero (the split-K counters) on
+ *     `stream` before its kernel.
+ *   - Calls whose work overlaps on the GPU (other streams, other host threads)
+ *     race on the array: serialise them.
+ */
+#define QMM_GEMV_STATIC_SCRATCH_BYTES ((size_t)1 << 20)
+qmm_status qmm_gemv_static_scratch(const qmm_weight_desc* w, const void* packed, const int8_t* a,
+                                   const float* sx, float* y, qmm_stream stream);
+
+/*
  * GEMM, any M >= 1, both variants, on the tcgen05 tensor cores
  * (cactus PR #697, Summary: fused GEMM with raw int32 partials and a separate
  * fp32 rescale; TensorFold PR #3215 for the affine tiles on the prepass sums).
