@@ -22,7 +22,7 @@ QMM_AFFINE = 1
 QMM_DTYPE_F32, QMM_DTYPE_F16, QMM_DTYPE_BF16 = 0, 1, 2
 QMM_PATH_GEMV, QMM_PATH_GEMM = 0, 1
 KERNEL_IDS = {0: "none", 1: "pack", 2: "prep_w4a8", 3: "prep_affine", 4: "gemv_w4a8", 5: "gemm_w4a8",
-              6: "gemm_affine"}
+              6: "gemm_affine", 7: "gemv_fused"}
 
 STATUS = {0: "QMM_OK", 1: "QMM_ERR_INVALID_ARG", 2: "QMM_ERR_UNSUPPORTED_SHAPE", 3: "QMM_ERR_UNSUPPORTED_DEVICE",
           4: "QMM_ERR_MISALIGNED", 5: "QMM_ERR_CUDA", 6: "QMM_ERR_TIMEOUT", 7: "QMM_ERR_WORKSPACE"}
@@ -52,6 +52,7 @@ def _load():
         "qmm_gemv_workspace_size": (SZ, [D]),
         "qmm_gemv": (I32, [D, P, P, P, P, P, SZ, P]),
         "qmm_gemv_static_scratch": (I32, [D, P, P, P, P, P]),
+        "qmm_gemv_fused": (I32, [D, P, P, I32, I32, P, P, P, P]),
         "qmm_gemm": (I32, [D, P, I32, P, P, P, P]),
         "qmm_debug_partials": (I32, [D, P, I32, I32, P, P, P]),
         "qmm_status_string": (ctypes.c_char_p, [I32]),
@@ -148,6 +149,11 @@ def qmm_gemv_static_scratch(desc, packed, a, sx, y, stream=None):
     """qmm_gemv with the library's own fixed scratch (allocates nothing)."""
     _check(_L.qmm_gemv_static_scratch(ctypes.byref(desc), _ptr(packed), _ptr(a), _ptr(sx), _ptr(y),
                                       _stream(stream)), "qmm_gemv_static_scratch")
+
+
+def qmm_gemv_fused(desc, packed, x, x_dtype, hadamard, y, a_out=None, sx_out=None, stream=None):
+    _check(_L.qmm_gemv_fused(ctypes.byref(desc), _ptr(packed), _ptr(x), x_dtype, hadamard, _ptr(y), _ptr(a_out),
+                             _ptr(sx_out), _stream(stream)), "qmm_gemv_fused")
 
 
 def qmm_gemm(desc, packed, M, act16, act_scale, Y, stream=None):

@@ -239,6 +239,27 @@ qmm_status qmm_gemv(const qmm_weight_desc* w, const void* packed, const int8_t* 
                     QMM_KERNEL_GEMV_W4A8);
 }
 
+qmm_status qmm_gemv_fused(const qmm_weight_desc* w, const void* packed, const void* x, int32_t x_dtype,
+                          int32_t hadamard, float* y, int8_t* a_out, float* sx_out, qmm_stream stream)
+{
+    qmm_status st = shape_ok(w);
+    if (st != QMM_OK) return st;
+    if (w->variant != QMM_W4A8) return QMM_ERR_UNSUPPORTED_SHAPE;
+    if (hadamard != 0 && hadamard != w->group) return QMM_ERR_UNSUPPORTED_SHAPE;
+    if (x_dtype != QMM_DTYPE_F32 && x_dtype != QMM_DTYPE_F16 && x_dtype != QMM_DTYPE_BF16) return QMM_ERR_INVALID_ARG;
+    if (!packed || !x || !y) return QMM_ERR_INVALID_ARG;
+    if (!aligned16(packed) || !aligned16(x) || !aligned16(y) || (a_out && !aligned16(a_out)) ||
+        (sx_out && !aligned16(sx_out)))
+        return QMM_ERR_MISALIGNED;
+    const int max_k = 16 * (w->group == 64 ? 44 : 22) * w->group;
+    if (w->K > max_k) return QMM_ERR_UNSUPPORTED_SHAPE;
+    LaunchCtx c;
+    if ((st = device_ctx(stream, &c)) != QMM_OK) return st;
+    return launched(launch_gemv_fused(c, w->N, w->K, w->group, hadamard, static_cast<const uint8_t*>(packed), x,
+                                      x_dtype, y, a_out, sx_out),
+                    QMM_KERNEL_GEMV_FUSED);
+}
+
 static qmm_status gemm_common(const qmm_weight_desc* w, const void* packed, int32_t M, const void* act16,
                               const float* act_scale, float* Y, int32_t* P, qmm_stream stream)
 {

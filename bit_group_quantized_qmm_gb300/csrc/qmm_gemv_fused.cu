@@ -1,0 +1,293 @@
+// qmm_gemv_fused.cu -- one-kernel M = 1 decode GEMV of the symmetric W4A8
+// variant: activation prepass and weight streaming in a single launch.
+//
+// cactus PR #697 "SME2 acceleration for CQ4 matmul, prefill attention, and
+// orthogonal embeddings", Summary: the M = 1 path is one dispatch in two
+// phases — phase A applies the Hadamard transform and quantizes the
+// activations to int8 per group, phase B streams the packed nibbles through
+// the integer partials leaf — and the dispatch itself was a measurable tax on
+// calls of tens of microseconds.
+//
+// GB300 design. A CTA owns one 128-row tile and a contiguous range of its
+// groups. Before waiting on the previous kernel (programmatic dependent
+// launch) a producer warp issues 1-D bulk copies of all the CTA's packed
+// chunks into shared memory, so a layer's weights stream while its
+// predecessor finishes. After the wait, phase A quantizes only the CTA's own
+// groups (quantization is per group, so no other CTA's input is needed), writing
+// the codes straight into the permuted order the dp4a expansion reads;
+// phase B is the exact int32 group-partial loop of the plain GEMV. The
+// K-slices of a tile form one thread-block cluster and are summed through
+// distributed shared memory in a fixed order by the cluster's first CTA: no
+// global workspace, no atomics, deterministic results.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "qmm.h"
+#include "qmm_internal.h"
+#include "qmm_ptx.cuh"
+
+namespace qmm {
+
+namespace {
+
+constexpr int kComputeThreads = 256;
+constexpr int kThreads = kComputeThreads + 32;   // + producer warp
+constexpr int kTargetCtas = 2 * 152;
+constexpr int kMaxCluster = 16;
+
+template <int GROUP>
+struct Cfg {
+    static constexpr int PP = GROUP / 32;
+    static constexpr int CB = 64 * GROUP + 256;
+    static constexpr int E = GROUP / 32;        // inputs per lane in phase A
+};
+
+__device__ __forceinline__ int nib_lo16(uint32_t w) { return (int)(((w << 4) ^ 0x80808080u) & 0xF0F0F0F0u); }
+__device__ __forceinline__ int nib_hi16(uint32_t w) { return (int)((w ^ 0x80808080u) & 0xF0F0F0F0u); }
+__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+template <int XDT>
+__device__ __forceinline__ float load_in(const void* x, size_t i)
+{
+    if (XDT == 0) return static_cast<const float*>(x)[i];
+    if (XDT == 1) return __half2float(static_cast<const __half*>(x)[i]);
+    return __bfloat162float(static_cast<const __nv_bfloat16*>(x)[i]);
+}
+
+size_t smem_bytes(int ring, int cb, int ng, int group)
+{
+    return (size_t)ring * cb + (size_t)ng * group + (size_t)ng * 4 + 2 * 128 * 4 + 2 * ring * 8 + 16 + 64;
+}
+
+// Grid (T, ksplit), cluster (1, ksplit): CTA (t, s) handles groups [g0, g1) of tile t.
+template <int GROUP, int XDT>
+__global__ void __launch_bounds__(kThreads)
+    gemv_fused_kernel(int N, int K, int ksplit, int hadamard, float rot_scale, const uint8_t* __restrict__ blob,
+                      const void* __restrict__ x, float* __restrict__ y, int8_t* __restrict__ a_out,
+                      float* __restrict__ sx_out, int* status)
+{
+    using C = Cfg<GROUP>;
+    const int G = K / GROUP;
+    const int t = blockIdx.x, s = blockIdx.y;
+    const int g0 = (int)((long long)G * s / ksplit), g1 = (int)((long long)G * (s + 1) / ksplit);
+    const int ng = g1 - g0;
+    const int ring = ng;   // the launcher keeps a CTA's whole slice resident
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t* stages = smem;
+    uint8_t* aperm = smem + (size_t)ring * C::CB;                              // permuted codes, ng*GROUP bytes
+    float* sxs = reinterpret_cast<float*>(aperm + (size_t)ng * GROUP);        // [ng]
+    float* red = sxs + ng;                                                     // [128]
+    float* part = red + 128;                                                   // [128] this CTA's partial y
+    uint64_t* full = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(part + 128) + 7) & ~uintptr_t(7));
+    int* flags = reinterpret_cast<int*>(full + ring);
+    volatile int* abort = flags;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    pdl_trigger();
+    if (tid == 0) {
+        for (int i = 0; i < ring; ++i) mbar_init(&full[i], 1);
+        flags[0] = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kComputeThreads / 32) {
+        // producer: the whole slice, before the dependency wait
+        if (lane == 0) {
+            const uint8_t* src = blob + ((size_t)t * G + g0) * C::CB;
+            for (int i = 0; i < ng; ++i) {
+                mbar_arrive_expect_tx(&full[i], C::CB);
+                bulk_g2s(stages + (size_t)i * C::CB, src + (size_t)i * C::CB, C::CB, &full[i]);
+            }
+            // the CTA must not exit with copies in flight
+            for (int i = 0; i < ng; ++i) mbar_wait(&full[i], 0, status, nullptr);
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------- phase A
+        pdl_wait();
+        for (int i = warp; i < ng; i += kComputeThreads / 32) {
+            const int g = g0 + i;
+            const size_t base = (size_t)g * GROUP + (size_t)lane * C::E;
+            float v[C::E];
+#pragma unroll
+            for (int e = 0; e < C::E; ++e) v[e] = load_in<XDT>(x, base + e);
+            if (hadamard) {
+#pragma unroll
+                for (int h = 1; h < GROUP; h <<= 1) {
+                    if (h < C::E) {
+#pragma unroll
+                        for (int e = 0; e < C::E; ++e)
+                            if ((e & h) == 0) {
+                                const float lo = v[e], hi = v[e + h];
+                                v[e] = __fadd_rn(lo, hi);
+                                v[e + h] = __fsub_rn(lo, hi);
+                            }
+                    } else {
+                        const int lm = h / C::E;
+                        const bool upper = (lane & lm) != 0;
+#pragma unroll
+                        for (int e = 0; e < C::E; ++e) {
+                            const float o = __shfl_xor_sync(0xffffffffu, v[e], lm);
+                            v[e] = upper ? __fsub_rn(o, v[e]) : __fadd_rn(v[e], o);
+                        }
+                    }
+                }
+            }
+            float amax = 0.f;
+#pragma unroll
+            for (int e = 0; e < C::E; ++e) amax = fmaxf(amax, fabsf(v[e]));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            float scale = 0.f;
+            int codes[C::E];
+            if (amax == 0.f) {
+#pragma unroll
+                for (int e = 0; e < C::E; ++e) codes[e] = 0;
+            } else {
+                const float sc = __fdiv_rn(amax, 127.0f);
+#pragma unroll
+                for (int e = 0; e < C::E; ++e) {
+                    float r = rintf(__fdiv_rn(v[e], sc));
+                    r = fminf(fmaxf(r, -127.f), 127.f);
+                    codes[e] = (int)r;
+                }
+                scale = __fmul_rn(sc, rot_scale);
+            }
+            // byte of local k within its 8-block in the dp4a order (k = 0, 4, 1, 5, 2, 6, 3, 7)
+#pragma unroll
+            for (int e = 0; e < C::E; ++e) {
+                const int k = lane * C::E + e;
+                aperm[(size_t)i * GROUP + (k & ~7) + 2 * (k & 3) + ((k >> 2) & 1)] = (uint8_t)(int8_t)codes[e];
+            }
+            if (a_out) {
+                uint32_t packed = 0;
+#pragma unroll
+                for (int e = 0; e < C::E; ++e) packed |= ((uint32_t)codes[e] & 0xFFu) << (8 * e);
+                if (C::E == 2)
+                    *reinterpret_cast<uint16_t*>(a_out + base) = (uint16_t)packed;
+                else
+                    *reinterpret_cast<uint32_t*>(a_out + base) = packed;
+            }
+            if (lane == 0) {
+                sxs[i] = scale;
+                if (sx_out) sx_out[g] = scale;
+            }
+        }
+        compute_sync();
+
+        // ---------------------------------------------------------- phase B
+        const int r = tid & 127, h = tid >> 7;
+        float acc = 0.f;
+        for (int i = h; i < ng; i += 2) {
+            if (!mbar_wait(&full[i], 0, status, abort)) break;
+            const uint8_t* c = stages + (size_t)i * C::CB;
+            int dp = 0;
+#pragma unroll
+            for (int p = 0; p < C::PP; ++p) {
+                const uint4 w = *reinterpret_cast<const uint4*>(c + p * 2048 + r * 16);
+                const uint4* ap = reinterpret_cast<const uint4*>(aperm + (size_t)i * GROUP + 32 * p);
+                const uint4 a0 = ap[0], a1 = ap[1];
+                dp = __dp4a(nib_lo16(w.x), (int)a0.x, dp);
+                dp = __dp4a(nib_hi16(w.x), (int)a0.y, dp);
+                dp = __dp4a(nib_lo16(w.y), (int)a0.z, dp);
+                dp = __dp4a(nib_hi16(w.y), (int)a0.w, dp);
+                dp = __dp4a(nib_lo16(w.z), (int)a1.x, dp);
+                dp = __dp4a(nib_hi16(w.z), (int)a1.y, dp);
+                dp = __dp4a(nib_lo16(w.w), (int)a1.z, dp);
+                dp = __dp4a(nib_hi16(w.w), (int)a1.w, dp);
+            }
+            const float sw = __half2float(reinterpret_cast<const __half*>(c + 64 * GROUP)[r]);
+            acc = fmaf((float)(dp >> 4), sw * sxs[i], acc);
+        }
+        if (h == 1) red[r] = acc;
+        compute_sync();
+        if (h == 0) {
+            part[r] = acc + red[r];
+            if (ksplit == 1 && t * 128 + r < N) y[t * 128 + r] = part[r];
+        }
+    }
+
+    if (ksplit > 1) {
+        // the cluster is this tile's K-slices; its first CTA sums them in order
+        cluster_sync_all();
+        if (s == 0 && tid < 128) {
+            const uint32_t addr = smem_u32(part + tid);
+            float v = 0.f;
+            for (int k = 0; k < ksplit; ++k) v += ld_shared_cluster_f32(map_shared_rank(addr, (uint32_t)k));
+            if (t * 128 + tid < N) y[t * 128 + tid] = v;
+        }
+        cluster_sync_all();   // keep every CTA's shared memory alive until it has been read
+    }
+}
+
+template <int GROUP, int XDT>
+cudaError_t run(const LaunchCtx& c, int N, int K, int hadamard, const uint8_t* blob, const void* x, float* y,
+                int8_t* a_out, float* sx_out)
+{
+    using C = Cfg<GROUP>;
+    auto kern = gemv_fused_kernel<GROUP, XDT>;
+    const int T = (N + 127) / 128, G = K / GROUP;
+    int ks = (kTargetCtas + T - 1) / T;
+    if (ks > G) ks = G;
+    if (ks > kMaxCluster) ks = kMaxCluster;
+    if (ks < 1) ks = 1;
+    // keep a CTA's slice within its shared memory (at most 48 chunks of group 64)
+    const int max_ng = GROUP == 64 ? 44 : 22;
+    while ((G + ks - 1) / ks > max_ng && ks < kMaxCluster && ks < G) ++ks;
+    const int ng_max = (G + ks - 1) / ks;
+    if (ng_max > max_ng) return cudaErrorInvalidValue;   // K too large for one cluster per tile
+    const size_t smem = smem_bytes(ng_max, C::CB, ng_max, GROUP);
+    static size_t configured = 0;
+    cudaError_t e;
+    if (smem > configured) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+        configured = smem;
+    }
+    const float rot = hadamard ? (float)(1.0 / sqrt((double)GROUP)) : 1.0f;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(T, ks);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = c.stream;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 1;
+    attr[na].val.clusterDim.y = ks;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+    if (c.pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kern, N, K, ks, hadamard, rot, blob, x, y, a_out, sx_out, c.status);
+}
+
+}  // namespace
+
+cudaError_t launch_gemv_fused(const LaunchCtx& c, int N, int K, int group, int hadamard, const uint8_t* blob,
+                              const void* x, int x_dtype, float* y, int8_t* a_out, float* sx_out)
+{
+    if (group == 64) {
+        if (x_dtype == 0) return run<64, 0>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
+        if (x_dtype == 1) return run<64, 1>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
+        return run<64, 2>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
+    }
+    if (group == 128) {
+        if (x_dtype == 0) return run<128, 0>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
+        if (x_dtype == 1) return run<128, 1>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
+        return run<128, 2>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace qmm

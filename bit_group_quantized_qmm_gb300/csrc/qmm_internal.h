@@ -56,6 +56,10 @@ cudaError_t launch_gemv(const LaunchCtx& c, int N, int K, int group, const uint8
 // Largest activation-row tile of the tensor-core GEMM (MMA N).
 constexpr int kMaxMTile = 224;
 
+// One-kernel decode GEMV: prepass of x and GEMV (optional code/scale outputs).
+cudaError_t launch_gemv_fused(const LaunchCtx& c, int N, int K, int group, int hadamard, const uint8_t* blob,
+                              const void* x, int x_dtype, float* y, int8_t* a_out, float* sx_out);
+
 struct GemmShape {
     int M, N, K;
     int m_tile;      // activation rows per tile (MMA N), multiple of 16, <= 224

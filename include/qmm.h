@@ -82,7 +82,8 @@ typedef enum {
     QMM_KERNEL_PREP_AFFINE = 3,
     QMM_KERNEL_GEMV_W4A8 = 4,
     QMM_KERNEL_GEMM_W4A8 = 5,
-    QMM_KERNEL_GEMM_AFFINE = 6
+    QMM_KERNEL_GEMM_AFFINE = 6,
+    QMM_KERNEL_GEMV_FUSED = 7
 } qmm_kernel_id;
 
 typedef void* qmm_stream; /* cudaStream_t */
@@ -203,6 +204,25 @@ size_t qmm_gemv_workspace_size(const qmm_weight_desc* w);
  */
 qmm_status qmm_gemv(const qmm_weight_desc* w, const void* packed, const int8_t* a, const float* sx,
                     float* y, void* workspace, size_t workspace_bytes, qmm_stream stream);
+
+/*
+ * One-kernel M = 1 decode GEMV, QMM_W4A8: the activation prepass and the GEMV
+ * in a single launch (cactus PR #697, Summary: the M = 1 path is one dispatch
+ * whose phase A rotates and quantizes the activations and whose phase B
+ * streams the packed nibbles through the integer partials).
+ *   x         device [K], dtype x_dtype (F32, F16, BF16)
+ *   hadamard  0 or w->group (as in qmm_prep_act)
+ *   y         device fp32 [N]
+ *   a_out     device int8 [K] or NULL: the codes (bit-identical to qmm_prep_act)
+ *   sx_out    device fp32 [G] or NULL: the scales (bit-identical to qmm_prep_act)
+ * y equals qmm_prep_act + qmm_gemv up to the fp32 summation order. The
+ * K-slices of a 128-row tile run as one thread-block cluster and are summed
+ * through distributed shared memory: no workspace, deterministic results.
+ * QMM_ERR_UNSUPPORTED_SHAPE if a tile's K range does not fit the cluster's
+ * shared memory (K > 16 x 44 x 64 for group 64, 16 x 22 x 128 for group 128).
+ */
+qmm_status qmm_gemv_fused(const qmm_weight_desc* w, const void* packed, const void* x, int32_t x_dtype,
+                          int32_t hadamard, float* y, int8_t* a_out, float* sx_out, qmm_stream stream);
 
 /*
  * M = 1 GEMV for callers that cannot allocate device memory. The pages have no

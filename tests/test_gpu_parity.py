@@ -205,6 +205,32 @@ def test_gemv_output(torch_cuda, orc, N, K, group, had, outl, workspace):
     assert ok, f"worst error / bound = {worst}"
 
 
+@pytest.mark.parametrize("N,K,group,had,outl", GEMV_CASES + [(256, 512, 128, 0, 0.0)])
+@pytest.mark.parametrize("x_dtype", [0, 1])
+def test_gemv_fused(torch_cuda, orc, N, K, group, had, outl, x_dtype):
+    """One-kernel prepass + GEMV: codes and scales bit-exact, y within tolerance."""
+    import torch
+    q = gc.lib()
+    qb, sw, x = gc.w4a8_case(12, f"fused/{N}/{K}", N, K, group, had, 1, outl)
+    d, packed = gc.pack(W4A8, N, K, group, qb, sw)
+    xin, xval = _prep_input(x, x_dtype)
+    dev = gc.dev()
+    y = torch.full((N,), float("nan"), dtype=torch.float32, device=dev)
+    a = torch.empty(K, dtype=torch.int8, device=dev)
+    sx = torch.empty(K // group, dtype=torch.float32, device=dev)
+    q.qmm_gemv_fused(d, packed, xin.to(dev), x_dtype, had, y, a, sx)
+    assert q.qmm_last_kernel_id() == 7
+    ra, rsx, _ = orc.prep_w4a8(xval, group, had)
+    assert np.array_equal(a.cpu().numpy(), ra[0])
+    assert np.array_equal(sx.cpu().numpy().view(np.uint32), rsx[0].view(np.uint32))
+    Y, Ym = orc.gemm_w4a8(qb, sw, ra, rsx, group)
+    y1 = y.cpu().numpy()
+    ok, worst = gc.within_w4a8(y1[None, :], Y, Ym)
+    assert ok, f"worst error / bound = {worst}"
+    q.qmm_gemv_fused(d, packed, xin.to(dev), x_dtype, had, y)
+    assert np.array_equal(y.cpu().numpy().view(np.uint32), y1.view(np.uint32)), "not deterministic"
+
+
 # ------------------------------------------------------------------ GEMM
 
 GEMM_CASES = [
