@@ -34,6 +34,9 @@ constexpr int kComputeThreads = 256;
 constexpr int kThreads = kComputeThreads + 32;   // + producer warp
 constexpr int kTargetCtas = 2 * 152;
 constexpr int kMaxCluster = 16;
+constexpr int kMaxNg = 48;                          // chunks a CTA may hold
+constexpr size_t kHeaderBytes = 1536;   // part, red (1 KB), flags (16 B), kMaxNg barriers, padding to 128 B
+static_assert(kHeaderBytes % 128 == 0 && kHeaderBytes >= 1024 + 16 + 8 * kMaxNg, "header layout");
 
 template <int GROUP>
 struct Cfg {
@@ -56,7 +59,7 @@ __device__ __forceinline__ float load_in(const void* x, size_t i)
 
 size_t smem_bytes(int ring, int cb, int ng, int group)
 {
-    return (size_t)ring * cb + (size_t)ng * group + (size_t)ng * 4 + 2 * 128 * 4 + 2 * ring * 8 + 16 + 64;
+    return kHeaderBytes + (size_t)ring * cb + (size_t)ng * group + (size_t)ng * 4 + 16;
 }
 
 // Grid (T, ksplit), cluster (1, ksplit): CTA (t, s) handles groups [g0, g1) of tile t.
@@ -73,14 +76,16 @@ __global__ void __launch_bounds__(kThreads)
     const int ng = g1 - g0;
     const int ring = ng;   // the launcher keeps a CTA's whole slice resident
 
+    // Fixed offsets first: the cluster's first CTA reads `part` of the other
+    // CTAs at its own offset, and ng differs between the K-slices.
     extern __shared__ __align__(128) uint8_t smem[];
-    uint8_t* stages = smem;
-    uint8_t* aperm = smem + (size_t)ring * C::CB;                              // permuted codes, ng*GROUP bytes
+    float* part = reinterpret_cast<float*>(smem);                             // [128] this CTA's partial y
+    float* red = part + 128;                                                   // [128]
+    int* flags = reinterpret_cast<int*>(red + 128);                            // [4]
+    uint64_t* full = reinterpret_cast<uint64_t*>(flags + 4);                   // [kMaxNg]
+    uint8_t* stages = smem + kHeaderBytes;
+    uint8_t* aperm = stages + (size_t)ring * C::CB;                            // permuted codes, ng*GROUP bytes
     float* sxs = reinterpret_cast<float*>(aperm + (size_t)ng * GROUP);        // [ng]
-    float* red = sxs + ng;                                                     // [128]
-    float* part = red + 128;                                                   // [128] this CTA's partial y
-    uint64_t* full = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(part + 128) + 7) & ~uintptr_t(7));
-    int* flags = reinterpret_cast<int*>(full + ring);
     volatile int* abort = flags;
 
     const int tid = threadIdx.x;
