@@ -35,8 +35,9 @@ constexpr int kThreads = kComputeThreads + 32;   // + producer warp
 constexpr int kTargetCtas = 2 * 152;
 constexpr int kMaxCluster = 16;
 constexpr int kMaxNg = 48;                          // chunks a CTA may hold
-constexpr size_t kHeaderBytes = 1536;   // part, red (1 KB), flags (16 B), kMaxNg barriers, padding to 128 B
-static_assert(kHeaderBytes % 128 == 0 && kHeaderBytes >= 1024 + 16 + 8 * kMaxNg, "header layout");
+// parts (16 x 512 B), red (512 B), flags (16 B), kMaxNg barriers, padded to 128 B
+constexpr size_t kHeaderBytes = 9216;
+static_assert(kHeaderBytes % 128 == 0 && kHeaderBytes >= (kMaxCluster + 1) * 512 + 16 + 8 * kMaxNg, "header layout");
 
 template <int GROUP>
 struct Cfg {
@@ -76,11 +77,12 @@ __global__ void __launch_bounds__(kThreads)
     const int ng = g1 - g0;
     const int ring = ng;   // the launcher keeps a CTA's whole slice resident
 
-    // Fixed offsets first: the cluster's first CTA reads `part` of the other
-    // CTAs at its own offset, and ng differs between the K-slices.
+    // Fixed offsets first: every CTA of the cluster stores its partial sums
+    // into the first CTA's `parts` at the same offset, and ng differs between
+    // the K-slices.
     extern __shared__ __align__(128) uint8_t smem[];
-    float* part = reinterpret_cast<float*>(smem);                             // [128] this CTA's partial y
-    float* red = part + 128;                                                   // [128]
+    float* parts = reinterpret_cast<float*>(smem);                            // [kMaxCluster][128] (rank 0)
+    float* red = parts + kMaxCluster * 128;                                    // [128]
     int* flags = reinterpret_cast<int*>(red + 128);                            // [4]
     uint64_t* full = reinterpret_cast<uint64_t*>(flags + 4);                   // [kMaxNg]
     uint8_t* stages = smem + kHeaderBytes;
@@ -210,21 +212,25 @@ __global__ void __launch_bounds__(kThreads)
         if (h == 1) red[r] = acc;
         compute_sync();
         if (h == 0) {
-            part[r] = acc + red[r];
-            if (ksplit == 1 && t * 128 + r < N) y[t * 128 + r] = part[r];
+            const float v = acc + red[r];
+            if (ksplit == 1) {
+                if (t * 128 + r < N) y[t * 128 + r] = v;
+            } else {
+                // push this slice's sums into the first CTA of the cluster
+                st_shared_cluster_f32(map_shared_rank(smem_u32(parts + s * 128 + r), 0u), v);
+            }
         }
     }
 
     if (ksplit > 1) {
-        // the cluster is this tile's K-slices; its first CTA sums them in order
+        // the cluster is this tile's K-slices: after the barrier (release /
+        // acquire) the first CTA holds every slice's sums and adds them in order
         cluster_sync_all();
         if (s == 0 && tid < 128) {
-            const uint32_t addr = smem_u32(part + tid);
             float v = 0.f;
-            for (int k = 0; k < ksplit; ++k) v += ld_shared_cluster_f32(map_shared_rank(addr, (uint32_t)k));
+            for (int k = 0; k < ksplit; ++k) v += parts[k * 128 + tid];
             if (t * 128 + tid < N) y[t * 128 + tid] = v;
         }
-        cluster_sync_all();   // keep every CTA's shared memory alive until it has been read
     }
 }
 

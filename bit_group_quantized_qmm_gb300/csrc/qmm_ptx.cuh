@@ -258,6 +258,11 @@ __device__ __forceinline__ uint32_t map_shared_rank(uint32_t addr, uint32_t rank
     return out;
 }
 
+__device__ __forceinline__ void st_shared_cluster_f32(uint32_t addr, float v)
+{
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
 __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr)
 {
     float v;
