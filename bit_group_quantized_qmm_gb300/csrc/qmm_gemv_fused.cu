@@ -83,8 +83,9 @@ __global__ void __launch_bounds__(kThreads)
     extern __shared__ __align__(128) uint8_t smem[];
     float* parts = reinterpret_cast<float*>(smem);                            // [kMaxCluster][128] (rank 0)
     float* red = parts + kMaxCluster * 128;                                    // [128]
-    int* flags = reinterpret_cast<int*>(red + 128);                            // [4]
-    uint64_t* full = reinterpret_cast<uint64_t*>(flags + 4);                   // [kMaxNg]
+    int* flags = reinterpret_cast<int*>(red + 128);                            // [2]
+    uint64_t* sums_in = reinterpret_cast<uint64_t*>(flags + 2);                // slices' sums arrived (rank 0)
+    uint64_t* full = sums_in + 1;                                              // [kMaxNg]
     uint8_t* stages = smem + kHeaderBytes;
     uint8_t* aperm = stages + (size_t)ring * C::CB;                            // permuted codes, ng*GROUP bytes
     float* sxs = reinterpret_cast<float*>(aperm + (size_t)ng * GROUP);        // [ng]
@@ -95,10 +96,17 @@ __global__ void __launch_bounds__(kThreads)
     pdl_trigger();
     if (tid == 0) {
         for (int i = 0; i < ring; ++i) mbar_init(&full[i], 1);
+        mbar_init(sums_in, ksplit > 1 ? ksplit - 1 : 1);
         flags[0] = 0;
         fence_barrier_init();
     }
-    __syncthreads();
+    // the other slices may arrive on sums_in only once it is initialised: a
+    // cluster barrier here, before the dependency wait, keeps it off the
+    // critical path
+    if (ksplit > 1)
+        cluster_sync_all();
+    else
+        __syncthreads();
 
     if (warp == kComputeThreads / 32) {
         // producer: the whole slice, before the dependency wait
@@ -114,73 +122,80 @@ __global__ void __launch_bounds__(kThreads)
         __syncwarp();
     } else {
         // ---------------------------------------------------------- phase A
+        // LPG lanes per group, 8 consecutive inputs per lane (one 8-block of
+        // the permuted code layout); GPW groups per warp.
         pdl_wait();
-        for (int i = warp; i < ng; i += kComputeThreads / 32) {
-            const int g = g0 + i;
-            const size_t base = (size_t)g * GROUP + (size_t)lane * C::E;
-            float v[C::E];
+        constexpr int LPG = GROUP / 8, GPW = 32 / LPG;
+        const int sub = lane / LPG, c8 = lane % LPG;
+        for (int i0 = warp * GPW; i0 < ng; i0 += (kComputeThreads / 32) * GPW) {
+            const int i = i0 + sub;
+            const bool valid = i < ng;
+            const int g = g0 + (valid ? i : 0);
+            const size_t base = (size_t)g * GROUP + (size_t)c8 * 8;
+            float v[8];
+            if (XDT == 0) {
+                const float4 p0 = reinterpret_cast<const float4*>(static_cast<const float*>(x) + base)[0];
+                const float4 p1 = reinterpret_cast<const float4*>(static_cast<const float*>(x) + base)[1];
+                v[0] = p0.x; v[1] = p0.y; v[2] = p0.z; v[3] = p0.w;
+                v[4] = p1.x; v[5] = p1.y; v[6] = p1.z; v[7] = p1.w;
+            } else {
 #pragma unroll
-            for (int e = 0; e < C::E; ++e) v[e] = load_in<XDT>(x, base + e);
+                for (int e = 0; e < 8; ++e) v[e] = load_in<XDT>(x, base + e);
+            }
             if (hadamard) {
+                // butterfly stages h = 1, 2, 4 inside the lane, 8 .. GROUP/2 across lanes
 #pragma unroll
-                for (int h = 1; h < GROUP; h <<= 1) {
-                    if (h < C::E) {
+                for (int h = 1; h < 8; h <<= 1)
 #pragma unroll
-                        for (int e = 0; e < C::E; ++e)
-                            if ((e & h) == 0) {
-                                const float lo = v[e], hi = v[e + h];
-                                v[e] = __fadd_rn(lo, hi);
-                                v[e + h] = __fsub_rn(lo, hi);
-                            }
-                    } else {
-                        const int lm = h / C::E;
-                        const bool upper = (lane & lm) != 0;
-#pragma unroll
-                        for (int e = 0; e < C::E; ++e) {
-                            const float o = __shfl_xor_sync(0xffffffffu, v[e], lm);
-                            v[e] = upper ? __fsub_rn(o, v[e]) : __fadd_rn(v[e], o);
+                    for (int e = 0; e < 8; ++e)
+                        if ((e & h) == 0) {
+                            const float lo = v[e], hi = v[e + h];
+                            v[e] = __fadd_rn(lo, hi);
+                            v[e + h] = __fsub_rn(lo, hi);
                         }
+#pragma unroll
+                for (int lm = 1; lm < LPG; lm <<= 1) {
+                    const bool upper = (c8 & lm) != 0;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float o = __shfl_xor_sync(0xffffffffu, v[e], lm);
+                        v[e] = upper ? __fsub_rn(o, v[e]) : __fadd_rn(v[e], o);
                     }
                 }
             }
             float amax = 0.f;
 #pragma unroll
-            for (int e = 0; e < C::E; ++e) amax = fmaxf(amax, fabsf(v[e]));
+            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(v[e]));
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            for (int o = 1; o < LPG; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
             float scale = 0.f;
-            int codes[C::E];
+            uint32_t b[8];
             if (amax == 0.f) {
 #pragma unroll
-                for (int e = 0; e < C::E; ++e) codes[e] = 0;
+                for (int e = 0; e < 8; ++e) b[e] = 0;
             } else {
                 const float sc = __fdiv_rn(amax, 127.0f);
 #pragma unroll
-                for (int e = 0; e < C::E; ++e) {
+                for (int e = 0; e < 8; ++e) {
                     float r = rintf(__fdiv_rn(v[e], sc));
                     r = fminf(fmaxf(r, -127.f), 127.f);
-                    codes[e] = (int)r;
+                    b[e] = (uint32_t)(int)r & 0xFFu;
                 }
                 scale = __fmul_rn(sc, rot_scale);
             }
-            // byte of local k within its 8-block in the dp4a order (k = 0, 4, 1, 5, 2, 6, 3, 7)
-#pragma unroll
-            for (int e = 0; e < C::E; ++e) {
-                const int k = lane * C::E + e;
-                aperm[(size_t)i * GROUP + (k & ~7) + 2 * (k & 3) + ((k >> 2) & 1)] = (uint8_t)(int8_t)codes[e];
-            }
-            if (a_out) {
-                uint32_t packed = 0;
-#pragma unroll
-                for (int e = 0; e < C::E; ++e) packed |= ((uint32_t)codes[e] & 0xFFu) << (8 * e);
-                if (C::E == 2)
-                    *reinterpret_cast<uint16_t*>(a_out + base) = (uint16_t)packed;
-                else
-                    *reinterpret_cast<uint32_t*>(a_out + base) = packed;
-            }
-            if (lane == 0) {
-                sxs[i] = scale;
-                if (sx_out) sx_out[g] = scale;
+            if (valid) {
+                // dp4a order of an 8-block: k = 0, 4, 1, 5 | 2, 6, 3, 7
+                const uint2 perm = make_uint2(b[0] | (b[4] << 8) | (b[1] << 16) | (b[5] << 24),
+                                              b[2] | (b[6] << 8) | (b[3] << 16) | (b[7] << 24));
+                *reinterpret_cast<uint2*>(aperm + (size_t)i * GROUP + (size_t)c8 * 8) = perm;
+                if (a_out)
+                    *reinterpret_cast<uint2*>(a_out + base) =
+                        make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24),
+                                   b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
+                if (c8 == 0) {
+                    sxs[i] = scale;
+                    if (sx_out) sx_out[g] = scale;
+                }
             }
         }
         compute_sync();
@@ -216,20 +231,23 @@ __global__ void __launch_bounds__(kThreads)
             if (ksplit == 1) {
                 if (t * 128 + r < N) y[t * 128 + r] = v;
             } else {
-                // push this slice's sums into the first CTA of the cluster
-                st_shared_cluster_f32(map_shared_rank(smem_u32(parts + s * 128 + r), 0u), v);
+                // this slice's sums go to the first CTA of the cluster
+                parts[s * 128 + r] = v;   // (rank 0 keeps its own locally)
+                if (s != 0) st_shared_cluster_f32(map_shared_rank(smem_u32(parts + s * 128 + r), 0u), v);
             }
         }
-    }
-
-    if (ksplit > 1) {
-        // the cluster is this tile's K-slices: after the barrier (release /
-        // acquire) the first CTA holds every slice's sums and adds them in order
-        cluster_sync_all();
-        if (s == 0 && tid < 128) {
-            float v = 0.f;
-            for (int k = 0; k < ksplit; ++k) v += parts[k * 128 + tid];
-            if (t * 128 + tid < N) y[t * 128 + tid] = v;
+        if (ksplit > 1) {
+            if (s != 0) {
+                // one release-arrive per slice on the first CTA's barrier
+                compute_sync();
+                if (tid == 0) mbar_arrive_remote(map_shared_rank(smem_u32(sums_in), 0u));
+            } else if (tid < 128) {
+                // the first CTA adds the slices in order once all have arrived
+                mbar_wait_cluster(sums_in, 0, status);
+                float v = 0.f;
+                for (int k = 0; k < ksplit; ++k) v += parts[k * 128 + tid];
+                if (t * 128 + tid < N) y[t * 128 + tid] = v;
+            }
         }
     }
 }
