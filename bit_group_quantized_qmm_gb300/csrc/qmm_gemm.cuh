@@ -14,14 +14,15 @@
 // are exact, and a 64- or 128-wide group sum stays below 2^24, so the fp32
 // accumulator holds the exact int32 group partial. Weights sit in the MMA's M
 // slot (128 rows of the packed tile), activations in its N slot (m_tile rows,
-// 16..224), so one kernel serves decode-sized and prefill-sized M.
+// 16..128), so one kernel serves decode-sized and prefill-sized M.
 //
 // Warp roles (512 threads, one CTA per SM, persistent over tiles):
 //   warps 0-3   expand: packed nibbles (smem) -> fp16 weight operand, written
 //               to tensor memory with tcgen05.st (or to 128-byte-swizzled
 //               shared memory); one tensor-memory lane quadrant per warp
 //   warps 4-11  epilogue: read each group's partials from tensor memory,
-//               rescale in fp32 into register accumulators, store Y
+//               rescale in fp32 into register accumulators (at most 64 per
+//               thread: m_tile <= 128, two warpgroups), store Y
 //   warp 12     producer: 1-D bulk copies of packed chunks, TMA tiles of the
 //               fp16 activations (128-byte swizzle)
 //   warp 13     MMA issuer; owns the tensor-memory allocation
@@ -39,27 +40,43 @@ namespace qmm {
 
 constexpr int kGemmThreads = 512;
 
-template <int VARIANT, int GROUP>
+// Pipeline depths. Narrow tiles (m_tile <= 64: decode-sized M) are bound by
+// the latency of the expand -> MMA -> epilogue hand-offs, so they keep more
+// k-steps and groups in flight; wide tiles are bound by tensor-memory space.
+template <int VARIANT, int GROUP, int MAXC>
 struct GemmCfg {
+    static constexpr bool NARROW = MAXC <= 32;
     static constexpr int CB = 64 * GROUP + 256 + (VARIANT == 1 ? 256 : 0);
-    static constexpr int KSG = GROUP / 64;              // 64-wide k-steps per group
-    static constexpr int RS = GROUP == 128 ? 6 : 8;     // packed-chunk stages
-    static constexpr int BS = 4;                         // activation stages
-    static constexpr int AS = 2;                         // weight-operand stages
-    static constexpr int XS = 4;                         // activation-scale stages
+    static constexpr int KSG = GROUP / 64;                                   // 64-wide k-steps per group
+    static constexpr int RS = NARROW ? (GROUP == 128 ? 10 : 16) : (GROUP == 128 ? 6 : 8);   // packed chunks
+    static constexpr int BS = NARROW ? 6 : 4;                                // activation tiles
+    static constexpr int AS = NARROW ? 4 : 2;                                // weight-operand stages
+    static constexpr int DS = NARROW ? 4 : 2;                                // accumulator buffers
+    static constexpr int XS = NARROW ? 8 : 4;                                // activation-scale stages
 };
 
-template <int VARIANT, int GROUP>
+template <int VARIANT, int GROUP, int MAXC>
 inline size_t gemm_smem_bytes(int m_tile, bool a_in_smem)
 {
-    using C = GemmCfg<VARIANT, GROUP>;
+    using C = GemmCfg<VARIANT, GROUP, MAXC>;
     size_t b = 1024;                                     // alignment slack
     b += (size_t)C::BS * m_tile * 128;
     if (a_in_smem) b += (size_t)C::AS * 16384;
     b += (size_t)C::RS * C::CB;
     b += (size_t)C::XS * m_tile * 4;
-    b += 8 * (2 * C::RS + 2 * C::BS + 2 * C::AS + 4 + 2 * C::XS + 1) + 64;
+    b += 8 * (2 * C::RS + 2 * C::BS + 2 * C::AS + 2 * C::DS + 2 * C::XS + 1) + 64;
     return b;
+}
+
+// Tensor-memory columns: DS accumulators (+ AS weight-operand stages).
+template <int VARIANT, int GROUP, int MAXC>
+inline int gemm_tmem_cols(int d_stride, bool a_in_smem)
+{
+    using C = GemmCfg<VARIANT, GROUP, MAXC>;
+    const int cols = C::DS * d_stride + (a_in_smem ? 0 : 32 * C::AS);
+    int alloc = 32;
+    while (alloc < cols) alloc <<= 1;
+    return alloc;
 }
 
 // fp16 pairs (k, k+1) of one packed word (slot order of the blob): exact
@@ -95,7 +112,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap act_map, const GemmShape sh, const uint8_t* __restrict__ blob,
                 const float* __restrict__ act_scale, float* __restrict__ Y, int32_t* __restrict__ P, int* status)
 {
-    using C = GemmCfg<VARIANT, GROUP>;
+    using C = GemmCfg<VARIANT, GROUP, MAXC>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int m_tile = sh.m_tile;
@@ -113,8 +130,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t* a_full = b_empty + C::BS;
     uint64_t* a_empty = a_full + C::AS;
     uint64_t* d_full = a_empty + C::AS;
-    uint64_t* d_empty = d_full + 2;
-    uint64_t* x_full = d_empty + 2;
+    uint64_t* d_empty = d_full + C::DS;
+    uint64_t* x_full = d_empty + C::DS;
     uint64_t* x_empty = x_full + C::XS;
     uint64_t* done = x_empty + C::XS;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
@@ -136,7 +153,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(&a_full[i], 4);      // expand warps
             mbar_init(&a_empty[i], 1);     // MMA commit
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < C::DS; ++i) {
             mbar_init(&d_full[i], 1);      // MMA commit
             mbar_init(&d_empty[i], 8);     // epilogue warps
         }
@@ -206,8 +223,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < sh.num_tiles; tile += gridDim.x) {
                 for (int g = 0; ok && g < G; ++g) {
-                    const int db = dc & 1;
-                    if (!mbar_wait(&d_empty[db], ((dc >> 1) & 1) ^ 1, status, abort)) {
+                    const int db = dc % C::DS;
+                    if (!mbar_wait(&d_empty[db], ((dc / C::DS) & 1) ^ 1, status, abort)) {
                         ok = false;
                         break;
                     }
@@ -226,7 +243,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         for (int kk = 0; kk < 4; ++kk) {
                             const uint32_t accum = (j > 0 || kk > 0) ? 1u : 0u;
                             if (A_TMEM) {
-                                const uint32_t a_tmem = tmem + (uint32_t)(2 * sh.d_stride + 32 * as + 8 * kk);
+                                const uint32_t a_tmem = tmem + (uint32_t)(C::DS * sh.d_stride + 32 * as + 8 * kk);
                                 mma_f16_ts(d_tmem, a_tmem, bdesc + 2 * kk, idesc, accum);
                             } else {
                                 const uint64_t adesc = sdesc_sw128(smem_u32(ast + (size_t)as * 16384));
@@ -304,7 +321,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     expand_word<OFF>(p1.w, hv + 28);
                     if (A_TMEM) {
                         const uint32_t taddr =
-                            tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(2 * sh.d_stride + 32 * as);
+                            tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(C::DS * sh.d_stride + 32 * as);
                         tmem_st32(taddr, hv);
                         tmem_st_wait();
                         tc_fence_before();
@@ -342,8 +359,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
             for (int c = 0; c < MAXC; ++c) acc[c] = 0.f;
             for (int g = 0; g < G; ++g) {
-                const int db = dc & 1, rs = rc % C::RS, xsi = xc % C::XS;
-                if (!mbar_wait(&d_full[db], (dc >> 1) & 1, status, abort) ||
+                const int db = dc % C::DS, rs = rc % C::RS, xsi = xc % C::XS;
+                if (!mbar_wait(&d_full[db], (dc / C::DS) & 1, status, abort) ||
                     !mbar_wait(&raw_full[rs], (rc / C::RS) & 1, status, abort) ||
                     !mbar_wait(&x_full[xsi], (xc / C::XS) & 1, status, abort)) {
                     ok = false;
@@ -356,23 +373,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     VARIANT == 1 ? __half2float(reinterpret_cast<const __half*>(ch + 64 * GROUP + 256)[r]) : 0.f;
                 const float* sxv = xs + (size_t)xsi * m_tile + c0;
                 const uint32_t dcol = lane_base + (uint32_t)(db * sh.d_stride + c0);
+                // BATCH columns at a time: up to BATCH/8 loads of 8 columns, one wait
+                constexpr int BATCH = MAXC <= 32 ? 32 : 16;
 #pragma unroll
-                for (int cb = 0; cb < MAXC; cb += 8) {
+                for (int cb = 0; cb < MAXC; cb += BATCH) {
                     if (cb < ncol) {
-                        uint32_t v[8];
-                        tmem_ld8(dcol + cb, v);
-                        tmem_ld_wait(v);
+                        uint32_t v[32];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const float pv = __uint_as_float(v[e]);
-                            if (DEBUG) {
-                                const int m = m0 + cb + e;
-                                if (m < sh.M && n < sh.N && cb + e < ncol)
-                                    P[((size_t)m * sh.N + n) * G + g] = __float2int_rn(pv);
-                            } else if (VARIANT == 0) {
-                                acc[cb + e] = fmaf(pv * sxv[cb + e], sw, acc[cb + e]);
-                            } else {
-                                acc[cb + e] = fmaf(pv, sw, fmaf(sxv[cb + e], bw, acc[cb + e]));
+                        for (int q8 = 0; q8 < BATCH / 8; ++q8)
+                            if (cb + 8 * q8 < MAXC && cb + 8 * q8 < ncol) tmem_ld8_at(dcol + cb + 8 * q8, v, 8 * q8);
+                        tmem_ld_wait32(v);
+#pragma unroll
+                        for (int e4 = 0; e4 < BATCH; e4 += 4) {
+                            if (cb + e4 < MAXC && cb + e4 < ncol) {
+                                const float4 s4 = *reinterpret_cast<const float4*>(sxv + cb + e4);
+                                const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const int c = cb + e4 + e;
+                                    const float pv = __uint_as_float(v[e4 + e]);
+                                    if (DEBUG) {
+                                        const int m = m0 + c;
+                                        if (m < sh.M && n < sh.N)
+                                            P[((size_t)m * sh.N + n) * G + g] = __float2int_rn(pv);
+                                    } else if (VARIANT == 0) {
+                                        acc[c] = fmaf(pv * sv[e], sw, acc[c]);
+                                    } else {
+                                        acc[c] = fmaf(pv, sw, fmaf(sv[e], bw, acc[c]));
+                                    }
+                                }
                             }
                         }
                     }
@@ -409,11 +438,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 // Host side: configure and launch one instance of gemm_kernel.
 template <int VARIANT, int GROUP, bool A_TMEM, bool DEBUG, int MAXC>
-cudaError_t run_gemm(const LaunchCtx& c, const CUtensorMap& map, const GemmShape& sh, const uint8_t* blob,
+cudaError_t run_gemm(const LaunchCtx& c, const CUtensorMap& map, const GemmShape& sh_in, const uint8_t* blob,
                      const float* act_scale, float* Y, int32_t* P)
 {
     auto kern = gemm_kernel<VARIANT, GROUP, A_TMEM, DEBUG, MAXC>;
-    const size_t smem = gemm_smem_bytes<VARIANT, GROUP>(sh.m_tile, !A_TMEM);
+    GemmShape sh = sh_in;
+    sh.tmem_cols = gemm_tmem_cols<VARIANT, GROUP, MAXC>(sh.d_stride, !A_TMEM);
+    const size_t smem = gemm_smem_bytes<VARIANT, GROUP, MAXC>(sh.m_tile, !A_TMEM);
     static size_t configured = 0;
     cudaError_t e;
     if (smem > configured) {

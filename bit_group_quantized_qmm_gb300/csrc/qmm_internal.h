@@ -54,7 +54,7 @@ cudaError_t launch_gemv(const LaunchCtx& c, int N, int K, int group, const uint8
                         const float* sx, float* y, int32_t* P_debug, void* ws, size_t ws_bytes);
 
 // Largest activation-row tile of the tensor-core GEMM (MMA N).
-constexpr int kMaxMTile = 224;
+constexpr int kMaxMTile = 128;
 
 // One-kernel decode GEMV: prepass of x and GEMV (optional code/scale outputs).
 cudaError_t launch_gemv_fused(const LaunchCtx& c, int N, int K, int group, int hadamard, const uint8_t* blob,
@@ -62,7 +62,7 @@ cudaError_t launch_gemv_fused(const LaunchCtx& c, int N, int K, int group, int h
 
 struct GemmShape {
     int M, N, K;
-    int m_tile;      // activation rows per tile (MMA N), multiple of 16, <= 224
+    int m_tile;      // activation rows per tile (MMA N), multiple of 16, <= kMaxMTile
     int mt_count;    // ceil(M / m_tile)
     int num_tiles;   // row tiles x mt_count
     int d_stride;    // tensor-memory columns per accumulator buffer
