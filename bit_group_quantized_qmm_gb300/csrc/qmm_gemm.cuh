@@ -267,6 +267,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else if (warp == 14) {
         // ---------------------------------------------------------- scale loader
         pdl_wait();
+        // no copy may still be landing when the CTA exits (checked below)
         int xc = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < sh.num_tiles; tile += gridDim.x) {
@@ -278,16 +279,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     ok = false;
                     break;
                 }
+                // asynchronous copies: the loader never waits for the data, the
+                // slot's barrier completes when every lane's copies have landed
                 float* dst = xs + (size_t)s * m_tile;
                 for (int c = lane; c < m_tile; c += 32) {
                     const int m = m0 + c;
-                    // the partials hook passes no scales
-                    dst[c] = (!DEBUG && m < sh.M) ? act_scale[(size_t)m * G + g] : 0.f;
+                    // rows beyond M, and the partials hook (no scales), read nothing: zero
+                    const bool have = !DEBUG && m < sh.M;
+                    cp_async_4(dst + c, have ? static_cast<const void*>(act_scale + (size_t)m * G + g)
+                                             : static_cast<const void*>(blob),
+                               have ? 4u : 0u);
                 }
-                mbar_arrive(&x_full[s]);
+                cp_async_arrive(&x_full[s]);
                 ++xc;
             }
         }
+        asm volatile("cp.async.wait_all;" ::: "memory");
     } else if (warp < 4) {
         // ---------------------------------------------------------- expand
         const int r = threadIdx.x;   // weight row within the tile == tensor-memory lane

@@ -110,6 +110,21 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
+// 4-byte asynchronous copy global -> shared; src_bytes = 0 writes zero
+// (nothing is read).
+__device__ __forceinline__ void cp_async_4(void* dst, const void* src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+// Arrive on `bar` once all of this thread's earlier cp.async copies have
+// landed (the arrival is counted in the barrier's initial count).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // 2-D tiled tensor-map load (box defined by the map) at coordinates (c0, c1).
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar)
 {
