@@ -23,10 +23,12 @@
 //   warps 4-11  epilogue: read each group's partials from tensor memory,
 //               rescale in fp32 into register accumulators (at most 64 per
 //               thread: m_tile <= 128, two warpgroups), store Y
-//   warp 12     producer: 1-D bulk copies of packed chunks, TMA tiles of the
-//               fp16 activations (128-byte swizzle)
+//   warp 12     weight producer: 1-D bulk copies of packed chunks
 //   warp 13     MMA issuer; owns the tensor-memory allocation
-//   warp 14     activation-scale loader (sx or S per group)
+//   warp 14     activation-scale loader (sx or S per group, cp.async)
+//   warp 15     activation producer: TMA tiles of the fp16 activations
+//               (128-byte swizzle), in a ring deep enough that these small
+//               loads never wait behind the weight chunks
 // Accumulators are double-buffered per group in tensor memory so the MMAs of
 // group g+1 run while the epilogue rescales group g. Every wait is bounded.
 #pragma once
@@ -49,18 +51,34 @@ struct GemmCfg {
     static constexpr int CB = 64 * GROUP + 256 + (VARIANT == 1 ? 256 : 0);
     static constexpr int KSG = GROUP / 64;                                   // 64-wide k-steps per group
     static constexpr int RS = NARROW ? (GROUP == 128 ? 10 : 16) : (GROUP == 128 ? 6 : 8);   // packed chunks
-    static constexpr int BS = NARROW ? 6 : 4;                                // activation tiles
+    static constexpr int BS = NARROW ? 32 : 4;                               // activation tiles (max)
     static constexpr int AS = NARROW ? 4 : 2;                                // weight-operand stages
     static constexpr int DS = NARROW ? 4 : 2;                                // accumulator buffers
     static constexpr int XS = NARROW ? 8 : 4;                                // activation-scale stages
 };
+
+// Activation-tile stages: the instance's maximum, as far as shared memory
+// allows next to the other rings (narrow tiles keep many in flight so the
+// small tensor-map loads never wait behind the weight chunks).
+template <int VARIANT, int GROUP, int MAXC>
+inline int gemm_stages_b(int m_tile, bool a_in_smem)
+{
+    using C = GemmCfg<VARIANT, GROUP, MAXC>;
+    const size_t fixed = 1024 + (a_in_smem ? (size_t)C::AS * 16384 : 0) + (size_t)C::RS * C::CB +
+                         (size_t)C::XS * m_tile * 4 + 8 * (2 * C::RS + 2 * C::BS + 2 * C::AS + 2 * C::DS + 2 * C::XS + 1) + 64;
+    const size_t budget = 220 * 1024;
+    int bs = (int)((budget - fixed) / ((size_t)m_tile * 128));
+    if (bs > C::BS) bs = C::BS;
+    if (bs < 2) bs = 2;
+    return bs;
+}
 
 template <int VARIANT, int GROUP, int MAXC>
 inline size_t gemm_smem_bytes(int m_tile, bool a_in_smem)
 {
     using C = GemmCfg<VARIANT, GROUP, MAXC>;
     size_t b = 1024;                                     // alignment slack
-    b += (size_t)C::BS * m_tile * 128;
+    b += (size_t)gemm_stages_b<VARIANT, GROUP, MAXC>(m_tile, a_in_smem) * m_tile * 128;
     if (a_in_smem) b += (size_t)C::AS * 16384;
     b += (size_t)C::RS * C::CB;
     b += (size_t)C::XS * m_tile * 4;
@@ -118,7 +136,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int m_tile = sh.m_tile;
     const int b_bytes = m_tile * 128;
     uint8_t* bst = base;
-    uint8_t* ast = bst + (size_t)C::BS * b_bytes;
+    const int BSr = sh.bs;   // activation stages in use
+    uint8_t* ast = bst + (size_t)BSr * b_bytes;
     uint8_t* raw = ast + (A_TMEM ? 0 : C::AS * 16384);
     float* xs = reinterpret_cast<float*>(raw + (size_t)C::RS * C::CB);
     uint64_t* bars =
@@ -145,7 +164,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(&raw_full[i], 1);
             mbar_init(&raw_empty[i], 8);   // epilogue warps
         }
-        for (int i = 0; i < C::BS; ++i) {
+        for (int i = 0; i < BSr; ++i) {
             mbar_init(&b_full[i], 1);
             mbar_init(&b_empty[i], 1);     // MMA commit
         }
@@ -165,7 +184,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         *abort = 0;
         fence_barrier_init();
     }
-    if (warp == 12 && lane == 0) prefetch_tensormap(&act_map);
+    if (warp == 15 && lane == 0) prefetch_tensormap(&act_map);
     if (warp == 13) {
         tmem_alloc(tmem_slot, (uint32_t)sh.tmem_cols);
         tmem_relinquish();
@@ -177,13 +196,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     pdl_trigger();
 
     if (warp == 12) {
-        // ---------------------------------------------------------- producer
+        // ---------------------------------------------------------- weight producer
         if (lane == 0) {
-            int rc = 0, bc = 0;
-            bool waited = false, ok = true;
+            int rc = 0;
+            bool ok = true;
             for (int tile = blockIdx.x; ok && tile < sh.num_tiles; tile += gridDim.x) {
-                const int nt = tile / sh.mt_count, mt = tile % sh.mt_count;
-                for (int g = 0; ok && g < G; ++g) {
+                const int nt = tile / sh.mt_count;
+                for (int g = 0; g < G; ++g) {
                     const int rs = rc % C::RS;
                     if (!mbar_wait(&raw_empty[rs], ((rc / C::RS) & 1) ^ 1, status, abort)) {
                         ok = false;
@@ -192,28 +211,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     mbar_arrive_expect_tx(&raw_full[rs], C::CB);
                     bulk_g2s(raw + (size_t)rs * C::CB, blob + ((size_t)nt * G + g) * C::CB, C::CB, &raw_full[rs]);
                     ++rc;
-                    for (int j = 0; j < C::KSG; ++j) {
-                        if (!waited) {
-                            pdl_wait();   // activations come from the previous kernel
-                            waited = true;
-                        }
-                        const int bs = bc % C::BS;
-                        if (!mbar_wait(&b_empty[bs], ((bc / C::BS) & 1) ^ 1, status, abort)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive_expect_tx(&b_full[bs], (uint32_t)b_bytes);
-                        tma_load_2d(bst + (size_t)bs * b_bytes, &act_map, g * GROUP + 64 * j, mt * m_tile,
-                                    &b_full[bs]);
-                        ++bc;
-                    }
                 }
             }
             // no copy may still be landing when the CTA exits
             for (int i = rc - C::RS > 0 ? rc - C::RS : 0; i < rc; ++i)
                 mbar_wait(&raw_full[i % C::RS], (i / C::RS) & 1, status, nullptr);
-            for (int i = bc - C::BS > 0 ? bc - C::BS : 0; i < bc; ++i)
-                mbar_wait(&b_full[i % C::BS], (i / C::BS) & 1, status, nullptr);
+        }
+    } else if (warp == 15) {
+        // ---------------------------------------------------------- activation producer
+        if (lane == 0) {
+            pdl_wait();   // activations come from the previous kernel
+            int bc = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < sh.num_tiles; tile += gridDim.x) {
+                const int mt = tile % sh.mt_count;
+                for (int kstep = 0; kstep < G * C::KSG; ++kstep) {
+                    const int bs = bc % BSr;
+                    if (!mbar_wait(&b_empty[bs], ((bc / BSr) & 1) ^ 1, status, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&b_full[bs], (uint32_t)b_bytes);
+                    tma_load_2d(bst + (size_t)bs * b_bytes, &act_map, kstep * 64, mt * m_tile, &b_full[bs]);
+                    ++bc;
+                }
+            }
+            for (int i = bc - BSr > 0 ? bc - BSr : 0; i < bc; ++i)
+                mbar_wait(&b_full[i % BSr], (i / BSr) & 1, status, nullptr);
         }
     } else if (warp == 13) {
         // ---------------------------------------------------------- MMA issuer
@@ -231,9 +255,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tc_fence_after();
                     const uint32_t d_tmem = tmem + (uint32_t)(db * sh.d_stride);
                     for (int j = 0; j < C::KSG; ++j) {
-                        const int as = ac % C::AS, bs = bc % C::BS;
+                        const int as = ac % C::AS, bs = bc % BSr;
                         if (!mbar_wait(&a_full[as], (ac / C::AS) & 1, status, abort) ||
-                            !mbar_wait(&b_full[bs], (bc / C::BS) & 1, status, abort)) {
+                            !mbar_wait(&b_full[bs], (bc / BSr) & 1, status, abort)) {
                             ok = false;
                             break;
                         }
@@ -381,7 +405,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const float* sxv = xs + (size_t)xsi * m_tile + c0;
                 const uint32_t dcol = lane_base + (uint32_t)(db * sh.d_stride + c0);
                 // BATCH columns at a time: up to BATCH/8 loads of 8 columns, one wait
-                constexpr int BATCH = MAXC <= 32 ? 32 : 16;
+                constexpr int BATCH = 32;
 #pragma unroll
                 for (int cb = 0; cb < MAXC; cb += BATCH) {
                     if (cb < ncol) {
@@ -451,6 +475,7 @@ cudaError_t run_gemm(const LaunchCtx& c, const CUtensorMap& map, const GemmShape
     auto kern = gemm_kernel<VARIANT, GROUP, A_TMEM, DEBUG, MAXC>;
     GemmShape sh = sh_in;
     sh.tmem_cols = gemm_tmem_cols<VARIANT, GROUP, MAXC>(sh.d_stride, !A_TMEM);
+    sh.bs = gemm_stages_b<VARIANT, GROUP, MAXC>(sh.m_tile, !A_TMEM);
     const size_t smem = gemm_smem_bytes<VARIANT, GROUP, MAXC>(sh.m_tile, !A_TMEM);
     static size_t configured = 0;
     cudaError_t e;
