@@ -51,9 +51,9 @@ struct GemmCfg {
     static constexpr int CB = 64 * GROUP + 256 + (VARIANT == 1 ? 256 : 0);
     static constexpr int KSG = GROUP / 64;                                   // 64-wide k-steps per group
     static constexpr int RS = NARROW ? (GROUP == 128 ? 10 : 16) : (GROUP == 128 ? 6 : 8);   // packed chunks
-    static constexpr int BS = NARROW ? 32 : 4;                               // activation tiles (max)
+    static constexpr int BS = NARROW ? 8 : 4;                                // activation tiles (max)
     static constexpr int AS = NARROW ? 4 : 2;                                // weight-operand stages
-    static constexpr int DS = NARROW ? 4 : 2;                                // accumulator buffers
+    static constexpr int DS = NARROW ? 4 : 3;                                // accumulator buffers
     static constexpr int XS = NARROW ? 8 : 4;                                // activation-scale stages
 };
 
@@ -123,6 +123,43 @@ __device__ __forceinline__ void expand_word(uint32_t w, uint32_t* out)
     out[1] = *reinterpret_cast<uint32_t*>(&r1);
     out[2] = *reinterpret_cast<uint32_t*>(&r2);
     out[3] = *reinterpret_cast<uint32_t*>(&r3);
+}
+
+// Packed fp32 pairs (fma.rn.f32x2 / mul.rn.f32x2: two lanes of fp32 per
+// instruction; each element rounds exactly as the scalar operation).
+__device__ __forceinline__ unsigned long long pack2(float a, float b)
+{
+    return (unsigned long long)__float_as_uint(a) | ((unsigned long long)__float_as_uint(b) << 32);
+}
+
+// (p0 * s0, p1 * s1) for raw fp32 bit patterns p0, p1
+__device__ __forceinline__ unsigned long long mul_pair(uint32_t p0, uint32_t p1, float s0, float s1)
+{
+    unsigned long long d;
+    const unsigned long long a = (unsigned long long)p0 | ((unsigned long long)p1 << 32);
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(pack2(s0, s1)));
+    return d;
+}
+
+// (acc0, acc1) += t * (w, w)
+__device__ __forceinline__ void fma_pair(float& acc0, float& acc1, unsigned long long t, float w)
+{
+    unsigned long long c = pack2(acc0, acc1), d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(t), "l"(pack2(w, w)), "l"(c));
+    acc0 = __uint_as_float((uint32_t)d);
+    acc1 = __uint_as_float((uint32_t)(d >> 32));
+}
+
+// (acc0, acc1) += (v0, v1) * (w, w)
+__device__ __forceinline__ void fma_pair_v(float& acc0, float& acc1, float v0, float v1, float w)
+{
+    fma_pair(acc0, acc1, pack2(v0, v1), w);
+}
+
+// (acc0, acc1) += (p0, p1) * (w, w) for raw fp32 bit patterns
+__device__ __forceinline__ void fma_pair_u(float& acc0, float& acc1, uint32_t p0, uint32_t p1, float w)
+{
+    fma_pair(acc0, acc1, (unsigned long long)p0 | ((unsigned long long)p1 << 32), w);
 }
 
 template <int VARIANT, int GROUP, bool A_TMEM, bool DEBUG, int MAXC>
@@ -418,20 +455,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         for (int e4 = 0; e4 < BATCH; e4 += 4) {
                             if (cb + e4 < MAXC && cb + e4 < ncol) {
                                 const float4 s4 = *reinterpret_cast<const float4*>(sxv + cb + e4);
-                                const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
+                                const int c = cb + e4;
+                                if (DEBUG) {
 #pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const int c = cb + e4 + e;
-                                    const float pv = __uint_as_float(v[e4 + e]);
-                                    if (DEBUG) {
-                                        const int m = m0 + c;
+                                    for (int e = 0; e < 4; ++e) {
+                                        const int m = m0 + c + e;
                                         if (m < sh.M && n < sh.N)
-                                            P[((size_t)m * sh.N + n) * G + g] = __float2int_rn(pv);
-                                    } else if (VARIANT == 0) {
-                                        acc[c] = fmaf(pv * sv[e], sw, acc[c]);
-                                    } else {
-                                        acc[c] = fmaf(pv, sw, fmaf(sv[e], bw, acc[c]));
+                                            P[((size_t)m * sh.N + n) * G + g] = __float2int_rn(__uint_as_float(v[e4 + e]));
                                     }
+                                } else if (VARIANT == 0) {
+                                    // acc += (P * sx) * sw, two columns per packed instruction
+                                    fma_pair(acc[c], acc[c + 1], mul_pair(v[e4], v[e4 + 1], s4.x, s4.y), sw);
+                                    fma_pair(acc[c + 2], acc[c + 3], mul_pair(v[e4 + 2], v[e4 + 3], s4.z, s4.w), sw);
+                                } else {
+                                    // acc += S * b + P * s
+                                    fma_pair_v(acc[c], acc[c + 1], s4.x, s4.y, bw);
+                                    fma_pair_v(acc[c + 2], acc[c + 3], s4.z, s4.w, bw);
+                                    fma_pair_u(acc[c], acc[c + 1], v[e4], v[e4 + 1], sw);
+                                    fma_pair_u(acc[c + 2], acc[c + 3], v[e4 + 2], v[e4 + 3], sw);
                                 }
                             }
                         }

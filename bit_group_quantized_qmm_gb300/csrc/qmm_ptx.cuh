@@ -13,8 +13,8 @@ namespace qmm {
 // Device error word bits (read back by qmm_device_status).
 constexpr int kErrTimeout = 1;
 
-// A bounded wait gives up after this many nanoseconds of %globaltimer.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// A bounded wait gives up after this many SM clock cycles.
+constexpr long long kWaitLimitCycles = 4000000000ll;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p)
 {
@@ -80,20 +80,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
     return ok != 0;
 }
 
-// Wait for the phase of `bar` with the given parity to complete. Gives up
-// after kWaitLimitNs, or as soon as *abort (shared, may be null) is set; on
+// Wait for the phase of `bar` with the given parity to complete. The loop
+// polls only the barrier; every 256 polls it looks at the SM cycle counter and
+// the CTA's abort flag. It gives up after kWaitLimitCycles cycles (about 2-4 s
+// at GB300 clocks), or as soon as *abort (shared, may be null) is set; on
 // giving up it sets kErrTimeout in *status and *abort and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status, volatile int* abort)
 {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
+    const long long t0 = clock64();
+    for (uint32_t spin = 1;; ++spin) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (abort && *abort) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-            if (status) atomicOr(status, kErrTimeout);
-            if (abort) *abort = 1;
-            return false;
+        if ((spin & 255u) == 0) {
+            if (abort && *abort) return false;
+            if (clock64() - t0 > kWaitLimitCycles) {
+                if (status) atomicOr(status, kErrTimeout);
+                if (abort) *abort = 1;
+                return false;
+            }
         }
     }
 }
@@ -335,10 +339,10 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, int* status)
 {
     if (mbar_try_wait_cluster(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
+    const long long t0 = clock64();
+    for (uint32_t spin = 1;; ++spin) {
         if (mbar_try_wait_cluster(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if ((spin & 255u) == 0 && clock64() - t0 > kWaitLimitCycles) {
             if (status) atomicOr(status, kErrTimeout);
             return false;
         }
