@@ -51,38 +51,31 @@ struct GemmCfg {
     static constexpr int CB = 64 * GROUP + 256 + (VARIANT == 1 ? 256 : 0);
     static constexpr int KSG = GROUP / 64;                                   // 64-wide k-steps per group
     static constexpr int RS = NARROW ? (GROUP == 128 ? 10 : 16) : (GROUP == 128 ? 6 : 8);   // packed chunks
-    static constexpr int BS = NARROW ? 8 : 4;                                // activation tiles (max)
-    static constexpr int AS = NARROW ? 4 : 2;                                // weight-operand stages
+    static constexpr int KS = NARROW ? 8 : 4;   // k-step stages: weight operand + activation tile together
     static constexpr int DS = NARROW ? 4 : 3;                                // accumulator buffers
     static constexpr int XS = NARROW ? 8 : 4;                                // activation-scale stages
 };
 
-// Activation-tile stages: the instance's maximum, as far as shared memory
-// allows next to the other rings (narrow tiles keep many in flight so the
-// small tensor-map loads never wait behind the weight chunks).
+// k-step stages in use: the weight operand in shared memory takes 16 KB per
+// stage, so that variant keeps fewer.
 template <int VARIANT, int GROUP, int MAXC>
-inline int gemm_stages_b(int m_tile, bool a_in_smem)
+inline int gemm_kstages(bool a_in_smem)
 {
     using C = GemmCfg<VARIANT, GROUP, MAXC>;
-    const size_t fixed = 1024 + (a_in_smem ? (size_t)C::AS * 16384 : 0) + (size_t)C::RS * C::CB +
-                         (size_t)C::XS * m_tile * 4 + 8 * (2 * C::RS + 2 * C::BS + 2 * C::AS + 2 * C::DS + 2 * C::XS + 1) + 64;
-    const size_t budget = 220 * 1024;
-    int bs = (int)((budget - fixed) / ((size_t)m_tile * 128));
-    if (bs > C::BS) bs = C::BS;
-    if (bs < 2) bs = 2;
-    return bs;
+    return a_in_smem && C::KS > 4 ? 4 : C::KS;
 }
 
 template <int VARIANT, int GROUP, int MAXC>
 inline size_t gemm_smem_bytes(int m_tile, bool a_in_smem)
 {
     using C = GemmCfg<VARIANT, GROUP, MAXC>;
+    const int ks = gemm_kstages<VARIANT, GROUP, MAXC>(a_in_smem);
     size_t b = 1024;                                     // alignment slack
-    b += (size_t)gemm_stages_b<VARIANT, GROUP, MAXC>(m_tile, a_in_smem) * m_tile * 128;
-    if (a_in_smem) b += (size_t)C::AS * 16384;
+    b += (size_t)ks * m_tile * 128;
+    if (a_in_smem) b += (size_t)ks * 16384;
     b += (size_t)C::RS * C::CB;
     b += (size_t)C::XS * m_tile * 4;
-    b += 8 * (2 * C::RS + 2 * C::BS + 2 * C::AS + 2 * C::DS + 2 * C::XS + 1) + 64;
+    b += 8 * (2 * C::RS + 2 * C::KS + 2 * C::DS + 2 * C::XS + 1) + 64;
     return b;
 }
 
@@ -91,7 +84,7 @@ template <int VARIANT, int GROUP, int MAXC>
 inline int gemm_tmem_cols(int d_stride, bool a_in_smem)
 {
     using C = GemmCfg<VARIANT, GROUP, MAXC>;
-    const int cols = C::DS * d_stride + (a_in_smem ? 0 : 32 * C::AS);
+    const int cols = C::DS * d_stride + (a_in_smem ? 0 : 32 * C::KS);
     int alloc = 32;
     while (alloc < cols) alloc <<= 1;
     return alloc;
@@ -173,19 +166,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int m_tile = sh.m_tile;
     const int b_bytes = m_tile * 128;
     uint8_t* bst = base;
-    const int BSr = sh.bs;   // activation stages in use
-    uint8_t* ast = bst + (size_t)BSr * b_bytes;
-    uint8_t* raw = ast + (A_TMEM ? 0 : C::AS * 16384);
+    const int KSr = sh.bs;   // k-step stages in use
+    uint8_t* ast = bst + (size_t)KSr * b_bytes;
+    uint8_t* raw = ast + (A_TMEM ? 0 : (size_t)KSr * 16384);
     float* xs = reinterpret_cast<float*>(raw + (size_t)C::RS * C::CB);
     uint64_t* bars =
         reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(xs + C::XS * m_tile) + 7) & ~uintptr_t(7));
     uint64_t* raw_full = bars;
     uint64_t* raw_empty = raw_full + C::RS;
-    uint64_t* b_full = raw_empty + C::RS;
-    uint64_t* b_empty = b_full + C::BS;
-    uint64_t* a_full = b_empty + C::BS;
-    uint64_t* a_empty = a_full + C::AS;
-    uint64_t* d_full = a_empty + C::AS;
+    uint64_t* k_full = raw_empty + C::RS;    // weight operand expanded + activation tile landed
+    uint64_t* k_empty = k_full + C::KS;      // the k-step's MMAs retired
+    uint64_t* d_full = k_empty + C::KS;
     uint64_t* d_empty = d_full + C::DS;
     uint64_t* x_full = d_empty + C::DS;
     uint64_t* x_empty = x_full + C::XS;
@@ -201,13 +192,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(&raw_full[i], 1);
             mbar_init(&raw_empty[i], 8);   // epilogue warps
         }
-        for (int i = 0; i < BSr; ++i) {
-            mbar_init(&b_full[i], 1);
-            mbar_init(&b_empty[i], 1);     // MMA commit
-        }
-        for (int i = 0; i < C::AS; ++i) {
-            mbar_init(&a_full[i], 4);      // expand warps
-            mbar_init(&a_empty[i], 1);     // MMA commit
+        for (int i = 0; i < KSr; ++i) {
+            mbar_init(&k_full[i], 5);      // 4 expand warps + the activation producer (with its bytes)
+            mbar_init(&k_empty[i], 1);     // MMA commit
         }
         for (int i = 0; i < C::DS; ++i) {
             mbar_init(&d_full[i], 1);      // MMA commit
@@ -263,24 +250,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int tile = blockIdx.x; ok && tile < sh.num_tiles; tile += gridDim.x) {
                 const int mt = tile % sh.mt_count;
                 for (int kstep = 0; kstep < G * C::KSG; ++kstep) {
-                    const int bs = bc % BSr;
-                    if (!mbar_wait(&b_empty[bs], ((bc / BSr) & 1) ^ 1, status, abort)) {
+                    const int bs = bc % KSr;
+                    if (!mbar_wait(&k_empty[bs], ((bc / KSr) & 1) ^ 1, status, abort)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&b_full[bs], (uint32_t)b_bytes);
-                    tma_load_2d(bst + (size_t)bs * b_bytes, &act_map, kstep * 64, mt * m_tile, &b_full[bs]);
+                    mbar_arrive_expect_tx(&k_full[bs], (uint32_t)b_bytes);
+                    tma_load_2d(bst + (size_t)bs * b_bytes, &act_map, kstep * 64, mt * m_tile, &k_full[bs]);
                     ++bc;
                 }
             }
-            for (int i = bc - BSr > 0 ? bc - BSr : 0; i < bc; ++i)
-                mbar_wait(&b_full[i % BSr], (i / BSr) & 1, status, nullptr);
+            for (int i = bc - KSr > 0 ? bc - KSr : 0; i < bc; ++i)
+                mbar_wait(&k_full[i % KSr], (i / KSr) & 1, status, nullptr);
         }
     } else if (warp == 13) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
             const uint32_t idesc = idesc_f16_f32(128, m_tile);
-            int ac = 0, bc = 0, dc = 0;
+            int kc = 0, dc = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < sh.num_tiles; tile += gridDim.x) {
                 for (int g = 0; ok && g < G; ++g) {
@@ -292,29 +279,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tc_fence_after();
                     const uint32_t d_tmem = tmem + (uint32_t)(db * sh.d_stride);
                     for (int j = 0; j < C::KSG; ++j) {
-                        const int as = ac % C::AS, bs = bc % BSr;
-                        if (!mbar_wait(&a_full[as], (ac / C::AS) & 1, status, abort) ||
-                            !mbar_wait(&b_full[bs], (bc / BSr) & 1, status, abort)) {
+                        const int ks = kc % KSr;
+                        if (!mbar_wait(&k_full[ks], (kc / KSr) & 1, status, abort)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint64_t bdesc = sdesc_sw128(smem_u32(bst + (size_t)bs * b_bytes));
+                        const uint64_t bdesc = sdesc_sw128(smem_u32(bst + (size_t)ks * b_bytes));
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
                             const uint32_t accum = (j > 0 || kk > 0) ? 1u : 0u;
                             if (A_TMEM) {
-                                const uint32_t a_tmem = tmem + (uint32_t)(C::DS * sh.d_stride + 32 * as + 8 * kk);
+                                const uint32_t a_tmem = tmem + (uint32_t)(C::DS * sh.d_stride + 32 * ks + 8 * kk);
                                 mma_f16_ts(d_tmem, a_tmem, bdesc + 2 * kk, idesc, accum);
                             } else {
-                                const uint64_t adesc = sdesc_sw128(smem_u32(ast + (size_t)as * 16384));
+                                const uint64_t adesc = sdesc_sw128(smem_u32(ast + (size_t)ks * 16384));
                                 mma_f16_ss(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, accum);
                             }
                         }
-                        tc_commit(&a_empty[as]);
-                        tc_commit(&b_empty[bs]);
-                        ++ac;
-                        ++bc;
+                        tc_commit(&k_empty[ks]);
+                        ++kc;
                     }
                     if (!ok) break;
                     tc_commit(&d_full[db]);
@@ -359,7 +343,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else if (warp < 4) {
         // ---------------------------------------------------------- expand
         const int r = threadIdx.x;   // weight row within the tile == tensor-memory lane
-        int ac = 0, rc = 0;
+        int kc = 0, rc = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < sh.num_tiles; tile += gridDim.x) {
             for (int g = 0; ok && g < G; ++g) {
@@ -370,8 +354,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 const uint8_t* ch = raw + (size_t)rs * C::CB;
                 for (int j = 0; j < C::KSG; ++j) {
-                    const int as = ac % C::AS;
-                    if (!mbar_wait(&a_empty[as], ((ac / C::AS) & 1) ^ 1, status, abort)) {
+                    const int as = kc % KSr;
+                    if (!mbar_wait(&k_empty[as], ((kc / KSr) & 1) ^ 1, status, abort)) {
                         ok = false;
                         break;
                     }
@@ -389,7 +373,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     expand_word<OFF>(p1.w, hv + 28);
                     if (A_TMEM) {
                         const uint32_t taddr =
-                            tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(C::DS * sh.d_stride + 32 * as);
+                            tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(C::DS * sh.d_stride + 32 * as);   // as < KS
                         tmem_st32(taddr, hv);
                         tmem_st_wait();
                         tc_fence_before();
@@ -402,8 +386,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         fence_proxy_async_smem();
                     }
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&a_full[as]);
-                    ++ac;
+                    if (lane == 0) mbar_arrive(&k_full[as]);
+                    ++kc;
                 }
                 ++rc;
             }
@@ -516,7 +500,7 @@ cudaError_t run_gemm(const LaunchCtx& c, const CUtensorMap& map, const GemmShape
     auto kern = gemm_kernel<VARIANT, GROUP, A_TMEM, DEBUG, MAXC>;
     GemmShape sh = sh_in;
     sh.tmem_cols = gemm_tmem_cols<VARIANT, GROUP, MAXC>(sh.d_stride, !A_TMEM);
-    sh.bs = gemm_stages_b<VARIANT, GROUP, MAXC>(sh.m_tile, !A_TMEM);
+    sh.bs = gemm_kstages<VARIANT, GROUP, MAXC>(!A_TMEM);
     const size_t smem = gemm_smem_bytes<VARIANT, GROUP, MAXC>(sh.m_tile, !A_TMEM);
     static size_t configured = 0;
     cudaError_t e;

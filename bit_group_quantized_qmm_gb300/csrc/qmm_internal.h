@@ -67,7 +67,7 @@ struct GemmShape {
     int num_tiles;   // row tiles x mt_count
     int d_stride;    // tensor-memory columns per accumulator buffer
     int tmem_cols;   // allocated tensor-memory columns (power of two)
-    int bs;          // activation-tile stages in use (<= the instance's maximum)
+    int bs;          // k-step stages in use (<= the instance's maximum)
 };
 
 cudaError_t launch_gemm_w4a8(const LaunchCtx& c, int group, const CUtensorMap& map, const GemmShape& sh,
