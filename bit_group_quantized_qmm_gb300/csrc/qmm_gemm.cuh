@@ -19,7 +19,10 @@
 // Warp roles (512 threads, one CTA per SM, persistent over tiles):
 //   warps 0-3   expand: packed nibbles (smem) -> fp16 weight operand, written
 //               to tensor memory with tcgen05.st (or to 128-byte-swizzled
-//               shared memory); one tensor-memory lane quadrant per warp
+//               shared memory); one tensor-memory lane quadrant per warp.
+//               They copy each group's scales to a small ring of their own
+//               and release the packed chunk at once, so the chunk ring is
+//               not held for the length of the MMA and epilogue pipeline.
 //   warps 4-11  epilogue: read each group's partials from tensor memory,
 //               rescale in fp32 into register accumulators (at most 64 per
 //               thread: m_tile <= 128, two warpgroups), store Y
@@ -50,10 +53,12 @@ struct GemmCfg {
     static constexpr bool NARROW = MAXC <= 32;
     static constexpr int CB = 64 * GROUP + 256 + (VARIANT == 1 ? 256 : 0);
     static constexpr int KSG = GROUP / 64;                                   // 64-wide k-steps per group
-    static constexpr int RS = NARROW ? (GROUP == 128 ? 10 : 16) : (GROUP == 128 ? 6 : 8);   // packed chunks
+    static constexpr int RS = NARROW ? (GROUP == 128 ? 10 : 16) : (GROUP == 128 ? 8 : 12);  // packed chunks
     static constexpr int KS = NARROW ? 8 : 4;   // k-step stages: weight operand + activation tile together
     static constexpr int DS = NARROW ? 4 : 3;                                // accumulator buffers
-    static constexpr int XS = NARROW ? 8 : 4;                                // activation-scale stages
+    static constexpr int XS = 16;                                            // activation-scale stages
+    static constexpr int SR = 8;                                             // weight-scale copies
+    static constexpr int SCB = VARIANT == 1 ? 512 : 256;                     // bytes per copy
 };
 
 // k-step stages in use: the weight operand in shared memory takes 16 KB per
@@ -75,7 +80,8 @@ inline size_t gemm_smem_bytes(int m_tile, bool a_in_smem)
     if (a_in_smem) b += (size_t)ks * 16384;
     b += (size_t)C::RS * C::CB;
     b += (size_t)C::XS * m_tile * 4;
-    b += 8 * (2 * C::RS + 2 * C::KS + 2 * C::DS + 2 * C::XS + 1) + 64;
+    b += (size_t)C::SR * C::SCB;
+    b += 8 * (2 * C::RS + 2 * C::KS + 2 * C::DS + 2 * C::XS + 2 * C::SR + 1) + 64;
     return b;
 }
 
@@ -170,8 +176,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint8_t* ast = bst + (size_t)KSr * b_bytes;
     uint8_t* raw = ast + (A_TMEM ? 0 : (size_t)KSr * 16384);
     float* xs = reinterpret_cast<float*>(raw + (size_t)C::RS * C::CB);
+    uint8_t* scr = reinterpret_cast<uint8_t*>(xs + C::XS * m_tile);   // per-group weight scales (+ biases)
     uint64_t* bars =
-        reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(xs + C::XS * m_tile) + 7) & ~uintptr_t(7));
+        reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(scr + C::SR * C::SCB) + 7) & ~uintptr_t(7));
     uint64_t* raw_full = bars;
     uint64_t* raw_empty = raw_full + C::RS;
     uint64_t* k_full = raw_empty + C::RS;    // weight operand expanded + activation tile landed
@@ -180,7 +187,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t* d_empty = d_full + C::DS;
     uint64_t* x_full = d_empty + C::DS;
     uint64_t* x_empty = x_full + C::XS;
-    uint64_t* done = x_empty + C::XS;
+    uint64_t* s_full = x_empty + C::XS;      // weight scales of a group copied
+    uint64_t* s_empty = s_full + C::SR;
+    uint64_t* done = s_empty + C::SR;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -190,7 +199,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::RS; ++i) {
             mbar_init(&raw_full[i], 1);
-            mbar_init(&raw_empty[i], 8);   // epilogue warps
+            mbar_init(&raw_empty[i], 4);   // expand warps, once they have read the chunk
+        }
+        for (int i = 0; i < C::SR; ++i) {
+            mbar_init(&s_full[i], 4);      // expand warps
+            mbar_init(&s_empty[i], 8);     // epilogue warps
         }
         for (int i = 0; i < KSr; ++i) {
             mbar_init(&k_full[i], 5);      // 4 expand warps + the activation producer (with its bytes)
@@ -353,6 +366,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     break;
                 }
                 const uint8_t* ch = raw + (size_t)rs * C::CB;
+                {
+                    // the epilogue gets this group's scales (and biases) in a ring of
+                    // its own, so the chunk can be released as soon as it has been read
+                    const int ss = rc % C::SR;
+                    if (!mbar_wait(&s_empty[ss], ((rc / C::SR) & 1) ^ 1, status, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    uint16_t* dst = reinterpret_cast<uint16_t*>(scr + (size_t)ss * C::SCB);
+                    const uint16_t* src = reinterpret_cast<const uint16_t*>(ch + 64 * GROUP);
+                    dst[r] = src[r];
+                    if (VARIANT == 1) dst[128 + r] = src[128 + r];
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&s_full[ss]);
+                }
                 for (int j = 0; j < C::KSG; ++j) {
                     const int as = kc % KSr;
                     if (!mbar_wait(&k_empty[as], ((kc / KSr) & 1) ^ 1, status, abort)) {
@@ -389,6 +417,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     if (lane == 0) mbar_arrive(&k_full[as]);
                     ++kc;
                 }
+                if (!ok) break;
+                if (lane == 0) mbar_arrive(&raw_empty[rs]);   // the warp's reads of the chunk are done
                 ++rc;
             }
         }
@@ -411,18 +441,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
             for (int c = 0; c < MAXC; ++c) acc[c] = 0.f;
             for (int g = 0; g < G; ++g) {
-                const int db = dc % C::DS, rs = rc % C::RS, xsi = xc % C::XS;
+                const int db = dc % C::DS, ss = rc % C::SR, xsi = xc % C::XS;
                 if (!mbar_wait(&d_full[db], (dc / C::DS) & 1, status, abort) ||
-                    !mbar_wait(&raw_full[rs], (rc / C::RS) & 1, status, abort) ||
+                    !mbar_wait(&s_full[ss], (rc / C::SR) & 1, status, abort) ||
                     !mbar_wait(&x_full[xsi], (xc / C::XS) & 1, status, abort)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint8_t* ch = raw + (size_t)rs * C::CB;
-                const float sw = __half2float(reinterpret_cast<const __half*>(ch + 64 * GROUP)[r]);
-                const float bw =
-                    VARIANT == 1 ? __half2float(reinterpret_cast<const __half*>(ch + 64 * GROUP + 256)[r]) : 0.f;
+                const __half* sc = reinterpret_cast<const __half*>(scr + (size_t)ss * C::SCB);
+                const float sw = __half2float(sc[r]);
+                const float bw = VARIANT == 1 ? __half2float(sc[128 + r]) : 0.f;
                 const float* sxv = xs + (size_t)xsi * m_tile + c0;
                 const uint32_t dcol = lane_base + (uint32_t)(db * sh.d_stride + c0);
                 // BATCH columns at a time: up to BATCH/8 loads of 8 columns, one wait
@@ -466,7 +495,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&d_empty[db]);
-                    mbar_arrive(&raw_empty[rs]);
+                    mbar_arrive(&s_empty[ss]);
                     mbar_arrive(&x_empty[xsi]);
                 }
                 ++dc;
