@@ -142,8 +142,8 @@ GemmShape gemm_shape(int M, int N, int K, bool a_in_smem)
     sh.K = K;
     const int tiles_m = (M + kMaxMTile - 1) / kMaxMTile;
     int mt = (M + tiles_m - 1) / tiles_m;
-    mt = (mt + 31) / 32 * 32;   // four epilogue column quarters of a multiple of 8 columns
-    if (mt < 32) mt = 32;
+    mt = (mt + 15) / 16 * 16;
+    if (mt < 16) mt = 16;
     sh.m_tile = mt;
     sh.mt_count = (M + mt - 1) / mt;
     sh.num_tiles = ((N + 127) / 128) * sh.mt_count;

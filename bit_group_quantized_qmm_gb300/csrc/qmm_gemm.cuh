@@ -14,23 +14,22 @@
 // are exact, and a 64- or 128-wide group sum stays below 2^24, so the fp32
 // accumulator holds the exact int32 group partial. Weights sit in the MMA's M
 // slot (128 rows of the packed tile), activations in its N slot (m_tile rows,
-// 32..128), so one kernel serves decode-sized and prefill-sized M.
+// 16..128), so one kernel serves decode-sized and prefill-sized M.
 //
-// Warp roles (768 threads, one CTA per SM, persistent over tiles):
+// Warp roles (512 threads, one CTA per SM, persistent over tiles):
 //   warps 0-3   expand: packed nibbles (smem) -> fp16 weight operand, written
 //               to tensor memory with tcgen05.st (or to 128-byte-swizzled
 //               shared memory); one tensor-memory lane quadrant per warp.
 //               They copy each group's scales to a small ring of their own
 //               and release the packed chunk at once, so the chunk ring is
 //               not held for the length of the MMA and epilogue pipeline.
-//   warps 4-19  epilogue: read each group's partials from tensor memory,
-//               rescale in fp32 into register accumulators, store Y; four
-//               warps per tensor-memory lane quadrant, one column quarter
-//               each (at most 32 columns: one load and one wait per group)
-//   warp 20     weight producer: 1-D bulk copies of packed chunks
-//   warp 21     MMA issuer; owns the tensor-memory allocation
-//   warp 22     activation-scale loader (sx or S per group, cp.async)
-//   warp 23     activation producer: TMA tiles of the fp16 activations
+//   warps 4-11  epilogue: read each group's partials from tensor memory,
+//               rescale in fp32 into register accumulators (at most 64 per
+//               thread: m_tile <= 128, two warpgroups), store Y
+//   warp 12     weight producer: 1-D bulk copies of packed chunks
+//   warp 13     MMA issuer; owns the tensor-memory allocation
+//   warp 14     activation-scale loader (sx or S per group, cp.async)
+//   warp 15     activation producer: TMA tiles of the fp16 activations
 //               (128-byte swizzle), in a ring deep enough that these small
 //               loads never wait behind the weight chunks
 // Accumulators are double-buffered per group in tensor memory so the MMAs of
@@ -44,15 +43,14 @@
 
 namespace qmm {
 
-constexpr int kGemmThreads = 768;   // 24 warps
-constexpr int kEpiWarps = 16;
+constexpr int kGemmThreads = 512;
 
 // Pipeline depths. Narrow tiles (m_tile <= 64: decode-sized M) are bound by
 // the latency of the expand -> MMA -> epilogue hand-offs, so they keep more
 // k-steps and groups in flight; wide tiles are bound by tensor-memory space.
 template <int VARIANT, int GROUP, int MAXC>
 struct GemmCfg {
-    static constexpr bool NARROW = MAXC <= 16;
+    static constexpr bool NARROW = MAXC <= 32;
     static constexpr int CB = 64 * GROUP + 256 + (VARIANT == 1 ? 256 : 0);
     static constexpr int KSG = GROUP / 64;                                   // 64-wide k-steps per group
     static constexpr int RS = NARROW ? (GROUP == 128 ? 10 : 16) : (GROUP == 128 ? 8 : 12);  // packed chunks
@@ -205,7 +203,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         for (int i = 0; i < C::SR; ++i) {
             mbar_init(&s_full[i], 4);      // expand warps
-            mbar_init(&s_empty[i], kEpiWarps);
+            mbar_init(&s_empty[i], 8);     // epilogue warps
         }
         for (int i = 0; i < KSr; ++i) {
             mbar_init(&k_full[i], 5);      // 4 expand warps + the activation producer (with its bytes)
@@ -213,18 +211,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         for (int i = 0; i < C::DS; ++i) {
             mbar_init(&d_full[i], 1);      // MMA commit
-            mbar_init(&d_empty[i], kEpiWarps);
+            mbar_init(&d_empty[i], 8);     // epilogue warps
         }
         for (int i = 0; i < C::XS; ++i) {
             mbar_init(&x_full[i], 32);     // loader lanes
-            mbar_init(&x_empty[i], kEpiWarps);
+            mbar_init(&x_empty[i], 8);     // epilogue warps
         }
         mbar_init(done, 1);
         *abort = 0;
         fence_barrier_init();
     }
-    if (warp == 23 && lane == 0) prefetch_tensormap(&act_map);
-    if (warp == 21) {
+    if (warp == 15 && lane == 0) prefetch_tensormap(&act_map);
+    if (warp == 13) {
         tmem_alloc(tmem_slot, (uint32_t)sh.tmem_cols);
         tmem_relinquish();
     }
@@ -234,7 +232,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t tmem = *tmem_slot;
     pdl_trigger();
 
-    if (warp == 20) {
+    if (warp == 12) {
         // ---------------------------------------------------------- weight producer
         if (lane == 0) {
             int rc = 0;
@@ -256,7 +254,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int i = rc - C::RS > 0 ? rc - C::RS : 0; i < rc; ++i)
                 mbar_wait(&raw_full[i % C::RS], (i / C::RS) & 1, status, nullptr);
         }
-    } else if (warp == 23) {
+    } else if (warp == 15) {
         // ---------------------------------------------------------- activation producer
         if (lane == 0) {
             pdl_wait();   // activations come from the previous kernel
@@ -278,7 +276,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int i = bc - KSr > 0 ? bc - KSr : 0; i < bc; ++i)
                 mbar_wait(&k_full[i % KSr], (i / KSr) & 1, status, nullptr);
         }
-    } else if (warp == 21) {
+    } else if (warp == 13) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
             const uint32_t idesc = idesc_f16_f32(128, m_tile);
@@ -324,7 +322,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             tc_commit(done);
             mbar_wait(done, 0, status, nullptr);
         }
-    } else if (warp == 22) {
+    } else if (warp == 14) {
         // ---------------------------------------------------------- scale loader
         pdl_wait();
         // no copy may still be landing when the CTA exits (checked below)
@@ -424,13 +422,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 ++rc;
             }
         }
-    } else if (warp < 4 + kEpiWarps) {
+    } else if (warp < 12) {
         // ---------------------------------------------------------- epilogue
-        const int q = warp & 3;                 // tensor-memory lane quadrant
-        const int quarter = (warp - 4) >> 2;    // column quarter
+        const int q = warp & 3;             // tensor-memory lane quadrant
+        const int half = (warp - 4) >> 2;   // column half
         const int r = 32 * q + lane;
-        const int ncol = m_tile >> 2;
-        const int c0 = quarter * ncol;
+        const int ncol = m_tile >> 1;
+        const int c0 = half * ncol;
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
         int dc = 0, rc = 0, xc = 0;
         bool ok = true;
@@ -517,7 +515,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ------------------------------------------------------------------ teardown
     tc_fence_before();
     __syncthreads();
-    if (warp == 21) {
+    if (warp == 13) {
         tc_fence_after();
         tmem_dealloc(tmem, (uint32_t)sh.tmem_cols);
     }

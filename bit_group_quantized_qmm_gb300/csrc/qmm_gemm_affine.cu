@@ -7,13 +7,13 @@ namespace qmm {
 cudaError_t launch_gemm_affine(const LaunchCtx& c, const CUtensorMap& map, const GemmShape& sh,
                                const uint8_t* blob, const float* gsum, float* Y, bool a_in_smem)
 {
-    const int quarter = sh.m_tile / 4;   // columns per epilogue thread
+    const int half = sh.m_tile / 2;
     if (a_in_smem) {
-        if (quarter <= 16) return run_gemm<1, 64, false, false, 16>(c, map, sh, blob, gsum, Y, nullptr);
-        return run_gemm<1, 64, false, false, 32>(c, map, sh, blob, gsum, Y, nullptr);
+        if (half <= 32) return run_gemm<1, 64, false, false, 32>(c, map, sh, blob, gsum, Y, nullptr);
+        return run_gemm<1, 64, false, false, 64>(c, map, sh, blob, gsum, Y, nullptr);
     }
-    if (quarter <= 16) return run_gemm<1, 64, true, false, 16>(c, map, sh, blob, gsum, Y, nullptr);
-    return run_gemm<1, 64, true, false, 32>(c, map, sh, blob, gsum, Y, nullptr);
+    if (half <= 32) return run_gemm<1, 64, true, false, 32>(c, map, sh, blob, gsum, Y, nullptr);
+    return run_gemm<1, 64, true, false, 64>(c, map, sh, blob, gsum, Y, nullptr);
 }
 
 }  // namespace qmm

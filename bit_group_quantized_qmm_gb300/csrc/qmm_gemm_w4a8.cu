@@ -9,17 +9,17 @@ template <int GROUP>
 static cudaError_t dispatch(const LaunchCtx& c, const CUtensorMap& map, const GemmShape& sh, const uint8_t* blob,
                             const float* sx, float* Y, int32_t* P, bool a_in_smem)
 {
-    const int quarter = sh.m_tile / 4;   // columns per epilogue thread
+    const int half = sh.m_tile / 2;
     if (P) {
-        if (a_in_smem) return run_gemm<0, GROUP, false, true, 32>(c, map, sh, blob, sx, Y, P);
-        return run_gemm<0, GROUP, true, true, 32>(c, map, sh, blob, sx, Y, P);
+        if (a_in_smem) return run_gemm<0, GROUP, false, true, 64>(c, map, sh, blob, sx, Y, P);
+        return run_gemm<0, GROUP, true, true, 64>(c, map, sh, blob, sx, Y, P);
     }
     if (a_in_smem) {
-        if (quarter <= 16) return run_gemm<0, GROUP, false, false, 16>(c, map, sh, blob, sx, Y, P);
-        return run_gemm<0, GROUP, false, false, 32>(c, map, sh, blob, sx, Y, P);
+        if (half <= 32) return run_gemm<0, GROUP, false, false, 32>(c, map, sh, blob, sx, Y, P);
+        return run_gemm<0, GROUP, false, false, 64>(c, map, sh, blob, sx, Y, P);
     }
-    if (quarter <= 16) return run_gemm<0, GROUP, true, false, 16>(c, map, sh, blob, sx, Y, P);
-    return run_gemm<0, GROUP, true, false, 32>(c, map, sh, blob, sx, Y, P);
+    if (half <= 32) return run_gemm<0, GROUP, true, false, 32>(c, map, sh, blob, sx, Y, P);
+    return run_gemm<0, GROUP, true, false, 64>(c, map, sh, blob, sx, Y, P);
 }
 
 cudaError_t launch_gemm_w4a8(const LaunchCtx& c, int group, const CUtensorMap& map, const GemmShape& sh,

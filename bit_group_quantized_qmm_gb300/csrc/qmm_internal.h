@@ -62,7 +62,7 @@ cudaError_t launch_gemv_fused(const LaunchCtx& c, int N, int K, int group, int h
 
 struct GemmShape {
     int M, N, K;
-    int m_tile;      // activation rows per tile (MMA N), multiple of 32, <= kMaxMTile
+    int m_tile;      // activation rows per tile (MMA N), multiple of 16, <= kMaxMTile
     int mt_count;    // ceil(M / m_tile)
     int num_tiles;   // row tiles x mt_count
     int d_stride;    // tensor-memory columns per accumulator buffer
