@@ -16,24 +16,34 @@
 // slot (128 rows of the packed tile), activations in its N slot (m_tile rows,
 // 16..128), so one kernel serves decode-sized and prefill-sized M.
 //
+// Every group's partials must be rescaled on their own (sw differs per row and
+// group, sx per activation row and group), so the epilogue reads the whole
+// accumulator from tensor memory once per group: 2 fp32 operations per
+// partial against 64 (g64) tensor-core MACs. That rescale, not the MMA, sets
+// the pace on wide tiles, so it gets the fewest instructions:
+//   - a thread keeps its running sums (up to 64 columns) as packed fp32 pairs
+//     (fma.rn.f32x2 / mul.rn.f32x2: two columns per instruction, each rounded
+//     as the scalar operation) and reads a group's columns with one
+//     tensor-memory round trip up to 48 columns (m_tile <= 96), two batches of
+//     32 at 64;
+//   - one scale stage per group carries the weight scales (+ biases) and the
+//     activation scales, filled by one loader warp with asynchronous copies:
+//     the epilogue waits on two barriers per group (partials, scales), and
+//     the expand warps only expand.
+// (Raising the epilogue's register budget with setmaxnreg, to hold a whole
+// group's columns and overlap the two batches, measured slower on GB300.)
 // Warp roles (512 threads, one CTA per SM, persistent over tiles):
 //   warps 0-3   expand: packed nibbles (smem) -> fp16 weight operand, written
 //               to tensor memory with tcgen05.st (or to 128-byte-swizzled
-//               shared memory); one tensor-memory lane quadrant per warp.
-//               They copy each group's scales to a small ring of their own
-//               and release the packed chunk at once, so the chunk ring is
-//               not held for the length of the MMA and epilogue pipeline.
-//   warps 4-11  epilogue: read each group's partials from tensor memory,
-//               rescale in fp32 into register accumulators (at most 64 per
-//               thread: m_tile <= 128, two warpgroups), store Y
+//               shared memory); one tensor-memory lane quadrant per warp
+//   warps 4-11  epilogue: rescale each group's partials into register sums
+//               (two warpgroups = two column halves), store Y per tile
 //   warp 12     weight producer: 1-D bulk copies of packed chunks
 //   warp 13     MMA issuer; owns the tensor-memory allocation
-//   warp 14     activation-scale loader (sx or S per group, cp.async)
+//   warp 14     scale loader (weight scales from the blob, sx or S per group)
 //   warp 15     activation producer: TMA tiles of the fp16 activations
-//               (128-byte swizzle), in a ring deep enough that these small
-//               loads never wait behind the weight chunks
-// Accumulators are double-buffered per group in tensor memory so the MMAs of
-// group g+1 run while the epilogue rescales group g. Every wait is bounded.
+// Ring positions advance incrementally (no division on the issue paths).
+// Every wait is bounded.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -45,8 +55,7 @@ namespace qmm {
 
 constexpr int kGemmThreads = 512;
 
-// Pipeline depths. Narrow tiles (m_tile <= 64: decode-sized M) are bound by
-// the latency of the expand -> MMA -> epilogue hand-offs, so they keep more
+// Pipeline depths. Narrow tiles (m_tile <= 64: decode-sized M) keep more
 // k-steps and groups in flight; wide tiles are bound by tensor-memory space.
 template <int VARIANT, int GROUP, int MAXC>
 struct GemmCfg {
@@ -54,20 +63,20 @@ struct GemmCfg {
     static constexpr int CB = 64 * GROUP + 256 + (VARIANT == 1 ? 256 : 0);
     static constexpr int KSG = GROUP / 64;                                   // 64-wide k-steps per group
     static constexpr int RS = NARROW ? (GROUP == 128 ? 10 : 16) : (GROUP == 128 ? 8 : 12);  // packed chunks
-    static constexpr int KS = NARROW ? 8 : 4;   // k-step stages: weight operand + activation tile together
-    static constexpr int DS = NARROW ? 4 : 3;                                // accumulator buffers
-    static constexpr int XS = 16;                                            // activation-scale stages
-    static constexpr int SR = 8;                                             // weight-scale copies
-    static constexpr int SCB = VARIANT == 1 ? 512 : 256;                     // bytes per copy
+    static constexpr int KS_TMEM = NARROW ? 8 : 4;   // k-step stages, weight operand in tensor memory
+    static constexpr int KS_SMEM = 4;                // k-step stages, weight operand in shared memory
+    static constexpr int DS = MAXC <= 48 ? 4 : 3;    // accumulator buffers
+    // epilogue columns per tensor-memory round trip (one wait): a whole
+    // group up to 48 columns, two batches of 32 for 64
+    static constexpr int EB = MAXC <= 48 ? MAXC : 32;
+    static constexpr int XS = 16;                    // scale stages
+    static constexpr int SWB = VARIANT == 1 ? 512 : 256;   // weight scales (+ biases) bytes per stage
 };
 
-// k-step stages in use: the weight operand in shared memory takes 16 KB per
-// stage, so that variant keeps fewer.
 template <int VARIANT, int GROUP, int MAXC>
-inline int gemm_kstages(bool a_in_smem)
+constexpr int gemm_kstages(bool a_in_smem)
 {
-    using C = GemmCfg<VARIANT, GROUP, MAXC>;
-    return a_in_smem && C::KS > 4 ? 4 : C::KS;
+    return a_in_smem ? GemmCfg<VARIANT, GROUP, MAXC>::KS_SMEM : GemmCfg<VARIANT, GROUP, MAXC>::KS_TMEM;
 }
 
 template <int VARIANT, int GROUP, int MAXC>
@@ -79,18 +88,17 @@ inline size_t gemm_smem_bytes(int m_tile, bool a_in_smem)
     b += (size_t)ks * m_tile * 128;
     if (a_in_smem) b += (size_t)ks * 16384;
     b += (size_t)C::RS * C::CB;
-    b += (size_t)C::XS * m_tile * 4;
-    b += (size_t)C::SR * C::SCB;
-    b += 8 * (2 * C::RS + 2 * C::KS + 2 * C::DS + 2 * C::XS + 2 * C::SR + 1) + 64;
+    b += (size_t)C::XS * (C::SWB + 4 * m_tile);
+    b += 8 * (2 * C::RS + 2 * ks + 2 * C::DS + 2 * C::XS + 1) + 64;
     return b;
 }
 
-// Tensor-memory columns: DS accumulators (+ AS weight-operand stages).
+// Tensor-memory columns: DS accumulators (+ the weight-operand stages).
 template <int VARIANT, int GROUP, int MAXC>
 inline int gemm_tmem_cols(int d_stride, bool a_in_smem)
 {
     using C = GemmCfg<VARIANT, GROUP, MAXC>;
-    const int cols = C::DS * d_stride + (a_in_smem ? 0 : 32 * C::KS);
+    const int cols = C::DS * d_stride + (a_in_smem ? 0 : 32 * C::KS_TMEM);
     int alloc = 32;
     while (alloc < cols) alloc <<= 1;
     return alloc;
@@ -124,41 +132,47 @@ __device__ __forceinline__ void expand_word(uint32_t w, uint32_t* out)
     out[3] = *reinterpret_cast<uint32_t*>(&r3);
 }
 
-// Packed fp32 pairs (fma.rn.f32x2 / mul.rn.f32x2: two lanes of fp32 per
-// instruction; each element rounds exactly as the scalar operation).
-__device__ __forceinline__ unsigned long long pack2(float a, float b)
-{
-    return (unsigned long long)__float_as_uint(a) | ((unsigned long long)__float_as_uint(b) << 32);
-}
-
-// (p0 * s0, p1 * s1) for raw fp32 bit patterns p0, p1
-__device__ __forceinline__ unsigned long long mul_pair(uint32_t p0, uint32_t p1, float s0, float s1)
+// Running sums of two columns as one packed fp32 pair.
+__device__ __forceinline__ unsigned long long splat2(float w)
 {
     unsigned long long d;
-    const unsigned long long a = (unsigned long long)p0 | ((unsigned long long)p1 << 32);
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(pack2(s0, s1)));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(d) : "f"(w));
     return d;
 }
 
-// (acc0, acc1) += t * (w, w)
-__device__ __forceinline__ void fma_pair(float& acc0, float& acc1, unsigned long long t, float w)
+// W4A8: acc += ((p0, p1) * (s0, s1)) * (w, w), p the raw fp32 partials.
+__device__ __forceinline__ void acc_w4a8(unsigned long long& acc, uint32_t p0, uint32_t p1, float s0, float s1,
+                                         unsigned long long w2)
 {
-    unsigned long long c = pack2(acc0, acc1), d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(t), "l"(pack2(w, w)), "l"(c));
-    acc0 = __uint_as_float((uint32_t)d);
-    acc1 = __uint_as_float((uint32_t)(d >> 32));
+    asm("{\n\t.reg .b64 t, s;\n\t"
+        "mov.b64 t, {%1, %2};\n\t"
+        "mov.b64 s, {%3, %4};\n\t"
+        "mul.rn.f32x2 t, t, s;\n\t"
+        "fma.rn.f32x2 %0, t, %5, %0;\n\t}"
+        : "+l"(acc)
+        : "r"(p0), "r"(p1), "f"(s0), "f"(s1), "l"(w2));
 }
 
-// (acc0, acc1) += (v0, v1) * (w, w)
-__device__ __forceinline__ void fma_pair_v(float& acc0, float& acc1, float v0, float v1, float w)
+// Affine: acc += (S0, S1) * (b, b), then acc += (p0, p1) * (s, s).
+__device__ __forceinline__ void acc_affine(unsigned long long& acc, uint32_t p0, uint32_t p1, float S0, float S1,
+                                           unsigned long long b2, unsigned long long s2)
 {
-    fma_pair(acc0, acc1, pack2(v0, v1), w);
+    asm("{\n\t.reg .b64 t, u;\n\t"
+        "mov.b64 u, {%3, %4};\n\t"
+        "fma.rn.f32x2 %0, u, %5, %0;\n\t"
+        "mov.b64 t, {%1, %2};\n\t"
+        "fma.rn.f32x2 %0, t, %6, %0;\n\t}"
+        : "+l"(acc)
+        : "r"(p0), "r"(p1), "f"(S0), "f"(S1), "l"(b2), "l"(s2));
 }
 
-// (acc0, acc1) += (p0, p1) * (w, w) for raw fp32 bit patterns
-__device__ __forceinline__ void fma_pair_u(float& acc0, float& acc1, uint32_t p0, uint32_t p1, float w)
+template <int S>
+__device__ __forceinline__ void ring_next(int& i, uint32_t& ph)
 {
-    fma_pair(acc0, acc1, (unsigned long long)p0 | ((unsigned long long)p1 << 32), w);
+    if (++i == S) {
+        i = 0;
+        ph ^= 1u;
+    }
 }
 
 template <int VARIANT, int GROUP, bool A_TMEM, bool DEBUG, int MAXC>
@@ -167,29 +181,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const float* __restrict__ act_scale, float* __restrict__ Y, int32_t* __restrict__ P, int* status)
 {
     using C = GemmCfg<VARIANT, GROUP, MAXC>;
+    constexpr int KS = A_TMEM ? C::KS_TMEM : C::KS_SMEM;
+    constexpr int RS = C::RS, DS = C::DS, XS = C::XS, KSG = C::KSG;
+    constexpr int EB = C::EB;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int m_tile = sh.m_tile;
     const int b_bytes = m_tile * 128;
+    const int ssb = C::SWB + 4 * m_tile;   // bytes per scale stage
     uint8_t* bst = base;
-    const int KSr = sh.bs;   // k-step stages in use
-    uint8_t* ast = bst + (size_t)KSr * b_bytes;
-    uint8_t* raw = ast + (A_TMEM ? 0 : (size_t)KSr * 16384);
-    float* xs = reinterpret_cast<float*>(raw + (size_t)C::RS * C::CB);
-    uint8_t* scr = reinterpret_cast<uint8_t*>(xs + C::XS * m_tile);   // per-group weight scales (+ biases)
+    uint8_t* ast = bst + (size_t)KS * b_bytes;
+    uint8_t* raw = ast + (A_TMEM ? 0 : (size_t)KS * 16384);
+    uint8_t* scs = raw + (size_t)RS * C::CB;
     uint64_t* bars =
-        reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(scr + C::SR * C::SCB) + 7) & ~uintptr_t(7));
+        reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(scs + (size_t)XS * ssb) + 7) & ~uintptr_t(7));
     uint64_t* raw_full = bars;
-    uint64_t* raw_empty = raw_full + C::RS;
-    uint64_t* k_full = raw_empty + C::RS;    // weight operand expanded + activation tile landed
-    uint64_t* k_empty = k_full + C::KS;      // the k-step's MMAs retired
-    uint64_t* d_full = k_empty + C::KS;
-    uint64_t* d_empty = d_full + C::DS;
-    uint64_t* x_full = d_empty + C::DS;
-    uint64_t* x_empty = x_full + C::XS;
-    uint64_t* s_full = x_empty + C::XS;      // weight scales of a group copied
-    uint64_t* s_empty = s_full + C::SR;
-    uint64_t* done = s_empty + C::SR;
+    uint64_t* raw_empty = raw_full + RS;
+    uint64_t* k_full = raw_empty + RS;    // weight operand expanded + activation tile landed
+    uint64_t* k_empty = k_full + KS;      // the k-step's MMAs retired
+    uint64_t* d_full = k_empty + KS;      // a group's partials complete
+    uint64_t* d_empty = d_full + DS;      // the epilogue's loads of them landed
+    uint64_t* x_full = d_empty + DS;      // a group's scales landed
+    uint64_t* x_empty = x_full + XS;      // the epilogue is done with them
+    uint64_t* done = x_empty + XS;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -197,23 +211,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int G = sh.K / GROUP;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < C::RS; ++i) {
+        for (int i = 0; i < RS; ++i) {
             mbar_init(&raw_full[i], 1);
             mbar_init(&raw_empty[i], 4);   // expand warps, once they have read the chunk
         }
-        for (int i = 0; i < C::SR; ++i) {
-            mbar_init(&s_full[i], 4);      // expand warps
-            mbar_init(&s_empty[i], 8);     // epilogue warps
-        }
-        for (int i = 0; i < KSr; ++i) {
+        for (int i = 0; i < KS; ++i) {
             mbar_init(&k_full[i], 5);      // 4 expand warps + the activation producer (with its bytes)
             mbar_init(&k_empty[i], 1);     // MMA commit
         }
-        for (int i = 0; i < C::DS; ++i) {
+        for (int i = 0; i < DS; ++i) {
             mbar_init(&d_full[i], 1);      // MMA commit
             mbar_init(&d_empty[i], 8);     // epilogue warps
         }
-        for (int i = 0; i < C::XS; ++i) {
+        for (int i = 0; i < XS; ++i) {
             mbar_init(&x_full[i], 32);     // loader lanes
             mbar_init(&x_empty[i], 8);     // epilogue warps
         }
@@ -230,160 +240,154 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    const uint32_t a_col0 = (uint32_t)(DS * sh.d_stride);   // first weight-operand column
     pdl_trigger();
 
-    if (warp == 12) {
-        // ---------------------------------------------------------- weight producer
-        if (lane == 0) {
-            int rc = 0;
-            bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < sh.num_tiles; tile += gridDim.x) {
-                const int nt = tile / sh.mt_count;
-                for (int g = 0; g < G; ++g) {
-                    const int rs = rc % C::RS;
-                    if (!mbar_wait(&raw_empty[rs], ((rc / C::RS) & 1) ^ 1, status, abort)) {
-                        ok = false;
-                        break;
+    if (warp >= 12) {
+        if (warp == 12) {
+            // ------------------------------------------------------ weight producer
+            if (lane == 0) {
+                int rs = 0, issued = 0;
+                uint32_t rph = 0;
+                bool ok = true;
+                for (int tile = blockIdx.x; ok && tile < sh.num_tiles; tile += gridDim.x) {
+                    const uint8_t* src = blob + (size_t)(tile / sh.mt_count) * G * C::CB;
+                    for (int g = 0; g < G; ++g) {
+                        if (!mbar_wait(&raw_empty[rs], rph ^ 1u, status, abort)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&raw_full[rs], C::CB);
+                        bulk_g2s(raw + (size_t)rs * C::CB, src + (size_t)g * C::CB, C::CB, &raw_full[rs]);
+                        ++issued;
+                        ring_next<RS>(rs, rph);
                     }
-                    mbar_arrive_expect_tx(&raw_full[rs], C::CB);
-                    bulk_g2s(raw + (size_t)rs * C::CB, blob + ((size_t)nt * G + g) * C::CB, C::CB, &raw_full[rs]);
-                    ++rc;
                 }
+                // no copy may still be landing when the CTA exits
+                for (int i = issued - RS > 0 ? issued - RS : 0; i < issued; ++i)
+                    mbar_wait(&raw_full[i % RS], (i / RS) & 1, status, nullptr);
             }
-            // no copy may still be landing when the CTA exits
-            for (int i = rc - C::RS > 0 ? rc - C::RS : 0; i < rc; ++i)
-                mbar_wait(&raw_full[i % C::RS], (i / C::RS) & 1, status, nullptr);
-        }
-    } else if (warp == 15) {
-        // ---------------------------------------------------------- activation producer
-        if (lane == 0) {
-            pdl_wait();   // activations come from the previous kernel
-            int bc = 0;
-            bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < sh.num_tiles; tile += gridDim.x) {
-                const int mt = tile % sh.mt_count;
-                for (int kstep = 0; kstep < G * C::KSG; ++kstep) {
-                    const int bs = bc % KSr;
-                    if (!mbar_wait(&k_empty[bs], ((bc / KSr) & 1) ^ 1, status, abort)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&k_full[bs], (uint32_t)b_bytes);
-                    tma_load_2d(bst + (size_t)bs * b_bytes, &act_map, kstep * 64, mt * m_tile, &k_full[bs]);
-                    ++bc;
-                }
-            }
-            for (int i = bc - KSr > 0 ? bc - KSr : 0; i < bc; ++i)
-                mbar_wait(&k_full[i % KSr], (i / KSr) & 1, status, nullptr);
-        }
-    } else if (warp == 13) {
-        // ---------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc = idesc_f16_f32(128, m_tile);
-            int kc = 0, dc = 0;
-            bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < sh.num_tiles; tile += gridDim.x) {
-                for (int g = 0; ok && g < G; ++g) {
-                    const int db = dc % C::DS;
-                    if (!mbar_wait(&d_empty[db], ((dc / C::DS) & 1) ^ 1, status, abort)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t d_tmem = tmem + (uint32_t)(db * sh.d_stride);
-                    for (int j = 0; j < C::KSG; ++j) {
-                        const int ks = kc % KSr;
-                        if (!mbar_wait(&k_full[ks], (kc / KSr) & 1, status, abort)) {
+        } else if (warp == 13) {
+            // ------------------------------------------------------ MMA issuer
+            if (lane == 0) {
+                const uint32_t idesc = idesc_f16_f32(128, m_tile);
+                int ks = 0, db = 0;
+                uint32_t kph = 0, dph = 0;
+                bool ok = true;
+                for (int tile = blockIdx.x; ok && tile < sh.num_tiles; tile += gridDim.x) {
+                    for (int g = 0; ok && g < G; ++g) {
+                        if (!mbar_wait(&d_empty[db], dph ^ 1u, status, abort)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint64_t bdesc = sdesc_sw128(smem_u32(bst + (size_t)ks * b_bytes));
+                        const uint32_t d_tmem = tmem + (uint32_t)(db * sh.d_stride);
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint32_t accum = (j > 0 || kk > 0) ? 1u : 0u;
-                            if (A_TMEM) {
-                                const uint32_t a_tmem = tmem + (uint32_t)(C::DS * sh.d_stride + 32 * ks + 8 * kk);
-                                mma_f16_ts(d_tmem, a_tmem, bdesc + 2 * kk, idesc, accum);
-                            } else {
-                                const uint64_t adesc = sdesc_sw128(smem_u32(ast + (size_t)ks * 16384));
-                                mma_f16_ss(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, accum);
+                        for (int j = 0; j < KSG; ++j) {
+                            if (!mbar_wait(&k_full[ks], kph, status, abort)) {
+                                ok = false;
+                                break;
                             }
+                            tc_fence_after();
+                            const uint64_t bdesc = sdesc_sw128(smem_u32(bst + (size_t)ks * b_bytes));
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const uint32_t accum = (j > 0 || kk > 0) ? 1u : 0u;
+                                if (A_TMEM) {
+                                    mma_f16_ts(d_tmem, tmem + a_col0 + (uint32_t)(32 * ks + 8 * kk), bdesc + 2 * kk,
+                                               idesc, accum);
+                                } else {
+                                    const uint64_t adesc = sdesc_sw128(smem_u32(ast + (size_t)ks * 16384));
+                                    mma_f16_ss(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, accum);
+                                }
+                            }
+                            tc_commit(&k_empty[ks]);
+                            ring_next<KS>(ks, kph);
                         }
-                        tc_commit(&k_empty[ks]);
-                        ++kc;
+                        if (!ok) break;
+                        tc_commit(&d_full[db]);
+                        ring_next<DS>(db, dph);
                     }
-                    if (!ok) break;
-                    tc_commit(&d_full[db]);
-                    ++dc;
+                }
+                // every issued MMA must retire before the allocation is released
+                tc_commit(done);
+                mbar_wait(done, 0, status, nullptr);
+            }
+        } else if (warp == 14) {
+            // ------------------------------------------------------ scale loader
+            pdl_wait();   // sx / S come from the previous kernel
+            int xs = 0;
+            uint32_t xph = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < sh.num_tiles; tile += gridDim.x) {
+                const int nt = tile / sh.mt_count, mt = tile - nt * sh.mt_count;
+                const int m0 = mt * m_tile;
+                const uint8_t* wsrc = blob + (size_t)nt * G * C::CB + 64 * GROUP;
+                for (int g = 0; g < G; ++g) {
+                    if (!mbar_wait(&x_empty[xs], xph ^ 1u, status, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    // asynchronous copies: the slot's barrier completes when every
+                    // lane's copies have landed
+                    uint8_t* st = scs + (size_t)xs * ssb;
+                    const uint8_t* ws = wsrc + (size_t)g * C::CB;
+#pragma unroll
+                    for (int j = lane; j < C::SWB / 4; j += 32) cp_async_4(st + 4 * j, ws + 4 * j, 4u);
+                    float* sxd = reinterpret_cast<float*>(st + C::SWB);
+                    for (int c = lane; c < m_tile; c += 32) {
+                        const int m = m0 + c;
+                        // rows beyond M, and the partials hook (no scales), read nothing: zero
+                        const bool have = !DEBUG && m < sh.M;
+                        cp_async_4(sxd + c, have ? static_cast<const void*>(act_scale + (size_t)m * G + g)
+                                                 : static_cast<const void*>(blob),
+                                   have ? 4u : 0u);
+                    }
+                    cp_async_arrive(&x_full[xs]);
+                    ring_next<XS>(xs, xph);
                 }
             }
-            // every issued MMA must retire before the allocation is released
-            tc_commit(done);
-            mbar_wait(done, 0, status, nullptr);
-        }
-    } else if (warp == 14) {
-        // ---------------------------------------------------------- scale loader
-        pdl_wait();
-        // no copy may still be landing when the CTA exits (checked below)
-        int xc = 0;
-        bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < sh.num_tiles; tile += gridDim.x) {
-            const int mt = tile % sh.mt_count;
-            const int m0 = mt * m_tile;
-            for (int g = 0; g < G; ++g) {
-                const int s = xc % C::XS;
-                if (!mbar_wait(&x_empty[s], ((xc / C::XS) & 1) ^ 1, status, abort)) {
-                    ok = false;
-                    break;
+            asm volatile("cp.async.wait_all;" ::: "memory");
+        } else {
+            // ------------------------------------------------------ activation producer
+            if (lane == 0) {
+                pdl_wait();   // activations come from the previous kernel
+                int ks = 0, issued = 0;
+                uint32_t kph = 0;
+                bool ok = true;
+                for (int tile = blockIdx.x; ok && tile < sh.num_tiles; tile += gridDim.x) {
+                    const int row0 = (tile % sh.mt_count) * m_tile;
+                    for (int kstep = 0; kstep < G * KSG; ++kstep) {
+                        if (!mbar_wait(&k_empty[ks], kph ^ 1u, status, abort)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&k_full[ks], (uint32_t)b_bytes);
+                        tma_load_2d(bst + (size_t)ks * b_bytes, &act_map, kstep * 64, row0, &k_full[ks]);
+                        ++issued;
+                        ring_next<KS>(ks, kph);
+                    }
                 }
-                // asynchronous copies: the loader never waits for the data, the
-                // slot's barrier completes when every lane's copies have landed
-                float* dst = xs + (size_t)s * m_tile;
-                for (int c = lane; c < m_tile; c += 32) {
-                    const int m = m0 + c;
-                    // rows beyond M, and the partials hook (no scales), read nothing: zero
-                    const bool have = !DEBUG && m < sh.M;
-                    cp_async_4(dst + c, have ? static_cast<const void*>(act_scale + (size_t)m * G + g)
-                                             : static_cast<const void*>(blob),
-                               have ? 4u : 0u);
-                }
-                cp_async_arrive(&x_full[s]);
-                ++xc;
+                for (int i = issued - KS > 0 ? issued - KS : 0; i < issued; ++i)
+                    mbar_wait(&k_full[i % KS], (i / KS) & 1, status, nullptr);
             }
         }
-        asm volatile("cp.async.wait_all;" ::: "memory");
     } else if (warp < 4) {
         // ---------------------------------------------------------- expand
         const int r = threadIdx.x;   // weight row within the tile == tensor-memory lane
-        int kc = 0, rc = 0;
+        int rs = 0, ks = 0;
+        uint32_t rph = 0, kph = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < sh.num_tiles; tile += gridDim.x) {
             for (int g = 0; ok && g < G; ++g) {
-                const int rs = rc % C::RS;
-                if (!mbar_wait(&raw_full[rs], (rc / C::RS) & 1, status, abort)) {
+                if (!mbar_wait(&raw_full[rs], rph, status, abort)) {
                     ok = false;
                     break;
                 }
                 const uint8_t* ch = raw + (size_t)rs * C::CB;
-                {
-                    // the epilogue gets this group's scales (and biases) in a ring of
-                    // its own, so the chunk can be released as soon as it has been read
-                    const int ss = rc % C::SR;
-                    if (!mbar_wait(&s_empty[ss], ((rc / C::SR) & 1) ^ 1, status, abort)) {
-                        ok = false;
-                        break;
-                    }
-                    uint16_t* dst = reinterpret_cast<uint16_t*>(scr + (size_t)ss * C::SCB);
-                    const uint16_t* src = reinterpret_cast<const uint16_t*>(ch + 64 * GROUP);
-                    dst[r] = src[r];
-                    if (VARIANT == 1) dst[128 + r] = src[128 + r];
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&s_full[ss]);
-                }
-                for (int j = 0; j < C::KSG; ++j) {
-                    const int as = kc % KSr;
-                    if (!mbar_wait(&k_empty[as], ((kc / KSr) & 1) ^ 1, status, abort)) {
+#pragma unroll
+                for (int j = 0; j < KSG; ++j) {
+                    if (!mbar_wait(&k_empty[ks], kph ^ 1u, status, abort)) {
                         ok = false;
                         break;
                     }
@@ -399,14 +403,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     expand_word<OFF>(p1.y, hv + 20);
                     expand_word<OFF>(p1.z, hv + 24);
                     expand_word<OFF>(p1.w, hv + 28);
+                    if (j == KSG - 1) {
+                        // the chunk's words are all in registers (the decode used them)
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&raw_empty[rs]);
+                    }
                     if (A_TMEM) {
-                        const uint32_t taddr =
-                            tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(C::DS * sh.d_stride + 32 * as);   // as < KS
-                        tmem_st32(taddr, hv);
+                        tmem_st32(tmem + ((uint32_t)(32 * warp) << 16) + a_col0 + (uint32_t)(32 * ks), hv);
                         tmem_st_wait();
                         tc_fence_before();
                     } else {
-                        uint8_t* row = ast + (size_t)as * 16384 + r * 128;
+                        uint8_t* row = ast + (size_t)ks * 16384 + r * 128;
 #pragma unroll
                         for (int c = 0; c < 8; ++c)
                             *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) * 16)) =
@@ -414,78 +421,71 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         fence_proxy_async_smem();
                     }
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&k_full[as]);
-                    ++kc;
+                    if (lane == 0) mbar_arrive(&k_full[ks]);
+                    ring_next<KS>(ks, kph);
                 }
-                if (!ok) break;
-                if (lane == 0) mbar_arrive(&raw_empty[rs]);   // the warp's reads of the chunk are done
-                ++rc;
+                ring_next<RS>(rs, rph);
             }
         }
-    } else if (warp < 12) {
+    } else {
         // ---------------------------------------------------------- epilogue
         const int q = warp & 3;             // tensor-memory lane quadrant
         const int half = (warp - 4) >> 2;   // column half
         const int r = 32 * q + lane;
         const int ncol = m_tile >> 1;
         const int c0 = half * ncol;
-        const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
-        int dc = 0, rc = 0, xc = 0;
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0;
+        int db = 0, xs = 0;
+        uint32_t dph = 0, xph = 0;
         bool ok = true;
         pdl_wait();   // outputs may still be read by the previous kernel
         for (int tile = blockIdx.x; ok && tile < sh.num_tiles; tile += gridDim.x) {
-            const int nt = tile / sh.mt_count, mt = tile % sh.mt_count;
+            const int nt = tile / sh.mt_count, mt = tile - nt * sh.mt_count;
             const int n = nt * 128 + r;
             const int m0 = mt * m_tile + c0;
-            float acc[MAXC];
+            unsigned long long acc[MAXC / 2];
 #pragma unroll
-            for (int c = 0; c < MAXC; ++c) acc[c] = 0.f;
+            for (int c = 0; c < MAXC / 2; ++c) acc[c] = 0ull;
             for (int g = 0; g < G; ++g) {
-                const int db = dc % C::DS, ss = rc % C::SR, xsi = xc % C::XS;
-                if (!mbar_wait(&d_full[db], (dc / C::DS) & 1, status, abort) ||
-                    !mbar_wait(&s_full[ss], (rc / C::SR) & 1, status, abort) ||
-                    !mbar_wait(&x_full[xsi], (xc / C::XS) & 1, status, abort)) {
+                if (!mbar_wait(&d_full[db], dph, status, abort) || !mbar_wait(&x_full[xs], xph, status, abort)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const __half* sc = reinterpret_cast<const __half*>(scr + (size_t)ss * C::SCB);
-                const float sw = __half2float(sc[r]);
-                const float bw = VARIANT == 1 ? __half2float(sc[128 + r]) : 0.f;
-                const float* sxv = xs + (size_t)xsi * m_tile + c0;
-                const uint32_t dcol = lane_base + (uint32_t)(db * sh.d_stride + c0);
-                // BATCH columns at a time: up to BATCH/8 loads of 8 columns, one wait
-                constexpr int BATCH = 32;
+                const uint8_t* st = scs + (size_t)xs * ssb;
+                const float* sxv = reinterpret_cast<const float*>(st + C::SWB) + c0;
+                const unsigned long long w2 = splat2(__half2float(reinterpret_cast<const __half*>(st)[r]));
+                const unsigned long long b2 =
+                    VARIANT == 1 ? splat2(__half2float(reinterpret_cast<const __half*>(st)[128 + r])) : 0ull;
+                const uint32_t dcol = lane_base + (uint32_t)(db * sh.d_stride);
 #pragma unroll
-                for (int cb = 0; cb < MAXC; cb += BATCH) {
+                for (int cb = 0; cb < MAXC; cb += EB) {
                     if (cb < ncol) {
-                        uint32_t v[32];
+                        uint32_t v[EB];
 #pragma unroll
-                        for (int q8 = 0; q8 < BATCH / 8; ++q8)
-                            if (cb + 8 * q8 < MAXC && cb + 8 * q8 < ncol) tmem_ld8_at(dcol + cb + 8 * q8, v, 8 * q8);
-                        tmem_ld_wait32(v);
+                        for (int q8 = 0; q8 < EB / 8; ++q8)
+                            if (cb + 8 * q8 < ncol) tmem_ld8_at(dcol + cb + 8 * q8, v, 8 * q8);
+                        tmem_ld_wait_n(v);
 #pragma unroll
-                        for (int e4 = 0; e4 < BATCH; e4 += 4) {
-                            if (cb + e4 < MAXC && cb + e4 < ncol) {
-                                const float4 s4 = *reinterpret_cast<const float4*>(sxv + cb + e4);
-                                const int c = cb + e4;
+                        for (int e4 = 0; e4 < EB; e4 += 4) {
+                            if (cb + e4 < ncol) {
                                 if (DEBUG) {
 #pragma unroll
                                     for (int e = 0; e < 4; ++e) {
-                                        const int m = m0 + c + e;
+                                        const int m = m0 + cb + e4 + e;
                                         if (m < sh.M && n < sh.N)
                                             P[((size_t)m * sh.N + n) * G + g] = __float2int_rn(__uint_as_float(v[e4 + e]));
                                     }
-                                } else if (VARIANT == 0) {
-                                    // acc += (P * sx) * sw, two columns per packed instruction
-                                    fma_pair(acc[c], acc[c + 1], mul_pair(v[e4], v[e4 + 1], s4.x, s4.y), sw);
-                                    fma_pair(acc[c + 2], acc[c + 3], mul_pair(v[e4 + 2], v[e4 + 3], s4.z, s4.w), sw);
                                 } else {
-                                    // acc += S * b + P * s
-                                    fma_pair_v(acc[c], acc[c + 1], s4.x, s4.y, bw);
-                                    fma_pair_v(acc[c + 2], acc[c + 3], s4.z, s4.w, bw);
-                                    fma_pair_u(acc[c], acc[c + 1], v[e4], v[e4 + 1], sw);
-                                    fma_pair_u(acc[c + 2], acc[c + 3], v[e4 + 2], v[e4 + 3], sw);
+                                    const float4 s4 = *reinterpret_cast<const float4*>(sxv + cb + e4);
+                                    const int c = (cb + e4) / 2;
+                                    if (VARIANT == 0) {
+                                        acc_w4a8(acc[c], v[e4], v[e4 + 1], s4.x, s4.y, w2);
+                                        acc_w4a8(acc[c + 1], v[e4 + 2], v[e4 + 3], s4.z, s4.w, w2);
+                                    } else {
+                                        acc_affine(acc[c], v[e4], v[e4 + 1], s4.x, s4.y, b2, w2);
+                                        acc_affine(acc[c + 1], v[e4 + 2], v[e4 + 3], s4.z, s4.w, b2, w2);
+                                    }
                                 }
                             }
                         }
@@ -493,20 +493,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&d_empty[db]);
-                    mbar_arrive(&s_empty[ss]);
-                    mbar_arrive(&x_empty[xsi]);
-                }
-                ++dc;
-                ++rc;
-                ++xc;
+                if (lane == 0) mbar_arrive(&d_empty[db]);
+                ring_next<DS>(db, dph);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&x_empty[xs]);
+                ring_next<XS>(xs, xph);
             }
             if (!DEBUG && ok && n < sh.N) {
 #pragma unroll
                 for (int c = 0; c < MAXC; ++c) {
                     const int m = m0 + c;
-                    if (c < ncol && m < sh.M) Y[(size_t)m * sh.N + n] = acc[c];
+                    const uint32_t bits = (uint32_t)(c & 1 ? acc[c / 2] >> 32 : acc[c / 2]);
+                    if (c < ncol && m < sh.M) Y[(size_t)m * sh.N + n] = __uint_as_float(bits);
                 }
             }
         }

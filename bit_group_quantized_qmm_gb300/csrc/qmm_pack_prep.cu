@@ -41,7 +41,9 @@ __global__ void __launch_bounds__(256) pack_kernel(int N, int K, const uint8_t* 
 {
     constexpr int PP = GROUP / 32;
     constexpr int CB = 64 * GROUP + 256 + (VARIANT == 1 ? 256 : 0);
-    pdl_trigger();
+    // No early trigger: the GEMV and GEMM kernels stream packed weights before
+    // their own dependency wait, so a kernel queued right after this one may
+    // start only once every byte of the blob is written.
     pdl_wait();
     const int G = K / GROUP;
     const int T = (N + 127) / 128;

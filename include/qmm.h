@@ -42,7 +42,11 @@
  *   - Device pointers must be 16-byte aligned (QMM_ERR_MISALIGNED otherwise).
  *   - Kernels are launched with programmatic dependent launch: each kernel
  *     streams its packed weights before waiting on the previous kernel in the
- *     stream, and waits before it reads activations or writes outputs.
+ *     stream, and waits before it reads activations or writes outputs. The
+ *     pack kernel lets the next kernel start only when it has finished, so a
+ *     blob packed on the same stream is complete before it is read. A blob
+ *     written by another producer must be complete before the call (any
+ *     kernel that does not trigger its dependents early qualifies).
  *   - Not thread-safe per stream; distinct host threads may use distinct
  *     streams.
  */
