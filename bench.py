@@ -5,11 +5,13 @@ Headline workload (one line of JSON on rank 0): the M = 1 decode projections of
 a Gemma-shaped decoder (gate_up 1536->12288, down 6144->1536, q 1536->2048,
 o 2048->1536), W4A8 with group 64, 64-wide Hadamard rotation of the
 activations, x ~ N(0,1) with 1% +-20 outliers. One step is one decode pass
-over LAYERS layers with their own weights: for each projection the activation
-prepass and the GEMV. The metric is weight+scale bytes streamed per second.
+over LAYERS layers with their own weights: for each projection one fused
+launch (activation prepass + GEMV in one kernel). The metric is weight+scale
+bytes streamed per second.
 The per-step weights (> 2x L2) are larger than L2, so no flush is needed.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--no-sweep]
+  python bench.py --profile-case prefill_gemm:1068     (a few GEMM launches, for ncu)
 
 The step is captured once in a CUDA graph (the kernels are launched with
 programmatic dependent launch, so each GEMV streams its weights while the
@@ -59,6 +61,8 @@ def parse_args():
     p.add_argument("--no-sweep", action="store_true", help="skip the other workloads' extra figures")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--profile-case", default=None, metavar="prefill_gemm:M",
+                   help="run one prefill GEMM shape a few times and exit (for profilers; prints one JSON line)")
     return p.parse_args()
 
 
@@ -490,11 +494,51 @@ def sweep(world):
     return out
 
 
+def profile_case(spec):
+    """A few launches of one prefill GEMM shape (K = 1536, N = 12288, group 64,
+    Hadamard-64): prepass, then 2 + 3 GEMM calls on one packed weight. Small
+    enough to capture under a profiler; the timing printed is informational."""
+    import torch
+    import bit_group_quantized_qmm_gb300 as q
+    name, _, m = spec.partition(":")
+    if name != "prefill_gemm" or not m.isdigit():
+        raise SystemExit(f"unknown profile case {spec!r} (expected prefill_gemm:M)")
+    M, N, K, g = int(m), 12288, 1536, 64
+    dev = torch.device("cuda", torch.cuda.current_device())
+    lay = qmm_synth.Layer("prefill_gemm", W4A8, N, K, g, g)
+    qb, s, _ = qmm_synth.layer_weights(0, "prefill_gemm", lay)
+    d = q.weight_desc(W4A8, N, K, g)
+    packed = torch.empty(q.qmm_packed_size(d), dtype=torch.uint8, device=dev)
+    q.qmm_pack_weights(d, torch.from_numpy(qb).to(dev), torch.from_numpy(s.view(np.int16)).to(dev), None, packed)
+    x = torch.from_numpy(qmm_synth.layer_activations(0, f"prefill_gemm/x{M}", lay, M)).to(dev)
+    a16 = torch.empty((M, K), dtype=torch.float16, device=dev)
+    sx = torch.empty((M, K // g), dtype=torch.float32, device=dev)
+    Y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    q.qmm_prep_act(W4A8, M, K, g, g, x, 0, a16=a16, sx=sx)
+    for _ in range(2):
+        q.qmm_gemm(d, packed, M, a16, sx, Y)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(3):
+        q.qmm_gemm(d, packed, M, a16, sx, Y)
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / 3
+    print(json.dumps({"profile_case": spec, "us_per_call": us, "TOPS": 2 * M * N * K / us / 1e6,
+                      "device_status": q.qmm_device_status()}))
+
+
 # ------------------------------------------------------------------ main
 
 def main():
     args = parse_args()
     rank, world, local = dist_env()
+    if args.profile_case:
+        import torch
+        torch.cuda.set_device(local)
+        profile_case(args.profile_case)
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
         return
