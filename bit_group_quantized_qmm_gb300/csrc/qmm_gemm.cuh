@@ -38,6 +38,9 @@
 //               shared memory); one tensor-memory lane quadrant per warp
 //   warps 4-11  epilogue: rescale each group's partials into register sums
 //               (two warpgroups = two column halves), store Y per tile
+//   (tiles of at most 32 activation rows instead run 8 expand warps, two sets
+//   taking alternate groups, and one epilogue warpgroup, warps 8-11: there
+//   the per-group expand chain, not the rescale, is the critical path)
 //   warp 12     weight producer: 1-D bulk copies of packed chunks
 //   warp 13     MMA issuer; owns the tensor-memory allocation
 //   warp 14     scale loader (weight scales from the blob, sx or S per group)
@@ -175,7 +178,7 @@ __device__ __forceinline__ void ring_next(int& i, uint32_t& ph)
     }
 }
 
-template <int VARIANT, int GROUP, bool A_TMEM, bool DEBUG, int MAXC>
+template <int VARIANT, int GROUP, bool A_TMEM, bool DEBUG, int MAXC, int EXPW>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap act_map, const GemmShape sh, const uint8_t* __restrict__ blob,
                 const float* __restrict__ act_scale, float* __restrict__ Y, int32_t* __restrict__ P, int* status)
@@ -183,6 +186,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     using C = GemmCfg<VARIANT, GROUP, MAXC>;
     constexpr int KS = A_TMEM ? C::KS_TMEM : C::KS_SMEM;
     constexpr int RS = C::RS, DS = C::DS, XS = C::XS, KSG = C::KSG;
+    // EXPW expand warps (4, or 8 = two sets taking alternate groups), then
+    // 12 - EXPW epilogue warps (two column halves with 8, one with 4)
+    static_assert(EXPW == 4 || EXPW == 8, "expand warps");
+    constexpr int EPIW = 12 - EXPW;
     constexpr int EB = C::EB;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -221,11 +228,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         for (int i = 0; i < DS; ++i) {
             mbar_init(&d_full[i], 1);      // MMA commit
-            mbar_init(&d_empty[i], 8);     // epilogue warps
+            mbar_init(&d_empty[i], EPIW);  // epilogue warps
         }
         for (int i = 0; i < XS; ++i) {
             mbar_init(&x_full[i], 32);     // loader lanes
-            mbar_init(&x_empty[i], 8);     // epilogue warps
+            mbar_init(&x_empty[i], EPIW);  // epilogue warps
         }
         mbar_init(done, 1);
         *abort = 0;
@@ -372,14 +379,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     mbar_wait(&k_full[i % KS], (i / KS) & 1, status, nullptr);
             }
         }
-    } else if (warp < 4) {
+    } else if (warp < EXPW) {
         // ---------------------------------------------------------- expand
-        const int r = threadIdx.x;   // weight row within the tile == tensor-memory lane
-        int rs = 0, ks = 0;
+        const int wq = warp & 3;           // tensor-memory lane quadrant
+        const int r = 32 * wq + lane;      // weight row within the tile == tensor-memory lane
+        const int set = warp >> 2;         // with two sets, set s takes the groups g % 2 == s
+        int rs = 0, ks = 0, turn = 0;
         uint32_t rph = 0, kph = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < sh.num_tiles; tile += gridDim.x) {
             for (int g = 0; ok && g < G; ++g) {
+                if (EXPW == 8) {
+                    const bool mine = turn == set;
+                    turn ^= 1;
+                    if (!mine) {   // the other set's group: only the ring positions move
+#pragma unroll
+                        for (int j = 0; j < KSG; ++j) ring_next<KS>(ks, kph);
+                        ring_next<RS>(rs, rph);
+                        continue;
+                    }
+                }
                 if (!mbar_wait(&raw_full[rs], rph, status, abort)) {
                     ok = false;
                     break;
@@ -409,7 +428,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         if (lane == 0) mbar_arrive(&raw_empty[rs]);
                     }
                     if (A_TMEM) {
-                        tmem_st32(tmem + ((uint32_t)(32 * warp) << 16) + a_col0 + (uint32_t)(32 * ks), hv);
+                        tmem_st32(tmem + ((uint32_t)(32 * wq) << 16) + a_col0 + (uint32_t)(32 * ks), hv);
                         tmem_st_wait();
                         tc_fence_before();
                     } else {
@@ -429,10 +448,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
     } else {
         // ---------------------------------------------------------- epilogue
-        const int q = warp & 3;             // tensor-memory lane quadrant
-        const int half = (warp - 4) >> 2;   // column half
+        const int q = warp & 3;                 // tensor-memory lane quadrant
+        const int half = (warp - EXPW) >> 2;    // column half (always 0 with one epilogue warpgroup)
         const int r = 32 * q + lane;
-        const int ncol = m_tile >> 1;
+        const int ncol = EPIW == 8 ? m_tile >> 1 : m_tile;
         const int c0 = half * ncol;
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0;
         int db = 0, xs = 0;
@@ -520,11 +539,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 // Host side: configure and launch one instance of gemm_kernel.
-template <int VARIANT, int GROUP, bool A_TMEM, bool DEBUG, int MAXC>
+template <int VARIANT, int GROUP, bool A_TMEM, bool DEBUG, int MAXC, int EXPW = 4>
 cudaError_t run_gemm(const LaunchCtx& c, const CUtensorMap& map, const GemmShape& sh_in, const uint8_t* blob,
                      const float* act_scale, float* Y, int32_t* P)
 {
-    auto kern = gemm_kernel<VARIANT, GROUP, A_TMEM, DEBUG, MAXC>;
+    auto kern = gemm_kernel<VARIANT, GROUP, A_TMEM, DEBUG, MAXC, EXPW>;
     GemmShape sh = sh_in;
     sh.tmem_cols = gemm_tmem_cols<VARIANT, GROUP, MAXC>(sh.d_stride, !A_TMEM);
     sh.bs = gemm_kstages<VARIANT, GROUP, MAXC>(!A_TMEM);

@@ -15,10 +15,12 @@ static cudaError_t dispatch(const LaunchCtx& c, const CUtensorMap& map, const Ge
         return run_gemm<0, GROUP, true, true, 64>(c, map, sh, blob, sx, Y, P);
     }
     if (a_in_smem) {
+        if (half <= 16) return run_gemm<0, GROUP, false, false, 32, 8>(c, map, sh, blob, sx, Y, P);
         if (half <= 32) return run_gemm<0, GROUP, false, false, 32>(c, map, sh, blob, sx, Y, P);
         if (half <= 48) return run_gemm<0, GROUP, false, false, 48>(c, map, sh, blob, sx, Y, P);
         return run_gemm<0, GROUP, false, false, 64>(c, map, sh, blob, sx, Y, P);
     }
+    if (half <= 16) return run_gemm<0, GROUP, true, false, 32, 8>(c, map, sh, blob, sx, Y, P);
     if (half <= 32) return run_gemm<0, GROUP, true, false, 32>(c, map, sh, blob, sx, Y, P);
     if (half <= 48) return run_gemm<0, GROUP, true, false, 48>(c, map, sh, blob, sx, Y, P);
     return run_gemm<0, GROUP, true, false, 64>(c, map, sh, blob, sx, Y, P);
