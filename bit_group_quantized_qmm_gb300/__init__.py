@@ -22,7 +22,7 @@ QMM_AFFINE = 1
 QMM_DTYPE_F32, QMM_DTYPE_F16, QMM_DTYPE_BF16 = 0, 1, 2
 QMM_PATH_GEMV, QMM_PATH_GEMM = 0, 1
 KERNEL_IDS = {0: "none", 1: "pack", 2: "prep_w4a8", 3: "prep_affine", 4: "gemv_w4a8", 5: "gemm_w4a8",
-              6: "gemm_affine", 7: "gemv_fused"}
+              6: "gemm_affine", 7: "gemv_fused", 8: "gemm_rows"}
 
 STATUS = {0: "QMM_OK", 1: "QMM_ERR_INVALID_ARG", 2: "QMM_ERR_UNSUPPORTED_SHAPE", 3: "QMM_ERR_UNSUPPORTED_DEVICE",
           4: "QMM_ERR_MISALIGNED", 5: "QMM_ERR_CUDA", 6: "QMM_ERR_TIMEOUT", 7: "QMM_ERR_WORKSPACE"}
@@ -60,6 +60,7 @@ def _load():
         "qmm_device_status": (I32, [P, ctypes.POINTER(I32)]),
         "qmm_set_pdl": (None, [I32]),
         "qmm_set_gemm_weight_operand": (None, [I32]),
+        "qmm_set_gemm_rows_max": (None, [I32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -185,3 +186,7 @@ def qmm_set_pdl(enable: bool):
 
 def qmm_set_gemm_weight_operand(in_shared_memory: bool):
     _L.qmm_set_gemm_weight_operand(1 if in_shared_memory else 0)
+
+
+def qmm_set_gemm_rows_max(max_rows: int):
+    _L.qmm_set_gemm_rows_max(int(max_rows))

@@ -31,6 +31,7 @@ DeviceInfo g_devices[kMaxDevices];
 thread_local int32_t g_last_kernel = QMM_KERNEL_NONE;
 int g_pdl = 1;
 int g_a_in_smem = 0;
+int g_rows_max = 8;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -272,11 +273,16 @@ static qmm_status gemm_common(const qmm_weight_desc* w, const void* packed, int3
     if (w->K % 64) return QMM_ERR_UNSUPPORTED_SHAPE;
     LaunchCtx c;
     if ((st = device_ctx(stream, &c)) != QMM_OK) return st;
+    const uint8_t* blob = static_cast<const uint8_t*>(packed);
+    if (w->variant == QMM_W4A8 && !P && M <= g_rows_max) {
+        const cudaError_t e = launch_gemm_rows(c, w->group, M, w->N, w->K, blob,
+                                               static_cast<const uint16_t*>(act16), act_scale, Y);
+        if (e != cudaErrorNotSupported) return launched(e, QMM_KERNEL_GEMM_ROWS);
+    }
     const bool a_smem = g_a_in_smem != 0;
     GemmShape sh = gemm_shape(M, w->N, w->K, a_smem);
     CUtensorMap map;
     if (!act_tensor_map(&map, act16, M, w->K, sh.m_tile)) return QMM_ERR_CUDA;
-    const uint8_t* blob = static_cast<const uint8_t*>(packed);
     if (w->variant == QMM_W4A8)
         return launched(launch_gemm_w4a8(c, w->group, map, sh, blob, act_scale, Y, P, a_smem), QMM_KERNEL_GEMM_W4A8);
     if (P) return QMM_ERR_UNSUPPORTED_SHAPE;
@@ -353,5 +359,7 @@ qmm_status qmm_device_status(qmm_stream stream, int32_t* flags)
 void qmm_set_pdl(int32_t enable) { g_pdl = enable ? 1 : 0; }
 
 void qmm_set_gemm_weight_operand(int32_t in_shared_memory) { g_a_in_smem = in_shared_memory ? 1 : 0; }
+
+void qmm_set_gemm_rows_max(int32_t max_rows) { g_rows_max = max_rows < 0 ? 0 : (max_rows > 16 ? 16 : max_rows); }
 
 }  // extern "C"

@@ -1,0 +1,311 @@
+// qmm_gemm_rows.cu -- the W4A8 GEMM for a few activation rows (M <= 16) on
+// the CUDA cores: exact int32 group partials with dp4a, one pass over the
+// packed weights for all rows.
+//
+// cactus PR #697 "SME2 acceleration for CQ4 matmul, prefill attention, and
+// orthogonal embeddings", Summary: partials are raw integer dot products of
+// the int4 weights and int8 codes, rescaled in fp32 per group; geistlib issue
+// #500 "native W*A8 int8 GEMM for prefill", Design sketch: one activation
+// quantization shared by the GEMV and the GEMM, no dequantized weights.
+//
+// GB300 design. At a handful of rows the GEMM is a weight stream (the whole
+// lm_head blob per call) with at most 16 multiply-adds per weight: the tensor
+// core path spends its time expanding nibbles per 128 x 64 block for one MMA,
+// while the dp4a loop of the GEMV consumes each expanded weight word once per
+// row from registers. So this kernel is the GEMV's structure with M rows:
+// grid = 128-row tiles x K-slices, the slices of a tile forming one
+// thread-block cluster; a producer warp issues the slice's packed chunks as
+// 1-D bulk copies before the dependency wait (weights do not depend on the
+// previous kernel); the compute warps stage the slice's activation codes
+// (given as their exact fp16 image, the GEMM's operand format) as int8 in the
+// dp4a order, then each thread takes one weight row and half the groups,
+// expands each 16-byte nibble piece once and runs it against every row's
+// codes. The halves meet in shared memory, the slices in the cluster's first
+// CTA through distributed shared memory, in a fixed order: deterministic, no
+// workspace, no atomics.
+#include <cuda_fp16.h>
+
+#include "qmm.h"
+#include "qmm_internal.h"
+#include "qmm_ptx.cuh"
+
+namespace qmm {
+
+namespace {
+
+constexpr int kComputeThreads = 256;
+constexpr int kThreads = kComputeThreads + 32;   // + producer warp
+constexpr int kTargetCtas = 2 * 152;
+constexpr int kMaxCluster = 8;                    // portable cluster size
+
+template <int GROUP, int MR>
+struct Cfg {
+    static constexpr int PP = GROUP / 32;         // 16-byte pieces per row and group
+    static constexpr int CB = 64 * GROUP + 256;   // packed chunk bytes
+    static constexpr int NG_MAX = GROUP == 64 ? 24 : 12;   // most chunks a CTA may hold
+    // preferred chunks per CTA: with up to 4 rows the loop is light and long
+    // CTAs keep more bytes in flight; with more rows, short CTAs give the
+    // SM more of them to overlap (measured on the lm_head shape)
+    static constexpr int NG_CAP = MR <= 4 ? NG_MAX : (GROUP == 64 ? 8 : 4);
+};
+
+__device__ __forceinline__ int nib_lo16(uint32_t w) { return (int)(((w << 4) ^ 0x80808080u) & 0xF0F0F0F0u); }
+__device__ __forceinline__ int nib_hi16(uint32_t w) { return (int)((w ^ 0x80808080u) & 0xF0F0F0F0u); }
+__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// Fixed header (same offsets in every CTA of a launch): the slices' partial
+// sums [ksplit][MR][128] (used in the first CTA of a cluster), the halves'
+// sums [MR][128], flags, the cluster barrier and one barrier per chunk.
+__host__ __device__ inline size_t header_bytes(int ksplit, int mr, int ng_max)
+{
+    const size_t b = (size_t)ksplit * mr * 512 + (size_t)mr * 512 + 16 + 8 + 8 * (size_t)ng_max;
+    return (b + 127) / 128 * 128;
+}
+
+size_t smem_bytes(int ksplit, int mr, int ng_max, int group, int cb)
+{
+    return header_bytes(ksplit, mr, ng_max) + (size_t)ng_max * cb + (size_t)ng_max * mr * group +
+           (size_t)ng_max * mr * 4 + 16;
+}
+
+// int8 of an exact fp16 integer code
+__device__ __forceinline__ uint32_t code_byte(uint16_t h)
+{
+    return (uint32_t)__half2int_rn(__ushort_as_half(h)) & 0xFFu;
+}
+
+// Grid (T, ksplit), cluster (1, ksplit): CTA (t, s) handles groups [g0, g1) of
+// tile t for all M (<= MR) rows.
+template <int GROUP, int MR>
+__global__ void __launch_bounds__(kThreads)
+    gemm_rows_kernel(int M, int N, int K, int ksplit, int ng_max, const uint8_t* __restrict__ blob,
+                     const uint16_t* __restrict__ act16, const float* __restrict__ sx, float* __restrict__ Y,
+                     int* status)
+{
+    using C = Cfg<GROUP, MR>;
+    const int G = K / GROUP;
+    const int t = blockIdx.x, s = blockIdx.y;
+    const int g0 = (int)((long long)G * s / ksplit), g1 = (int)((long long)G * (s + 1) / ksplit);
+    const int ng = g1 - g0;
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    float* parts = reinterpret_cast<float*>(smem);                 // [ksplit][MR][128]
+    float* red = parts + (size_t)ksplit * MR * 128;                 // [MR][128]
+    int* flags = reinterpret_cast<int*>(red + MR * 128);           // [4]
+    uint64_t* sums_in = reinterpret_cast<uint64_t*>(flags + 4);     // slices' sums arrived (first CTA)
+    uint64_t* full = sums_in + 1;                                   // [ng_max]
+    uint8_t* stages = smem + header_bytes(ksplit, MR, ng_max);
+    uint8_t* aperm = stages + (size_t)ng_max * C::CB;               // [ng][MR][GROUP] codes, dp4a order
+    float* sxs = reinterpret_cast<float*>(aperm + (size_t)ng_max * MR * GROUP);   // [ng][MR]
+    volatile int* abort = flags;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    pdl_trigger();
+    if (tid == 0) {
+        for (int i = 0; i < ng; ++i) mbar_init(&full[i], 1);
+        mbar_init(sums_in, ksplit > 1 ? ksplit - 1 : 1);
+        flags[0] = 0;
+        fence_barrier_init();
+    }
+    // the other slices arrive on sums_in only once it is initialised
+    if (ksplit > 1)
+        cluster_sync_all();
+    else
+        __syncthreads();
+
+    if (warp == kComputeThreads / 32) {
+        // producer: the whole slice, before the dependency wait
+        if (lane == 0) {
+            const uint8_t* src = blob + ((size_t)t * G + g0) * C::CB;
+            for (int i = 0; i < ng; ++i) {
+                mbar_arrive_expect_tx(&full[i], C::CB);
+                bulk_g2s(stages + (size_t)i * C::CB, src + (size_t)i * C::CB, C::CB, &full[i]);
+            }
+            // the CTA must not exit with copies in flight
+            for (int i = 0; i < ng; ++i) mbar_wait(&full[i], 0, status, nullptr);
+        }
+        __syncwarp();
+        return;
+    }
+
+    // ---------------------------------------------------------- stage codes
+    pdl_wait();   // codes and scales come from the previous kernel
+    {
+        constexpr int B8 = GROUP / 8;   // 8-blocks per group
+        for (int w = tid; w < ng * MR * B8; w += kComputeThreads) {
+            const int c8 = w % B8, rest = w / B8;
+            const int m = rest % MR, i = rest / MR;
+            uint2 perm = make_uint2(0u, 0u);
+            if (m < M) {
+                const uint4 hv = *reinterpret_cast<const uint4*>(act16 + (size_t)m * K + (size_t)(g0 + i) * GROUP +
+                                                                 (size_t)c8 * 8);
+                const uint32_t b0 = code_byte((uint16_t)hv.x), b1 = code_byte((uint16_t)(hv.x >> 16));
+                const uint32_t b2 = code_byte((uint16_t)hv.y), b3 = code_byte((uint16_t)(hv.y >> 16));
+                const uint32_t b4 = code_byte((uint16_t)hv.z), b5 = code_byte((uint16_t)(hv.z >> 16));
+                const uint32_t b6 = code_byte((uint16_t)hv.w), b7 = code_byte((uint16_t)(hv.w >> 16));
+                // dp4a order of an 8-block: k = 0, 4, 1, 5 | 2, 6, 3, 7
+                perm = make_uint2(b0 | (b4 << 8) | (b1 << 16) | (b5 << 24), b2 | (b6 << 8) | (b3 << 16) | (b7 << 24));
+            }
+            *reinterpret_cast<uint2*>(aperm + ((size_t)i * MR + m) * GROUP + (size_t)c8 * 8) = perm;
+        }
+        for (int w = tid; w < ng * MR; w += kComputeThreads) {
+            const int m = w % MR, i = w / MR;
+            sxs[w] = m < M ? sx[(size_t)m * G + g0 + i] : 0.f;
+        }
+    }
+    compute_sync();
+
+    // ---------------------------------------------------------- partials
+    const int r = tid & 127, h = tid >> 7;
+    float acc[MR];
+#pragma unroll
+    for (int m = 0; m < MR; ++m) acc[m] = 0.f;
+    for (int i = h; i < ng; i += 2) {
+        if (!mbar_wait(&full[i], 0, status, abort)) break;
+        const uint8_t* c = stages + (size_t)i * C::CB;
+        int wv[8 * C::PP];   // 16 * q bytes of the row's GROUP weights, in the blob's slot order
+#pragma unroll
+        for (int p = 0; p < C::PP; ++p) {
+            const uint4 w = *reinterpret_cast<const uint4*>(c + p * 2048 + r * 16);
+            wv[8 * p + 0] = nib_lo16(w.x);
+            wv[8 * p + 1] = nib_hi16(w.x);
+            wv[8 * p + 2] = nib_lo16(w.y);
+            wv[8 * p + 3] = nib_hi16(w.y);
+            wv[8 * p + 4] = nib_lo16(w.z);
+            wv[8 * p + 5] = nib_hi16(w.z);
+            wv[8 * p + 6] = nib_lo16(w.w);
+            wv[8 * p + 7] = nib_hi16(w.w);
+        }
+        const float sw = __half2float(reinterpret_cast<const __half*>(c + 64 * GROUP)[r]);
+        // one dp4a chain per row, interleaved piece by piece
+        int dp[MR];
+#pragma unroll
+        for (int m = 0; m < MR; ++m) dp[m] = 0;
+        const uint4* ap = reinterpret_cast<const uint4*>(aperm + (size_t)i * MR * GROUP);
+#pragma unroll
+        for (int p = 0; p < C::PP; ++p) {
+#pragma unroll
+            for (int m = 0; m < MR; ++m) {
+                const uint4 a0 = ap[m * (GROUP / 16) + 2 * p], a1 = ap[m * (GROUP / 16) + 2 * p + 1];
+                dp[m] = __dp4a(wv[8 * p + 0], (int)a0.x, dp[m]);
+                dp[m] = __dp4a(wv[8 * p + 1], (int)a0.y, dp[m]);
+                dp[m] = __dp4a(wv[8 * p + 2], (int)a0.z, dp[m]);
+                dp[m] = __dp4a(wv[8 * p + 3], (int)a0.w, dp[m]);
+                dp[m] = __dp4a(wv[8 * p + 4], (int)a1.x, dp[m]);
+                dp[m] = __dp4a(wv[8 * p + 5], (int)a1.y, dp[m]);
+                dp[m] = __dp4a(wv[8 * p + 6], (int)a1.z, dp[m]);
+                dp[m] = __dp4a(wv[8 * p + 7], (int)a1.w, dp[m]);
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < MR; ++m) acc[m] = fmaf((float)(dp[m] >> 4), sw * sxs[i * MR + m], acc[m]);
+    }
+
+    // ---------------------------------------------------------- reduce, store
+    if (h == 1) {
+#pragma unroll
+        for (int m = 0; m < MR; ++m) red[m * 128 + r] = acc[m];
+    }
+    compute_sync();
+    const int n = t * 128 + r;
+    if (h == 0) {
+#pragma unroll
+        for (int m = 0; m < MR; ++m) {
+            const float v = acc[m] + red[m * 128 + r];
+            if (ksplit == 1) {
+                if (m < M && n < N) Y[(size_t)m * N + n] = v;
+            } else {
+                float* slot = parts + ((size_t)s * MR + m) * 128 + r;
+                if (s == 0)
+                    *slot = v;
+                else
+                    st_shared_cluster_f32(map_shared_rank(smem_u32(slot), 0u), v);
+            }
+        }
+    }
+    if (ksplit > 1) {
+        if (s != 0) {
+            // one release-arrive per slice on the first CTA's barrier
+            compute_sync();
+            if (tid == 0) mbar_arrive_remote(map_shared_rank(smem_u32(sums_in), 0u));
+        } else if (tid < 128) {
+            // the first CTA adds the slices in order once all have arrived
+            mbar_wait_cluster(sums_in, 0, status);
+#pragma unroll
+            for (int m = 0; m < MR; ++m) {
+                float v = 0.f;
+                for (int k = 0; k < ksplit; ++k) v += parts[((size_t)k * MR + m) * 128 + tid];
+                if (m < M && t * 128 + tid < N) Y[(size_t)m * N + t * 128 + tid] = v;
+            }
+        }
+    }
+}
+
+template <int GROUP, int MR>
+cudaError_t run(const LaunchCtx& c, int M, int N, int K, const uint8_t* blob, const uint16_t* act16,
+                const float* sx, float* Y)
+{
+    using C = Cfg<GROUP, MR>;
+    auto kern = gemm_rows_kernel<GROUP, MR>;
+    const int T = (N + 127) / 128, G = K / GROUP;
+    int ks = (kTargetCtas + T - 1) / T;
+    const int ks_ng = (G + C::NG_CAP - 1) / C::NG_CAP;
+    if (ks < ks_ng) ks = ks_ng;
+    if (ks > G) ks = G;
+    if (ks > kMaxCluster) ks = kMaxCluster;
+    if (ks < 1) ks = 1;
+    const int ng_max = (G + ks - 1) / ks;
+    if (ng_max > C::NG_MAX) return cudaErrorNotSupported;   // K too large: the tensor-core path takes it
+    const size_t smem = smem_bytes(ks, MR, ng_max, GROUP, C::CB);
+    static size_t configured = 0;
+    cudaError_t e;
+    if (smem > configured) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        configured = smem;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(T, ks);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = c.stream;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 1;
+    attr[na].val.clusterDim.y = ks;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+    if (c.pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kern, M, N, K, ks, ng_max, blob, act16, sx, Y, c.status);
+}
+
+template <int GROUP>
+cudaError_t dispatch(const LaunchCtx& c, int M, int N, int K, const uint8_t* blob, const uint16_t* act16,
+                     const float* sx, float* Y)
+{
+    if (M <= 2) return run<GROUP, 2>(c, M, N, K, blob, act16, sx, Y);
+    if (M <= 4) return run<GROUP, 4>(c, M, N, K, blob, act16, sx, Y);
+    if (M <= 8) return run<GROUP, 8>(c, M, N, K, blob, act16, sx, Y);
+    if (M <= 16) return run<GROUP, 16>(c, M, N, K, blob, act16, sx, Y);
+    return cudaErrorNotSupported;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_rows(const LaunchCtx& c, int group, int M, int N, int K, const uint8_t* blob,
+                             const uint16_t* act16, const float* sx, float* Y)
+{
+    if (group == 64) return dispatch<64>(c, M, N, K, blob, act16, sx, Y);
+    if (group == 128) return dispatch<128>(c, M, N, K, blob, act16, sx, Y);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace qmm

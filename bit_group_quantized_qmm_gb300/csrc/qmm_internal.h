@@ -72,6 +72,10 @@ struct GemmShape {
 
 cudaError_t launch_gemm_w4a8(const LaunchCtx& c, int group, const CUtensorMap& map, const GemmShape& sh,
                              const uint8_t* blob, const float* sx, float* Y, int32_t* P, bool a_in_smem);
+// W4A8 GEMM for M <= 16 on the CUDA cores; cudaErrorNotSupported when the
+// shape does not fit it (the caller then uses the tensor-core kernel).
+cudaError_t launch_gemm_rows(const LaunchCtx& c, int group, int M, int N, int K, const uint8_t* blob,
+                             const uint16_t* act16, const float* sx, float* Y);
 cudaError_t launch_gemm_affine(const LaunchCtx& c, const CUtensorMap& map, const GemmShape& sh,
                                const uint8_t* blob, const float* gsum, float* Y, bool a_in_smem);
 

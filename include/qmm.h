@@ -87,7 +87,8 @@ typedef enum {
     QMM_KERNEL_GEMV_W4A8 = 4,
     QMM_KERNEL_GEMM_W4A8 = 5,
     QMM_KERNEL_GEMM_AFFINE = 6,
-    QMM_KERNEL_GEMV_FUSED = 7
+    QMM_KERNEL_GEMV_FUSED = 7,
+    QMM_KERNEL_GEMM_ROWS = 8
 } qmm_kernel_id;
 
 typedef void* qmm_stream; /* cudaStream_t */
@@ -255,6 +256,12 @@ qmm_status qmm_gemv_static_scratch(const qmm_weight_desc* w, const void* packed,
  * GEMM, any M >= 1, both variants, on the tcgen05 tensor cores
  * (cactus PR #697, Summary: fused GEMM with raw int32 partials and a separate
  * fp32 rescale; TensorFold PR #3215 for the affine tiles on the prepass sums).
+ * A W4A8 call with M at or below the limit set by qmm_set_gemm_rows_max
+ * (default 8) runs instead on the CUDA cores: exact int32 partials with dp4a,
+ * each weight read once for all rows (qmm_last_kernel_id reports
+ * QMM_KERNEL_GEMM_ROWS); same inputs, same outputs within the W4A8 tolerance.
+ * Shapes that kernel cannot hold (K above 1536 per 8-CTA cluster slice of
+ * 24 groups of 64, or 12 of 128) stay on the tensor cores.
  *   QMM_W4A8:   act16 = qmm_prep_act a16 [M][K] fp16 codes, act_scale = sx [M][G]
  *               Y[m][n] = sum_g sw[n][g] * sx[m][g] * P[m][n][g]
  *   QMM_AFFINE: act16 = x as fp16 [M][K],     act_scale = S  [M][G]
@@ -302,6 +309,12 @@ void qmm_set_pdl(int32_t enable);
  * tcgen05.mma as its A operand; 1 into 128-byte-swizzled shared memory. Both
  * give the same partials; the choice only moves on-chip traffic. */
 void qmm_set_gemm_weight_operand(int32_t in_shared_memory);
+
+/* Largest M for which a W4A8 qmm_gemm runs on the CUDA-core (dp4a) kernel
+ * (process-wide, launches after the call): 0 sends every call to the tensor
+ * cores; values above 16 are treated as 16. Default 8 (above it the tensor
+ * cores are as fast or faster on the measured shapes). */
+void qmm_set_gemm_rows_max(int32_t max_rows);
 
 #ifdef __cplusplus
 }

@@ -71,12 +71,18 @@ def gemv(d, packed, a, sx, workspace=True):
     return y
 
 
-def gemm(d, packed, M, act16, act_scale):
+def gemm(d, packed, M, act16, act_scale, kernel=None):
+    """qmm_gemm into a NaN-filled Y; checks which kernel ran (W4A8: the
+    tensor-core kernel 5 or the CUDA-core small-M kernel 8; affine: 6)."""
     import torch
     q = lib()
     Y = torch.full((M, d.N), float("nan"), dtype=torch.float32, device=dev())
     q.qmm_gemm(d, packed, M, act16, act_scale, Y)
-    assert q.qmm_last_kernel_id() == (5 if d.variant == W4A8 else 6)
+    kid = q.qmm_last_kernel_id()
+    if kernel is not None:
+        assert kid == kernel, kid
+    else:
+        assert kid in ((5, 8) if d.variant == W4A8 else (6,)), kid
     return Y
 
 

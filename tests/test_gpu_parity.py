@@ -314,16 +314,90 @@ def test_lm_head_full_size_sampled(lm_head, orc, M):
     g = lay.group
     x = qmm_synth.layer_activations(0, f"lm_head/x{M}", lay, M)
     a, a16, sx, _, _ = gc.prep_w4a8(x, g, g)
-    Yg = gc.gemm(d, packed, M, a16, sx).cpu().numpy()
+    Yg = gc.gemm(d, packed, M, a16, sx, kernel=8 if M <= 8 else 5).cpu().numpy()
     ra, rsx, _ = orc.prep_w4a8(x, g, g)
     rows = _sample_rows(lay.N)
     Y, Ym = orc.gemm_w4a8(qb, sw, ra, rsx, g, rows=rows)
     ok, worst = gc.within_w4a8(Yg[:, rows], Y, Ym)
     assert ok, f"GEMM worst error / bound = {worst}"
+    if M <= 16:
+        # the same call on the other kernel
+        q = gc.lib()
+        q.qmm_set_gemm_rows_max(0 if M <= 8 else 16)
+        try:
+            Yt = gc.gemm(d, packed, M, a16, sx, kernel=5 if M <= 8 else 8).cpu().numpy()
+        finally:
+            q.qmm_set_gemm_rows_max(ROWS_DEFAULT)
+        ok, worst = gc.within_w4a8(Yt[:, rows], Y, Ym)
+        assert ok, f"tensor-core GEMM worst error / bound = {worst}"
     if M == 1:
         y = gc.gemv(d, packed, a, sx).cpu().numpy()
         ok, worst = gc.within_w4a8(y[None, rows], Y, Ym)
         assert ok, f"GEMV worst error / bound = {worst}"
+
+
+# ------------------------------------------------------------------ small-M GEMM (CUDA cores)
+
+ROWS_DEFAULT = 8   # qmm_set_gemm_rows_max's default
+
+ROWS_CASES = [
+    (1, 256, 256, 64, 64),
+    (2, 200, 192, 64, 0),        # ragged columns, odd group count
+    (3, 384, 1024, 64, 64),
+    (5, 128, 512, 128, 128),
+    (8, 256, 1536, 128, 128),
+    (9, 130, 640, 64, 64),
+    (16, 512, 1536, 64, 64),
+]
+
+
+@pytest.mark.parametrize("M,N,K,group,had", ROWS_CASES)
+def test_gemm_rows_output(torch_cuda, orc, M, N, K, group, had):
+    """M <= 16 W4A8 runs on the dp4a kernel: every output against the oracle,
+    the same call on the tensor cores, and a repeat (deterministic)."""
+    q = gc.lib()
+    qb, sw, x = gc.w4a8_case(11, f"rows/{M}/{N}/{K}", N, K, group, had, M)
+    d, packed = gc.pack(W4A8, N, K, group, qb, sw)
+    _, a16, sx, _, _ = gc.prep_w4a8(x, group, had)
+    q.qmm_set_gemm_rows_max(16)
+    try:
+        Yr = gc.gemm(d, packed, M, a16, sx, kernel=8).cpu().numpy()
+        Yr2 = gc.gemm(d, packed, M, a16, sx, kernel=8).cpu().numpy()
+        assert np.array_equal(Yr, Yr2)
+        q.qmm_set_gemm_rows_max(0)
+        Yt = gc.gemm(d, packed, M, a16, sx, kernel=5).cpu().numpy()
+    finally:
+        q.qmm_set_gemm_rows_max(ROWS_DEFAULT)
+    ra, rsx, _ = orc.prep_w4a8(x, group, had)
+    Y, Ym = orc.gemm_w4a8(qb, sw, ra, rsx, group)
+    for name, Yg in (("dp4a", Yr), ("tensor", Yt)):
+        ok, worst = gc.within_w4a8(Yg, Y, Ym)
+        assert ok, f"{name}: worst error / bound = {worst}"
+
+
+def test_gemm_rows_limit_and_fallback(torch_cuda, orc):
+    """The rows limit picks the kernel; a K too long for one cluster of the
+    dp4a kernel (193 groups of 64) falls back to the tensor cores."""
+    q = gc.lib()
+    M, N, K, group = 4, 128, 193 * 64, 64
+    qb, sw, x = gc.w4a8_case(12, "rows/fallback", N, K, group, 0, M)
+    d, packed = gc.pack(W4A8, N, K, group, qb, sw)
+    _, a16, sx, _, _ = gc.prep_w4a8(x, group, 0)
+    Yg = gc.gemm(d, packed, M, a16, sx, kernel=5).cpu().numpy()
+    ra, rsx, _ = orc.prep_w4a8(x, group, 0)
+    Y, Ym = orc.gemm_w4a8(qb, sw, ra, rsx, group)
+    ok, worst = gc.within_w4a8(Yg, Y, Ym)
+    assert ok, f"worst error / bound = {worst}"
+    qb, sw, x = gc.w4a8_case(13, "rows/limit", 256, 512, 64, 64, 8)
+    d, packed = gc.pack(W4A8, 256, 512, 64, qb, sw)
+    _, a16, sx, _, _ = gc.prep_w4a8(x, 64, 64)
+    gc.gemm(d, packed, ROWS_DEFAULT, a16, sx, kernel=8)     # the library default
+    q.qmm_set_gemm_rows_max(4)
+    try:
+        gc.gemm(d, packed, 4, a16, sx, kernel=8)
+        gc.gemm(d, packed, 8, a16, sx, kernel=5)
+    finally:
+        q.qmm_set_gemm_rows_max(ROWS_DEFAULT)
 
 
 # ------------------------------------------------------------------ affine GEMM
