@@ -104,7 +104,10 @@ __global__ void __launch_bounds__(kThreads)
     pdl_trigger();
     if (tid == 0) {
         for (int i = 0; i < ng; ++i) mbar_init(&full[i], 1);
-        mbar_init(sums_in, ksplit > 1 ? ksplit - 1 : 1);
+        // the other slices' sums land with st.async, completing their bytes on
+        // this barrier
+        mbar_init(sums_in, 1);
+        if (ksplit > 1 && s == 0) mbar_arrive_expect_tx(sums_in, (uint32_t)(ksplit - 1) * MR * 512u);
         flags[0] = 0;
         fence_barrier_init();
     }
@@ -216,19 +219,19 @@ __global__ void __launch_bounds__(kThreads)
             if (ksplit == 1) {
                 if (m < M && n < N) Y[(size_t)m * N + n] = v;
             } else {
-                float* slot = parts + ((size_t)s * MR + m) * 128 + r;
-                if (s == 0)
-                    *slot = v;
-                else
-                    st_shared_cluster_f32(map_shared_rank(smem_u32(slot), 0u), v);
+                parts[((size_t)s * MR + m) * 128 + r] = v;   // this slice's sums, locally first
             }
         }
     }
     if (ksplit > 1) {
         if (s != 0) {
-            // one release-arrive per slice on the first CTA's barrier
+            // the slice's MR x 128 sums go to the first CTA of the cluster as
+            // asynchronous 16-byte stores that complete on its barrier
             compute_sync();
-            if (tid == 0) mbar_arrive_remote(map_shared_rank(smem_u32(sums_in), 0u));
+            const float4* src = reinterpret_cast<const float4*>(parts + (size_t)s * MR * 128);
+            const uint32_t dst = map_shared_rank(smem_u32(parts + (size_t)s * MR * 128), 0u);
+            const uint32_t bar = map_shared_rank(smem_u32(sums_in), 0u);
+            for (int j = tid; j < MR * 32; j += kComputeThreads) st_async_cluster_v4(dst + 16u * j, src[j], bar);
         } else if (tid < 128) {
             // the first CTA adds the slices in order once all have arrived
             mbar_wait_cluster(sums_in, 0, status);

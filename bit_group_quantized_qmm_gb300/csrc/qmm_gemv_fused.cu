@@ -43,7 +43,6 @@ template <int GROUP>
 struct Cfg {
     static constexpr int PP = GROUP / 32;
     static constexpr int CB = 64 * GROUP + 256;
-    static constexpr int E = GROUP / 32;        // inputs per lane in phase A
 };
 
 __device__ __forceinline__ int nib_lo16(uint32_t w) { return (int)(((w << 4) ^ 0x80808080u) & 0xF0F0F0F0u); }
@@ -64,7 +63,9 @@ size_t smem_bytes(int ring, int cb, int ng, int group)
 }
 
 // Grid (T, ksplit), cluster (1, ksplit): CTA (t, s) handles groups [g0, g1) of tile t.
-template <int GROUP, int XDT>
+// EPL inputs per lane in phase A: 8 for long slices; GROUP/32 (a whole warp per
+// group, fewer serial divisions per lane) for short ones.
+template <int GROUP, int XDT, int EPL>
 __global__ void __launch_bounds__(kThreads)
     gemv_fused_kernel(int N, int K, int ksplit, int hadamard, float rot_scale, const uint8_t* __restrict__ blob,
                       const void* __restrict__ x, float* __restrict__ y, int8_t* __restrict__ a_out,
@@ -96,7 +97,11 @@ __global__ void __launch_bounds__(kThreads)
     pdl_trigger();
     if (tid == 0) {
         for (int i = 0; i < ring; ++i) mbar_init(&full[i], 1);
-        mbar_init(sums_in, ksplit > 1 ? ksplit - 1 : 1);
+        // the other slices' sums land with st.async, each completing its bytes
+        // on this barrier; the phase completes when all (ksplit - 1) x 512
+        // bytes are in
+        mbar_init(sums_in, 1);
+        if (ksplit > 1 && s == 0) mbar_arrive_expect_tx(sums_in, (uint32_t)(ksplit - 1) * 512u);
         flags[0] = 0;
         fence_barrier_init();
     }
@@ -122,32 +127,39 @@ __global__ void __launch_bounds__(kThreads)
         __syncwarp();
     } else {
         // ---------------------------------------------------------- phase A
-        // LPG lanes per group, 8 consecutive inputs per lane (one 8-block of
-        // the permuted code layout); GPW groups per warp.
+        // LPG lanes per group, EPL consecutive inputs per lane; GPW groups per
+        // warp. Transform stages below EPL run inside the lane, the others
+        // across lanes, in the ascending order of the page's butterfly.
         pdl_wait();
-        constexpr int LPG = GROUP / 8, GPW = 32 / LPG;
-        const int sub = lane / LPG, c8 = lane % LPG;
+        constexpr int LPG = GROUP / EPL, GPW = 32 / LPG;
+        static_assert(LPG <= 32 && EPL >= 2, "phase A layout");
+        const int sub = lane / LPG, cl = lane % LPG;
         for (int i0 = warp * GPW; i0 < ng; i0 += (kComputeThreads / 32) * GPW) {
             const int i = i0 + sub;
             const bool valid = i < ng;
             const int g = g0 + (valid ? i : 0);
-            const size_t base = (size_t)g * GROUP + (size_t)c8 * 8;
-            float v[8];
-            if (XDT == 0) {
+            const size_t base = (size_t)g * GROUP + (size_t)cl * EPL;
+            float v[EPL];
+            if (XDT == 0 && EPL == 8) {
                 const float4 p0 = reinterpret_cast<const float4*>(static_cast<const float*>(x) + base)[0];
                 const float4 p1 = reinterpret_cast<const float4*>(static_cast<const float*>(x) + base)[1];
                 v[0] = p0.x; v[1] = p0.y; v[2] = p0.z; v[3] = p0.w;
                 v[4] = p1.x; v[5] = p1.y; v[6] = p1.z; v[7] = p1.w;
+            } else if (XDT == 0 && EPL == 4) {
+                const float4 p0 = *reinterpret_cast<const float4*>(static_cast<const float*>(x) + base);
+                v[0] = p0.x; v[1] = p0.y; v[2] = p0.z; v[3] = p0.w;
+            } else if (XDT == 0 && EPL == 2) {
+                const float2 p0 = *reinterpret_cast<const float2*>(static_cast<const float*>(x) + base);
+                v[0] = p0.x; v[1] = p0.y;
             } else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = load_in<XDT>(x, base + e);
+                for (int e = 0; e < EPL; ++e) v[e] = load_in<XDT>(x, base + e);
             }
             if (hadamard) {
-                // butterfly stages h = 1, 2, 4 inside the lane, 8 .. GROUP/2 across lanes
 #pragma unroll
-                for (int h = 1; h < 8; h <<= 1)
+                for (int h = 1; h < EPL; h <<= 1)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
+                    for (int e = 0; e < EPL; ++e)
                         if ((e & h) == 0) {
                             const float lo = v[e], hi = v[e + h];
                             v[e] = __fadd_rn(lo, hi);
@@ -155,9 +167,9 @@ __global__ void __launch_bounds__(kThreads)
                         }
 #pragma unroll
                 for (int lm = 1; lm < LPG; lm <<= 1) {
-                    const bool upper = (c8 & lm) != 0;
+                    const bool upper = (cl & lm) != 0;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
+                    for (int e = 0; e < EPL; ++e) {
                         const float o = __shfl_xor_sync(0xffffffffu, v[e], lm);
                         v[e] = upper ? __fsub_rn(o, v[e]) : __fadd_rn(v[e], o);
                     }
@@ -165,18 +177,18 @@ __global__ void __launch_bounds__(kThreads)
             }
             float amax = 0.f;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(v[e]));
+            for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(v[e]));
 #pragma unroll
             for (int o = 1; o < LPG; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
             float scale = 0.f;
-            uint32_t b[8];
+            uint32_t b[EPL];
             if (amax == 0.f) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) b[e] = 0;
+                for (int e = 0; e < EPL; ++e) b[e] = 0;
             } else {
                 const float sc = __fdiv_rn(amax, 127.0f);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
+                for (int e = 0; e < EPL; ++e) {
                     float r = rintf(__fdiv_rn(v[e], sc));
                     r = fminf(fmaxf(r, -127.f), 127.f);
                     b[e] = (uint32_t)(int)r & 0xFFu;
@@ -184,15 +196,30 @@ __global__ void __launch_bounds__(kThreads)
                 scale = __fmul_rn(sc, rot_scale);
             }
             if (valid) {
-                // dp4a order of an 8-block: k = 0, 4, 1, 5 | 2, 6, 3, 7
-                const uint2 perm = make_uint2(b[0] | (b[4] << 8) | (b[1] << 16) | (b[5] << 24),
-                                              b[2] | (b[6] << 8) | (b[3] << 16) | (b[7] << 24));
-                *reinterpret_cast<uint2*>(aperm + (size_t)i * GROUP + (size_t)c8 * 8) = perm;
-                if (a_out)
-                    *reinterpret_cast<uint2*>(a_out + base) =
-                        make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24),
-                                   b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
-                if (c8 == 0) {
+                uint8_t* blk = aperm + (size_t)i * GROUP + (size_t)(cl * EPL / 8) * 8;
+                if (EPL == 8) {
+                    // dp4a order of an 8-block: k = 0, 4, 1, 5 | 2, 6, 3, 7
+                    *reinterpret_cast<uint2*>(blk) = make_uint2(b[0] | (b[4] << 8) | (b[1] << 16) | (b[5] << 24),
+                                                                b[2] | (b[6] << 8) | (b[3] << 16) | (b[7] << 24));
+                } else {
+                    // this lane's EPL inputs k = k0 .. k0+EPL-1 of an 8-block, at
+                    // their positions in the dp4a order
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e) {
+                        const int k = (cl * EPL + e) & 7;
+                        blk[2 * (k & 3) + (k >> 2)] = (uint8_t)b[e];
+                    }
+                }
+                if (a_out) {
+                    if (EPL == 8)
+                        *reinterpret_cast<uint2*>(a_out + base) =
+                            make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24),
+                                       b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
+                    else
+#pragma unroll
+                        for (int e = 0; e < EPL; ++e) a_out[base + e] = (int8_t)b[e];
+                }
+                if (cl == 0) {
                     sxs[i] = scale;
                     if (sx_out) sx_out[g] = scale;
                 }
@@ -203,8 +230,7 @@ __global__ void __launch_bounds__(kThreads)
         // ---------------------------------------------------------- phase B
         const int r = tid & 127, h = tid >> 7;
         float acc = 0.f;
-        for (int i = h; i < ng; i += 2) {
-            if (!mbar_wait(&full[i], 0, status, abort)) break;
+        auto partial = [&](int i) {
             const uint8_t* c = stages + (size_t)i * C::CB;
             int dp = 0;
 #pragma unroll
@@ -221,8 +247,22 @@ __global__ void __launch_bounds__(kThreads)
                 dp = __dp4a(nib_lo16(w.w), (int)a1.z, dp);
                 dp = __dp4a(nib_hi16(w.w), (int)a1.w, dp);
             }
-            const float sw = __half2float(reinterpret_cast<const __half*>(c + 64 * GROUP)[r]);
-            acc = fmaf((float)(dp >> 4), sw * sxs[i], acc);
+            return dp;
+        };
+        // two groups per step (independent dp4a chains), added in group order
+        for (int i = h; i < ng; i += 4) {
+            const bool two = i + 2 < ng;
+            if (!mbar_wait(&full[i], 0, status, abort)) break;
+            if (two && !mbar_wait(&full[i + 2], 0, status, abort)) break;
+            const int dp0 = partial(i);
+            const int dp1 = two ? partial(i + 2) : 0;
+            const float sw0 = __half2float(reinterpret_cast<const __half*>(stages + (size_t)i * C::CB + 64 * GROUP)[r]);
+            acc = fmaf((float)(dp0 >> 4), sw0 * sxs[i], acc);
+            if (two) {
+                const float sw1 =
+                    __half2float(reinterpret_cast<const __half*>(stages + (size_t)(i + 2) * C::CB + 64 * GROUP)[r]);
+                acc = fmaf((float)(dp1 >> 4), sw1 * sxs[i + 2], acc);
+            }
         }
         if (h == 1) red[r] = acc;
         compute_sync();
@@ -231,16 +271,19 @@ __global__ void __launch_bounds__(kThreads)
             if (ksplit == 1) {
                 if (t * 128 + r < N) y[t * 128 + r] = v;
             } else {
-                // this slice's sums go to the first CTA of the cluster
-                parts[s * 128 + r] = v;   // (rank 0 keeps its own locally)
-                if (s != 0) st_shared_cluster_f32(map_shared_rank(smem_u32(parts + s * 128 + r), 0u), v);
+                parts[s * 128 + r] = v;   // this slice's sums, locally first
             }
         }
         if (ksplit > 1) {
             if (s != 0) {
-                // one release-arrive per slice on the first CTA's barrier
+                // the slice's 128 sums go to the first CTA of the cluster as 32
+                // asynchronous 16-byte stores that complete on its barrier
                 compute_sync();
-                if (tid == 0) mbar_arrive_remote(map_shared_rank(smem_u32(sums_in), 0u));
+                if (warp == 0) {
+                    const float4 v4 = reinterpret_cast<const float4*>(parts + s * 128)[lane];
+                    st_async_cluster_v4(map_shared_rank(smem_u32(parts + s * 128 + 4 * lane), 0u), v4,
+                                        map_shared_rank(smem_u32(sums_in), 0u));
+                }
             } else if (tid < 128) {
                 // the first CTA adds the slices in order once all have arrived
                 mbar_wait_cluster(sums_in, 0, status);
@@ -252,22 +295,31 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
-template <int GROUP, int XDT>
-cudaError_t run(const LaunchCtx& c, int N, int K, int hadamard, const uint8_t* blob, const void* x, float* y,
-                int8_t* a_out, float* sx_out)
+// K-slices per tile: about two CTAs per SM over the grid, at most 16 (one
+// cluster), and few enough groups per CTA for its shared memory (44 chunks of
+// group 64, 22 of group 128).
+int fused_ksplit(int N, int K, int group)
 {
-    using C = Cfg<GROUP>;
-    auto kern = gemv_fused_kernel<GROUP, XDT>;
-    const int T = (N + 127) / 128, G = K / GROUP;
+    const int T = (N + 127) / 128, G = K / group;
     int ks = (kTargetCtas + T - 1) / T;
     if (ks > G) ks = G;
     if (ks > kMaxCluster) ks = kMaxCluster;
     if (ks < 1) ks = 1;
-    // keep a CTA's slice within its shared memory (at most 48 chunks of group 64)
-    const int max_ng = GROUP == 64 ? 44 : 22;
+    const int max_ng = group == 64 ? 44 : 22;
     while ((G + ks - 1) / ks > max_ng && ks < kMaxCluster && ks < G) ++ks;
+    return ks;
+}
+
+template <int GROUP, int XDT, int EPL>
+cudaError_t run(const LaunchCtx& c, int N, int K, int hadamard, const uint8_t* blob, const void* x, float* y,
+                int8_t* a_out, float* sx_out)
+{
+    using C = Cfg<GROUP>;
+    auto kern = gemv_fused_kernel<GROUP, XDT, EPL>;
+    const int G = K / GROUP, T = (N + 127) / 128;
+    const int ks = fused_ksplit(N, K, GROUP);
     const int ng_max = (G + ks - 1) / ks;
-    if (ng_max > max_ng) return cudaErrorInvalidValue;   // K too large for one cluster per tile
+    if (ng_max > (GROUP == 64 ? 44 : 22)) return cudaErrorInvalidValue;   // K too large for one cluster per tile
     const size_t smem = smem_bytes(ng_max, C::CB, ng_max, GROUP);
     static size_t configured = 0;
     cudaError_t e;
@@ -306,15 +358,27 @@ cudaError_t run(const LaunchCtx& c, int N, int K, int hadamard, const uint8_t* b
 cudaError_t launch_gemv_fused(const LaunchCtx& c, int N, int K, int group, int hadamard, const uint8_t* blob,
                               const void* x, int x_dtype, float* y, int8_t* a_out, float* sx_out)
 {
+    // short slices (at most 16 groups per CTA) quantize with a warp per group
+    const bool short_slice = (K / group + fused_ksplit(N, K, group) - 1) / fused_ksplit(N, K, group) <= 16;
     if (group == 64) {
-        if (x_dtype == 0) return run<64, 0>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
-        if (x_dtype == 1) return run<64, 1>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
-        return run<64, 2>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
+        if (short_slice) {
+            if (x_dtype == 0) return run<64, 0, 2>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
+            if (x_dtype == 1) return run<64, 1, 2>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
+            return run<64, 2, 2>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
+        }
+        if (x_dtype == 0) return run<64, 0, 8>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
+        if (x_dtype == 1) return run<64, 1, 8>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
+        return run<64, 2, 8>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
     }
     if (group == 128) {
-        if (x_dtype == 0) return run<128, 0>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
-        if (x_dtype == 1) return run<128, 1>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
-        return run<128, 2>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
+        if (short_slice) {
+            if (x_dtype == 0) return run<128, 0, 4>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
+            if (x_dtype == 1) return run<128, 1, 4>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
+            return run<128, 2, 4>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
+        }
+        if (x_dtype == 0) return run<128, 0, 8>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
+        if (x_dtype == 1) return run<128, 1, 8>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
+        return run<128, 2, 8>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
     }
     return cudaErrorInvalidValue;
 }
