@@ -23,15 +23,15 @@
 // the pace on wide tiles, so it gets the fewest instructions:
 //   - a thread keeps its running sums (up to 64 columns) as packed fp32 pairs
 //     (fma.rn.f32x2 / mul.rn.f32x2: two columns per instruction, each rounded
-//     as the scalar operation) and reads a group's columns with one
-//     tensor-memory round trip up to 48 columns (m_tile <= 96), two batches of
-//     32 at 64;
+//     as the scalar operation) and reads all of a group's columns with one
+//     tensor-memory round trip; the epilogue warpgroups raise their register
+//     budget with setmaxnreg to hold both;
+//   - every column of the instance is loaded and rescaled without column
+//     guards (guarded loops scheduled 1.4x slower);
 //   - one scale stage per group carries the weight scales (+ biases) and the
 //     activation scales, filled by one loader warp with asynchronous copies:
 //     the epilogue waits on two barriers per group (partials, scales), and
 //     the expand warps only expand.
-// (Raising the epilogue's register budget with setmaxnreg, to hold a whole
-// group's columns and overlap the two batches, measured slower on GB300.)
 // Warp roles (512 threads, one CTA per SM, persistent over tiles):
 //   warps 0-3   expand: packed nibbles (smem) -> fp16 weight operand, written
 //               to tensor memory with tcgen05.st (or to 128-byte-swizzled
@@ -57,6 +57,14 @@
 namespace qmm {
 
 constexpr int kGemmThreads = 512;
+// Register budgets after setmaxnreg: the expand and single-role warpgroups drop
+// to 80 per thread, the epilogue warpgroups rise to 176 (a whole group's 64
+// columns and their 64 running sums in registers). With 4 expand warps the
+// four warpgroups sum to exactly the launch's 512 x 128 registers; with 8 the
+// one epilogue warpgroup needs less than is freed.
+constexpr int kGemmRegsLow = 80;
+constexpr int kGemmRegsHigh = 176;
+static_assert(128 * (2 * kGemmRegsLow + 2 * kGemmRegsHigh) <= kGemmThreads * 128, "register split");
 
 // Pipeline depths. Narrow tiles (m_tile <= 64: decode-sized M) keep more
 // k-steps and groups in flight; wide tiles are bound by tensor-memory space.
@@ -69,9 +77,8 @@ struct GemmCfg {
     static constexpr int KS_TMEM = NARROW ? 8 : 4;   // k-step stages, weight operand in tensor memory
     static constexpr int KS_SMEM = 4;                // k-step stages, weight operand in shared memory
     static constexpr int DS = MAXC <= 48 ? 4 : 3;    // accumulator buffers
-    // epilogue columns per tensor-memory round trip (one wait): a whole
-    // group up to 48 columns, two batches of 32 for 64
-    static constexpr int EB = MAXC <= 48 ? MAXC : 32;
+    // epilogue columns per tensor-memory round trip: the whole group
+    static constexpr int EB = MAXC;
     static constexpr int XS = 16;                    // scale stages
     static constexpr int SWB = VARIANT == 1 ? 512 : 256;   // weight scales (+ biases) bytes per stage
 };
@@ -251,6 +258,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     pdl_trigger();
 
     if (warp >= 12) {
+        setmaxnreg_dec<kGemmRegsLow>();   // one instruction for the whole warpgroup
         if (warp == 12) {
             // ------------------------------------------------------ weight producer
             if (lane == 0) {
@@ -380,6 +388,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
         }
     } else if (warp < EXPW) {
+        setmaxnreg_dec<kGemmRegsLow>();
         // ---------------------------------------------------------- expand
         const int wq = warp & 3;           // tensor-memory lane quadrant
         const int r = 32 * wq + lane;      // weight row within the tile == tensor-memory lane
@@ -448,6 +457,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
     } else {
         // ---------------------------------------------------------- epilogue
+        setmaxnreg_inc<kGemmRegsHigh>();
         const int q = warp & 3;                 // tensor-memory lane quadrant
         const int half = (warp - EXPW) >> 2;    // column half (always 0 with one epilogue warpgroup)
         const int r = 32 * q + lane;
@@ -556,12 +566,21 @@ cudaError_t run_gemm(const LaunchCtx& c, const CUtensorMap& map, const GemmShape
     const int first_col = EXPW == 8 ? 0 : sh.m_tile / 2;
     if (!DEBUG && first_col + MAXC > sh.d_stride) return cudaErrorInvalidValue;
     static size_t configured = 0;
+    static int regs = 0;
     cudaError_t e;
     if (smem > configured) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         configured = smem;
     }
+    if (regs == 0) {
+        // the setmaxnreg split draws on the launch's 128 registers per thread
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, kern);
+        if (e != cudaSuccess) return e;
+        regs = fa.numRegs;
+    }
+    if (regs * kGemmThreads != 65536) return cudaErrorInvalidConfiguration;
     int occ = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kGemmThreads, smem);
     if (e != cudaSuccess) return e;
