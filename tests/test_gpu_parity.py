@@ -231,6 +231,46 @@ def test_gemv_fused(torch_cuda, orc, N, K, group, had, outl, x_dtype):
     assert np.array_equal(y.cpu().numpy().view(np.uint32), y1.view(np.uint32)), "not deterministic"
 
 
+def test_pack_then_consume_same_stream(torch_cuda, orc):
+    """A blob packed on the stream is complete before the next kernel reads it:
+    the consumers stream weights before their dependency wait, so the pack must
+    not let them start early. Each consumer runs right after packing into a
+    buffer full of stale bytes, with nothing in between."""
+    import torch
+    q = gc.lib()
+    N, K, g = 32768, 1536, 64
+    qb, sw, x = gc.w4a8_case(14, "pack_then_consume", N, K, g, g, 64)
+    d = q.weight_desc(W4A8, N, K, g)
+    size = q.qmm_packed_size(d)
+    _, a16, sx, _, _ = gc.prep_w4a8(x, g, g)
+    xt = gc.t(x.astype(np.float32))
+    qt, st = gc.t(qb), gc.t(sw)
+    ra, rsx, _ = orc.prep_w4a8(x, g, g)
+    rows = _sample_rows(N)
+    Y, Ym = orc.gemm_w4a8(qb, sw, ra, rsx, g, rows=rows)
+    torch.cuda.synchronize()
+
+    def fresh():
+        return torch.full((size,), 0xFF, dtype=torch.uint8, device=gc.dev())
+
+    # fused GEMV (row 0 of x)
+    blob = fresh()
+    y = torch.full((N,), float("nan"), dtype=torch.float32, device=gc.dev())
+    q.qmm_pack_weights(d, qt, st, None, blob)
+    q.qmm_gemv_fused(d, blob, xt[0], 0, g, y)
+    ok, worst = gc.within_w4a8(y.cpu().numpy()[None, rows], Y[:1], Ym[:1])
+    assert ok, f"fused GEMV: worst error / bound = {worst}"
+    # GEMM on the CUDA cores (M = 2) and on the tensor cores (M = 64)
+    for M, kernel in ((2, 8), (64, 5)):
+        blob = fresh()
+        Yg = torch.full((M, N), float("nan"), dtype=torch.float32, device=gc.dev())
+        q.qmm_pack_weights(d, qt, st, None, blob)
+        q.qmm_gemm(d, blob, M, a16[:M], sx[:M], Yg)
+        assert q.qmm_last_kernel_id() == kernel
+        ok, worst = gc.within_w4a8(Yg.cpu().numpy()[:, rows], Y[:M], Ym[:M])
+        assert ok, f"GEMM M={M}: worst error / bound = {worst}"
+
+
 # ------------------------------------------------------------------ GEMM
 
 GEMM_CASES = [
