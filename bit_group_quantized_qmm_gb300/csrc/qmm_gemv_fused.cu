@@ -130,6 +130,12 @@ __global__ void __launch_bounds__(kThreads)
         // LPG lanes per group, EPL consecutive inputs per lane; GPW groups per
         // warp. Transform stages below EPL run inside the lane, the others
         // across lanes, in the ascending order of the page's butterfly.
+        // The slice of x is warmed in L2 before the dependency wait (a
+        // prefetch returns no data; the loads after the wait read the lines
+        // the previous kernel wrote).
+        constexpr int XSZ = XDT == 0 ? 4 : 2;
+        if (tid == 0)
+            bulk_prefetch_l2(static_cast<const uint8_t*>(x) + (size_t)g0 * GROUP * XSZ, (uint32_t)(ng * GROUP * XSZ));
         pdl_wait();
         constexpr int LPG = GROUP / EPL, GPW = 32 / LPG;
         static_assert(LPG <= 32 && EPL >= 2, "phase A layout");
