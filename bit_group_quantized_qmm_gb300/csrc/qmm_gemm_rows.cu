@@ -133,6 +133,10 @@ __global__ void __launch_bounds__(kThreads)
     }
 
     // ---------------------------------------------------------- stage codes
+    // warm the slice's codes in L2 first (a prefetch returns no data, so it
+    // may run before the dependency wait)
+    if (tid < M)
+        bulk_prefetch_l2(act16 + (size_t)tid * K + (size_t)g0 * GROUP, (uint32_t)(ng * GROUP * 2));
     pdl_wait();   // codes and scales come from the previous kernel
     {
         constexpr int B8 = GROUP / 8;   // 8-blocks per group
