@@ -384,8 +384,9 @@ def run_reference(args, rank, world):
 
 def sweep(world):
     """Extra figures for the other workloads (not the headline): GEMV at
-    K = N = 1024, prefill GEMM TOPS vs M, affine GEMM, lm_head sweep. Each
-    call rotates over enough weight copies to exceed L2 twice."""
+    K = N = 1024, sibling GEMVs (q | k | v) in one launch vs three, prefill
+    GEMM TOPS vs M, affine GEMM, lm_head sweep. Each call rotates over enough
+    weight copies to exceed L2 twice."""
     import torch
     import bit_group_quantized_qmm_gb300 as q
     dev = torch.device("cuda", torch.cuda.current_device())
@@ -423,6 +424,32 @@ def sweep(world):
     t = timed(gemv_pool) / len(pool)
     out["gemv_k1024_n1024"] = {"us_per_call": t * 1e6, "weight_GBps": size / t / 1e9}
     del pool
+
+    # sibling GEMVs sharing x (q | k | v of one layer, K = 1536): one launch vs three
+    Ns, K = (2048, 512, 512), 1536
+    sib = []
+    for i, N in enumerate(Ns):
+        lay_i, d_i, pool_i, size_i = pack_pool(W4A8, N, K, 64, f"siblings/{i}")
+        sib.append((d_i, pool_i, size_i))
+    ncopy = min(len(p[1]) for p in sib)
+    x = torch.from_numpy(qmm_synth.layer_activations(0, "siblings/x", lay_i, 1)).to(dev)[0].contiguous()
+    ys = [torch.empty(N, dtype=torch.float32, device=dev) for N in Ns]
+    descs = [p[0] for p in sib]
+    set_bytes = sum(p[2] for p in sib)
+
+    def separate():
+        for c in range(ncopy):
+            for (d_i, pool_i, _), y_i in zip(sib, ys):
+                q.qmm_gemv_fused(d_i, pool_i[c], x, 0, 64, y_i)
+
+    def together():
+        for c in range(ncopy):
+            q.qmm_gemv_fused_siblings(descs, [p[1][c] for p in sib], x, 0, 64, ys)
+    t_sep = timed(separate) / ncopy
+    t_tog = timed(together) / ncopy
+    out["siblings_qkv"] = {"separate_us": t_sep * 1e6, "one_launch_us": t_tog * 1e6,
+                           "weight_GBps_one_launch": set_bytes / t_tog / 1e9}
+    del sib
 
     # prefill GEMM K=1536 N=12288 vs M
     lay, d, pool, size = pack_pool(W4A8, 12288, 1536, 64, "prefill_gemm")

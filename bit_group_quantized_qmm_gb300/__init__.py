@@ -22,7 +22,7 @@ QMM_AFFINE = 1
 QMM_DTYPE_F32, QMM_DTYPE_F16, QMM_DTYPE_BF16 = 0, 1, 2
 QMM_PATH_GEMV, QMM_PATH_GEMM = 0, 1
 KERNEL_IDS = {0: "none", 1: "pack", 2: "prep_w4a8", 3: "prep_affine", 4: "gemv_w4a8", 5: "gemm_w4a8",
-              6: "gemm_affine", 7: "gemv_fused", 8: "gemm_rows"}
+              6: "gemm_affine", 7: "gemv_fused", 8: "gemm_rows", 9: "gemv_fused_siblings"}
 
 STATUS = {0: "QMM_OK", 1: "QMM_ERR_INVALID_ARG", 2: "QMM_ERR_UNSUPPORTED_SHAPE", 3: "QMM_ERR_UNSUPPORTED_DEVICE",
           4: "QMM_ERR_MISALIGNED", 5: "QMM_ERR_CUDA", 6: "QMM_ERR_TIMEOUT", 7: "QMM_ERR_WORKSPACE"}
@@ -53,6 +53,7 @@ def _load():
         "qmm_gemv": (I32, [D, P, P, P, P, P, SZ, P]),
         "qmm_gemv_static_scratch": (I32, [D, P, P, P, P, P]),
         "qmm_gemv_fused": (I32, [D, P, P, I32, I32, P, P, P, P]),
+        "qmm_gemv_fused_siblings": (I32, [I32, D, P, P, I32, I32, P, P, P, P]),
         "qmm_gemm": (I32, [D, P, I32, P, P, P, P]),
         "qmm_debug_partials": (I32, [D, P, I32, I32, P, P, P]),
         "qmm_status_string": (ctypes.c_char_p, [I32]),
@@ -155,6 +156,18 @@ def qmm_gemv_static_scratch(desc, packed, a, sx, y, stream=None):
 def qmm_gemv_fused(desc, packed, x, x_dtype, hadamard, y, a_out=None, sx_out=None, stream=None):
     _check(_L.qmm_gemv_fused(ctypes.byref(desc), _ptr(packed), _ptr(x), x_dtype, hadamard, _ptr(y), _ptr(a_out),
                              _ptr(sx_out), _stream(stream)), "qmm_gemv_fused")
+
+
+def qmm_gemv_fused_siblings(descs, packed, x, x_dtype, hadamard, ys, a_out=None, sx_out=None, stream=None):
+    """descs, packed, ys: sequences of equal length (the sibling matrices)."""
+    n = len(descs)
+    if len(packed) != n or len(ys) != n:
+        raise ValueError("descs, packed and ys must have the same length")
+    darr = (qmm_weight_desc * max(n, 1))(*descs)
+    parr = (ctypes.c_void_p * max(n, 1))(*[_ptr(p) for p in packed])
+    yarr = (ctypes.c_void_p * max(n, 1))(*[_ptr(v) for v in ys])
+    _check(_L.qmm_gemv_fused_siblings(n, darr, parr, _ptr(x), x_dtype, hadamard, yarr, _ptr(a_out), _ptr(sx_out),
+                                      _stream(stream)), "qmm_gemv_fused_siblings")
 
 
 def qmm_gemm(desc, packed, M, act16, act_scale, Y, stream=None):

@@ -261,6 +261,39 @@ qmm_status qmm_gemv_fused(const qmm_weight_desc* w, const void* packed, const vo
                     QMM_KERNEL_GEMV_FUSED);
 }
 
+qmm_status qmm_gemv_fused_siblings(int32_t count, const qmm_weight_desc* w, const void* const* packed,
+                                   const void* x, int32_t x_dtype, int32_t hadamard, float* const* y,
+                                   int8_t* a_out, float* sx_out, qmm_stream stream)
+{
+    if (count < 1 || count > QMM_MAX_SIBLINGS || count > kMaxSiblings || !w || !packed || !y || !x)
+        return QMM_ERR_INVALID_ARG;
+    int N[QMM_MAX_SIBLINGS];
+    const uint8_t* blobs[QMM_MAX_SIBLINGS];
+    float* ys[QMM_MAX_SIBLINGS];
+    for (int i = 0; i < count; ++i) {
+        qmm_status st = shape_ok(&w[i]);
+        if (st != QMM_OK) return st;
+        if (w[i].variant != QMM_W4A8 || w[i].K != w[0].K || w[i].group != w[0].group)
+            return QMM_ERR_UNSUPPORTED_SHAPE;
+        if (!packed[i] || !y[i]) return QMM_ERR_INVALID_ARG;
+        if (!aligned16(packed[i]) || !aligned16(y[i])) return QMM_ERR_MISALIGNED;
+        N[i] = w[i].N;
+        blobs[i] = static_cast<const uint8_t*>(packed[i]);
+        ys[i] = y[i];
+    }
+    if (hadamard != 0 && hadamard != w[0].group) return QMM_ERR_UNSUPPORTED_SHAPE;
+    if (x_dtype != QMM_DTYPE_F32 && x_dtype != QMM_DTYPE_F16 && x_dtype != QMM_DTYPE_BF16) return QMM_ERR_INVALID_ARG;
+    if (!aligned16(x) || (a_out && !aligned16(a_out)) || (sx_out && !aligned16(sx_out))) return QMM_ERR_MISALIGNED;
+    const int max_k = 16 * (w[0].group == 64 ? 44 : 22) * w[0].group;
+    if (w[0].K > max_k) return QMM_ERR_UNSUPPORTED_SHAPE;
+    LaunchCtx c;
+    qmm_status st = device_ctx(stream, &c);
+    if (st != QMM_OK) return st;
+    return launched(launch_gemv_fused_set(c, count, N, w[0].K, w[0].group, hadamard, blobs, x, x_dtype, ys, a_out,
+                                          sx_out),
+                    QMM_KERNEL_GEMV_FUSED_SIBLINGS);
+}
+
 static qmm_status gemm_common(const qmm_weight_desc* w, const void* packed, int32_t M, const void* act16,
                               const float* act_scale, float* Y, int32_t* P, qmm_stream stream)
 {

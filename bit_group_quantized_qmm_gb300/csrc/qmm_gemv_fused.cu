@@ -57,23 +57,38 @@ __device__ __forceinline__ float load_in(const void* x, size_t i)
     return __bfloat162float(static_cast<const __nv_bfloat16*>(x)[i]);
 }
 
+// The weight matrices of one launch (siblings share x, K and the group size):
+// matrix i owns grid rows [tile0[i], tile0[i + 1]).
+struct FusedSet {
+    int count;
+    int tile0[kMaxSiblings + 1];
+    int N[kMaxSiblings];
+    const uint8_t* blob[kMaxSiblings];
+    float* y[kMaxSiblings];
+};
+
 size_t smem_bytes(int ring, int cb, int ng, int group)
 {
     return kHeaderBytes + (size_t)ring * cb + (size_t)ng * group + (size_t)ng * 4 + 16;
 }
 
-// Grid (T, ksplit), cluster (1, ksplit): CTA (t, s) handles groups [g0, g1) of tile t.
+// Grid (sum of the matrices' tiles, ksplit), cluster (1, ksplit): CTA (b, s)
+// handles groups [g0, g1) of tile t of the matrix that owns grid row b.
 // EPL inputs per lane in phase A: 8 for long slices; GROUP/32 (a whole warp per
 // group, fewer serial divisions per lane) for short ones.
 template <int GROUP, int XDT, int EPL>
 __global__ void __launch_bounds__(kThreads)
-    gemv_fused_kernel(int N, int K, int ksplit, int hadamard, float rot_scale, const uint8_t* __restrict__ blob,
-                      const void* __restrict__ x, float* __restrict__ y, int8_t* __restrict__ a_out,
-                      float* __restrict__ sx_out, int* status)
+    gemv_fused_kernel(const __grid_constant__ FusedSet set, int K, int ksplit, int hadamard, float rot_scale,
+                      const void* __restrict__ x, int8_t* __restrict__ a_out, float* __restrict__ sx_out, int* status)
 {
     using C = Cfg<GROUP>;
     const int G = K / GROUP;
-    const int t = blockIdx.x, s = blockIdx.y;
+    int mi = 0;
+    while (mi + 1 < set.count && (int)blockIdx.x >= set.tile0[mi + 1]) ++mi;
+    const int t = blockIdx.x - set.tile0[mi], s = blockIdx.y;
+    const int N = set.N[mi];
+    const uint8_t* __restrict__ blob = set.blob[mi];
+    float* __restrict__ y = set.y[mi];
     const int g0 = (int)((long long)G * s / ksplit), g1 = (int)((long long)G * (s + 1) / ksplit);
     const int ng = g1 - g0;
     const int ring = ng;   // the launcher keeps a CTA's whole slice resident
@@ -304,9 +319,9 @@ __global__ void __launch_bounds__(kThreads)
 // K-slices per tile: about two CTAs per SM over the grid, at most 16 (one
 // cluster), and few enough groups per CTA for its shared memory (44 chunks of
 // group 64, 22 of group 128).
-int fused_ksplit(int N, int K, int group)
+int fused_ksplit(int T, int K, int group)
 {
-    const int T = (N + 127) / 128, G = K / group;
+    const int G = K / group;
     int ks = (kTargetCtas + T - 1) / T;
     if (ks > G) ks = G;
     if (ks > kMaxCluster) ks = kMaxCluster;
@@ -317,13 +332,13 @@ int fused_ksplit(int N, int K, int group)
 }
 
 template <int GROUP, int XDT, int EPL>
-cudaError_t run(const LaunchCtx& c, int N, int K, int hadamard, const uint8_t* blob, const void* x, float* y,
-                int8_t* a_out, float* sx_out)
+cudaError_t run(const LaunchCtx& c, const FusedSet& set, int K, int hadamard, const void* x, int8_t* a_out,
+                float* sx_out)
 {
     using C = Cfg<GROUP>;
     auto kern = gemv_fused_kernel<GROUP, XDT, EPL>;
-    const int G = K / GROUP, T = (N + 127) / 128;
-    const int ks = fused_ksplit(N, K, GROUP);
+    const int G = K / GROUP, T = set.tile0[set.count];
+    const int ks = fused_ksplit(T, K, GROUP);
     const int ng_max = (G + ks - 1) / ks;
     if (ng_max > (GROUP == 64 ? 44 : 22)) return cudaErrorInvalidValue;   // K too large for one cluster per tile
     const size_t smem = smem_bytes(ng_max, C::CB, ng_max, GROUP);
@@ -356,37 +371,50 @@ cudaError_t run(const LaunchCtx& c, int N, int K, int hadamard, const uint8_t* b
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, kern, N, K, ks, hadamard, rot, blob, x, y, a_out, sx_out, c.status);
+    return cudaLaunchKernelEx(&cfg, kern, set, K, ks, hadamard, rot, x, a_out, sx_out, c.status);
+}
+
+template <int GROUP, int EPL>
+cudaError_t run_dtype(const LaunchCtx& c, const FusedSet& set, int K, int hadamard, const void* x, int x_dtype,
+                      int8_t* a_out, float* sx_out)
+{
+    if (x_dtype == 0) return run<GROUP, 0, EPL>(c, set, K, hadamard, x, a_out, sx_out);
+    if (x_dtype == 1) return run<GROUP, 1, EPL>(c, set, K, hadamard, x, a_out, sx_out);
+    return run<GROUP, 2, EPL>(c, set, K, hadamard, x, a_out, sx_out);
 }
 
 }  // namespace
 
+cudaError_t launch_gemv_fused_set(const LaunchCtx& c, int count, const int* N, int K, int group, int hadamard,
+                                  const uint8_t* const* blob, const void* x, int x_dtype, float* const* y,
+                                  int8_t* a_out, float* sx_out)
+{
+    if (count < 1 || count > kMaxSiblings) return cudaErrorInvalidValue;
+    FusedSet set = {};
+    set.count = count;
+    set.tile0[0] = 0;
+    for (int i = 0; i < count; ++i) {
+        set.N[i] = N[i];
+        set.blob[i] = blob[i];
+        set.y[i] = y[i];
+        set.tile0[i + 1] = set.tile0[i] + (N[i] + 127) / 128;
+    }
+    // short slices (at most 16 groups per CTA) quantize with a warp per group
+    const int ks = fused_ksplit(set.tile0[count], K, group);
+    const bool short_slice = (K / group + ks - 1) / ks <= 16;
+    if (group == 64)
+        return short_slice ? run_dtype<64, 2>(c, set, K, hadamard, x, x_dtype, a_out, sx_out)
+                           : run_dtype<64, 8>(c, set, K, hadamard, x, x_dtype, a_out, sx_out);
+    if (group == 128)
+        return short_slice ? run_dtype<128, 4>(c, set, K, hadamard, x, x_dtype, a_out, sx_out)
+                           : run_dtype<128, 8>(c, set, K, hadamard, x, x_dtype, a_out, sx_out);
+    return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_gemv_fused(const LaunchCtx& c, int N, int K, int group, int hadamard, const uint8_t* blob,
                               const void* x, int x_dtype, float* y, int8_t* a_out, float* sx_out)
 {
-    // short slices (at most 16 groups per CTA) quantize with a warp per group
-    const bool short_slice = (K / group + fused_ksplit(N, K, group) - 1) / fused_ksplit(N, K, group) <= 16;
-    if (group == 64) {
-        if (short_slice) {
-            if (x_dtype == 0) return run<64, 0, 2>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
-            if (x_dtype == 1) return run<64, 1, 2>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
-            return run<64, 2, 2>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
-        }
-        if (x_dtype == 0) return run<64, 0, 8>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
-        if (x_dtype == 1) return run<64, 1, 8>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
-        return run<64, 2, 8>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
-    }
-    if (group == 128) {
-        if (short_slice) {
-            if (x_dtype == 0) return run<128, 0, 4>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
-            if (x_dtype == 1) return run<128, 1, 4>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
-            return run<128, 2, 4>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
-        }
-        if (x_dtype == 0) return run<128, 0, 8>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
-        if (x_dtype == 1) return run<128, 1, 8>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
-        return run<128, 2, 8>(c, N, K, hadamard, blob, x, y, a_out, sx_out);
-    }
-    return cudaErrorInvalidValue;
+    return launch_gemv_fused_set(c, 1, &N, K, group, hadamard, &blob, x, x_dtype, &y, a_out, sx_out);
 }
 
 }  // namespace qmm

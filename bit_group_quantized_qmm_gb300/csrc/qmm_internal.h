@@ -57,6 +57,12 @@ cudaError_t launch_gemv(const LaunchCtx& c, int N, int K, int group, const uint8
 constexpr int kMaxMTile = 128;
 
 // One-kernel decode GEMV: prepass of x and GEMV (optional code/scale outputs).
+// Fused prepass + GEMV over up to kMaxSiblings weight matrices that share x,
+// K and the group size (one launch; matrix i writes y[i]).
+constexpr int kMaxSiblings = 8;
+cudaError_t launch_gemv_fused_set(const LaunchCtx& c, int count, const int* N, int K, int group, int hadamard,
+                                  const uint8_t* const* blob, const void* x, int x_dtype, float* const* y,
+                                  int8_t* a_out, float* sx_out);
 cudaError_t launch_gemv_fused(const LaunchCtx& c, int N, int K, int group, int hadamard, const uint8_t* blob,
                               const void* x, int x_dtype, float* y, int8_t* a_out, float* sx_out);
 

@@ -88,7 +88,8 @@ typedef enum {
     QMM_KERNEL_GEMM_W4A8 = 5,
     QMM_KERNEL_GEMM_AFFINE = 6,
     QMM_KERNEL_GEMV_FUSED = 7,
-    QMM_KERNEL_GEMM_ROWS = 8
+    QMM_KERNEL_GEMM_ROWS = 8,
+    QMM_KERNEL_GEMV_FUSED_SIBLINGS = 9
 } qmm_kernel_id;
 
 typedef void* qmm_stream; /* cudaStream_t */
@@ -228,6 +229,26 @@ qmm_status qmm_gemv(const qmm_weight_desc* w, const void* packed, const int8_t* 
  */
 qmm_status qmm_gemv_fused(const qmm_weight_desc* w, const void* packed, const void* x, int32_t x_dtype,
                           int32_t hadamard, float* y, int8_t* a_out, float* sx_out, qmm_stream stream);
+
+/*
+ * Fused sibling GEMVs, QMM_W4A8: up to QMM_MAX_SIBLINGS weight matrices that
+ * read the same input (q|k|v, gate|up) in one launch, x rotated and quantized
+ * once per K-slice for all of them (cactus engine PR #750 "Metal Support":
+ * sibling quantized GEMVs fused into one batched dispatch; geistlib issue #500,
+ * Design sketch item 5: paired linears share one activation quantization).
+ *   w[i], packed[i]  the matrices: same variant (W4A8), K and group; any N[i]
+ *   x, x_dtype, hadamard, a_out, sx_out   as qmm_gemv_fused
+ *   y[i]             device fp32 [w[i].N]
+ * Each y[i] matches qmm_gemv_fused on matrix i within the W4A8 tolerance (the
+ * K-slice split, and with it the fp32 sum order, follows the launch's total
+ * tile count); results are deterministic.
+ * QMM_ERR_INVALID_ARG for count outside [1, QMM_MAX_SIBLINGS] or NULL
+ * pointers; QMM_ERR_UNSUPPORTED_SHAPE for mismatched K, group or variant.
+ */
+#define QMM_MAX_SIBLINGS 8
+qmm_status qmm_gemv_fused_siblings(int32_t count, const qmm_weight_desc* w, const void* const* packed,
+                                   const void* x, int32_t x_dtype, int32_t hadamard, float* const* y,
+                                   int8_t* a_out, float* sx_out, qmm_stream stream);
 
 /*
  * M = 1 GEMV for callers that cannot allocate device memory. The pages have no

@@ -68,6 +68,19 @@ def test_host_validation(q):
     assert L.qmm_debug_partials(D(q.weight_desc(1, 256, 256, 64)), A, 1, 0, A, A, None) == SHAPE
     assert L.qmm_debug_partials(D(d), A, 2, 0, A, A, None) == INV    # GEMV path needs M == 1
     assert L.qmm_debug_partials(D(d), A, 1, 9, A, A, None) == INV
+    # sibling GEMVs: count, per-matrix shape agreement, alignment
+    descs = (q.qmm_weight_desc * 3)(q.weight_desc(0, 256, 256, 64), q.weight_desc(0, 128, 256, 64),
+                                    q.weight_desc(0, 64, 256, 64))
+    ptrs = (ctypes.c_void_p * 3)(A, A, A)
+    assert L.qmm_gemv_fused_siblings(0, descs, ptrs, A, 0, 64, ptrs, None, None, None) == INV
+    assert L.qmm_gemv_fused_siblings(9, descs, ptrs, A, 0, 64, ptrs, None, None, None) == INV
+    assert L.qmm_gemv_fused_siblings(3, descs, ptrs, A + 8, 0, 64, ptrs, None, None, None) == MIS
+    mixed = (q.qmm_weight_desc * 2)(q.weight_desc(0, 256, 256, 64), q.weight_desc(0, 256, 512, 64))
+    assert L.qmm_gemv_fused_siblings(2, mixed, ptrs, A, 0, 64, ptrs, None, None, None) == SHAPE
+    grp = (q.qmm_weight_desc * 2)(q.weight_desc(0, 256, 256, 64), q.weight_desc(0, 256, 256, 128))
+    assert L.qmm_gemv_fused_siblings(2, grp, ptrs, A, 0, 64, ptrs, None, None, None) == SHAPE
+    nulls = (ctypes.c_void_p * 3)(A, None, A)
+    assert L.qmm_gemv_fused_siblings(3, descs, nulls, A, 0, 64, ptrs, None, None, None) == INV
 
 
 def test_valid_arguments_reach_the_device_probe(q):

@@ -231,6 +231,49 @@ def test_gemv_fused(torch_cuda, orc, N, K, group, had, outl, x_dtype):
     assert np.array_equal(y.cpu().numpy().view(np.uint32), y1.view(np.uint32)), "not deterministic"
 
 
+SIBLING_CASES = [
+    ((2048, 512, 512), 1536, 64, 64),     # q | k | v
+    ((6144, 6144), 1536, 64, 64),         # gate | up
+    ((200, 100, 384), 512, 64, 0),        # ragged tiles, no rotation
+    ((256, 130), 1024, 128, 128),
+]
+
+
+@pytest.mark.parametrize("Ns,K,group,had", SIBLING_CASES)
+def test_gemv_fused_siblings(torch_cuda, orc, Ns, K, group, had):
+    """Sibling matrices in one launch: shared codes/scales bit-exact, every
+    output within tolerance of the oracle, deterministic."""
+    import torch
+    q = gc.lib()
+    dev = gc.dev()
+    x = None
+    descs, packs, ys, refs = [], [], [], []
+    for i, N in enumerate(Ns):
+        qb, sw, xi = gc.w4a8_case(20 + i, f"siblings/{i}/{N}/{K}", N, K, group, had, 1)
+        x = xi if x is None else x
+        d, packed = gc.pack(W4A8, N, K, group, qb, sw)
+        descs.append(d)
+        packs.append(packed)
+        ys.append(torch.full((N,), float("nan"), dtype=torch.float32, device=dev))
+        refs.append((qb, sw))
+    a = torch.empty(K, dtype=torch.int8, device=dev)
+    sx = torch.empty(K // group, dtype=torch.float32, device=dev)
+    xt = gc.t(x[0].astype(np.float32))
+    q.qmm_gemv_fused_siblings(descs, packs, xt, 0, had, ys, a, sx)
+    assert q.qmm_last_kernel_id() == 9
+    ra, rsx, _ = orc.prep_w4a8(x, group, had)
+    assert np.array_equal(a.cpu().numpy(), ra[0])
+    assert np.array_equal(sx.cpu().numpy().view(np.uint32), rsx[0].view(np.uint32))
+    first = [y.cpu().numpy().copy() for y in ys]
+    for (qb, sw), y in zip(refs, first):
+        Y, Ym = orc.gemm_w4a8(qb, sw, ra, rsx, group)
+        ok, worst = gc.within_w4a8(y[None, :], Y, Ym)
+        assert ok, f"worst error / bound = {worst}"
+    q.qmm_gemv_fused_siblings(descs, packs, xt, 0, had, ys)
+    for y0, y in zip(first, ys):
+        assert np.array_equal(y.cpu().numpy().view(np.uint32), y0.view(np.uint32)), "not deterministic"
+
+
 def test_pack_then_consume_same_stream(torch_cuda, orc):
     """A blob packed on the stream is complete before the next kernel reads it:
     the consumers stream weights before their dependency wait, so the pack must
