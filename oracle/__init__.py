@@ -28,6 +28,7 @@ LIB = os.path.join(HERE, "libqmm_oracle.so")
 
 W4A8 = 0
 AFFINE = 1
+CQ4 = 2
 
 CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-Wall"]
 
@@ -73,6 +74,9 @@ def _bind(path: str):
     L.oracle_gemm_w4a8_rows.argtypes = [i, i, i, i, P, P, P, P, i, P, P, P]
     L.oracle_group_sums_affine.argtypes = [i, i, i, P, P]
     L.oracle_gemm_affine_rows.argtypes = [i, i, i, i, P, P, P, P, i, P, P, P]
+    L.oracle_pack_cq4.argtypes = [i, i, i, P, P, c.c_float, P, P]
+    L.oracle_partials_cq4.argtypes = [i, i, i, i, P, P, P, P]
+    L.oracle_gemm_cq4_rows.argtypes = [i, i, i, i, P, P, c.c_float, P, P, P, i, P, P, P]
     return L
 
 
@@ -191,6 +195,39 @@ class Oracle:
         _check(self.L.oracle_gemm_w4a8_rows(M, N, K, group, _p(q_bytes), _p(_c(sw, np.uint16)), _p(a),
                                             _p(_c(sx, np.float32)), nr, _p(r), _p(Y), _p(Ym)),
                "gemm_w4a8")
+        return Y, Ym
+
+    # -------------------------------------------------------------- CQ4
+    def pack_cq4(self, N, K, group, idx_bytes, codebook, cb_scale, scales) -> np.ndarray:
+        out = np.empty(self.packed_size(CQ4, N, K, group), dtype=np.uint8)
+        _check(self.L.oracle_pack_cq4(N, K, group, _p(_c(idx_bytes, np.uint8)), _p(_c(codebook, np.int8)),
+                                      float(cb_scale), _p(_c(scales, np.uint16)), _p(out)), "pack_cq4")
+        return out
+
+    def partials_cq4(self, idx_bytes, codebook, a, group) -> np.ndarray:
+        """P int32 [M][N][G] with P = sum codebook[index] * a."""
+        idx_bytes = _c(idx_bytes, np.uint8)
+        a = _c(a, np.int8)
+        M, K = a.shape
+        N = idx_bytes.shape[0]
+        P = np.empty((M, N, K // group), dtype=np.int32)
+        _check(self.L.oracle_partials_cq4(M, N, K, group, _p(idx_bytes), _p(_c(codebook, np.int8)), _p(a), _p(P)),
+               "partials_cq4")
+        return P
+
+    def gemm_cq4(self, idx_bytes, codebook, cb_scale, sw, a, sx, group, rows=None):
+        """(Y, Ymag) float64 [M][len(rows)] (all N rows when rows is None)."""
+        idx_bytes = _c(idx_bytes, np.uint8)
+        a = _c(a, np.int8)
+        M, K = a.shape
+        N = idx_bytes.shape[0]
+        r = None if rows is None else _c(rows, np.int32)
+        nr = N if r is None else r.size
+        Y = np.empty((M, nr), dtype=np.float64)
+        Ym = np.empty((M, nr), dtype=np.float64)
+        _check(self.L.oracle_gemm_cq4_rows(M, N, K, group, _p(idx_bytes), _p(_c(codebook, np.int8)), float(cb_scale),
+                                           _p(_c(sw, np.uint16)), _p(a), _p(_c(sx, np.float32)), nr, _p(r), _p(Y),
+                                           _p(Ym)), "gemm_cq4")
         return Y, Ym
 
     # -------------------------------------------------------------- affine

@@ -138,7 +138,7 @@ int oracle_unpack_nibbles(int variant, int N, int K, const uint8_t* q_bytes, int
 static int blob_ok(int variant, int N, int K, int group)
 {
     if (N < 1 || K < 1) return 0;
-    if (variant == ORACLE_W4A8) return (group == 64 || group == 128) && K % group == 0;
+    if (variant == ORACLE_W4A8 || variant == ORACLE_CQ4) return (group == 64 || group == 128) && K % group == 0;
     if (variant == ORACLE_AFFINE) return group == 64 && K % group == 0;
     return 0;
 }
@@ -152,7 +152,7 @@ size_t oracle_packed_size(int variant, int N, int K, int group)
 {
     if (!blob_ok(variant, N, K, group)) return 0;
     size_t T = (size_t)(N + 127) / 128;
-    return T * (size_t)(K / group) * chunk_bytes(variant, group);
+    return T * (size_t)(K / group) * chunk_bytes(variant, group) + (variant == ORACLE_CQ4 ? ORACLE_CQ4_TRAILER : 0);
 }
 
 static size_t nibble_offset(int r, int kl, int* high)
@@ -445,4 +445,91 @@ int oracle_gemm_affine(int M, int N, int K, int group, const uint8_t* q_bytes,
                        double* Y, double* Ymag)
 {
     return oracle_gemm_affine_rows(M, N, K, group, q_bytes, s, b, x16, N, NULL, Y, Ymag);
+}
+
+/* ------------------------------------------------------------ CQ4 */
+
+/*
+ * Codebook 4-bit weights (cactus PR #697 "SME2 acceleration for CQ4 matmul,
+ * prefill attention, and orthogonal embeddings", Summary: in-engine 4-bit
+ * codebook expansion in the GEMV leaf; follow-up "single runtime weight
+ * format": codebook table lookup, a single fp32 rescale with the codebook
+ * scale folded into the per-row norms).
+ * Reading: each weight is a 4-bit index i (even k in the low nibble) into one
+ * 16-entry int8 codebook C of the matrix; the weight is cb_scale * sw * C[i].
+ * The partial stays integer, P[m][n][g] = sum_{k in g} C[i[n][k]] * a[m][k],
+ * and the output is Y = sum_g (sw * cb_scale) * sx * P (here exactly, fp64).
+ * Blob: the symmetric tile layout with the raw indices as nibbles, then a
+ * 32-byte trailer: C[0..15] (int8), cb_scale (fp32), 12 zero bytes.
+ */
+int oracle_pack_cq4(int N, int K, int group, const uint8_t* idx_bytes, const int8_t* codebook, float cb_scale,
+                    const uint16_t* scales, uint8_t* blob)
+{
+    if (!blob_ok(ORACLE_CQ4, N, K, group)) return 1;
+    int8_t* q = malloc((size_t)N * K);
+    if (!q) return 2;
+    oracle_unpack_nibbles(ORACLE_CQ4, N, K, idx_bytes, q);
+    int rc = oracle_pack_from_values(ORACLE_CQ4, N, K, group, q, scales, NULL, blob);
+    free(q);
+    if (rc) return rc;
+    uint8_t* tr = blob + oracle_packed_size(ORACLE_CQ4, N, K, group) - ORACLE_CQ4_TRAILER;
+    memcpy(tr, codebook, 16);
+    memcpy(tr + 16, &cb_scale, 4);
+    return 0;
+}
+
+int oracle_partials_cq4(int M, int N, int K, int group, const uint8_t* idx_bytes, const int8_t* codebook,
+                        const int8_t* a, int32_t* P)
+{
+    if (M < 1 || N < 1 || K % group != 0) return 1;
+    int G = K / group;
+    int8_t* idx = malloc((size_t)N * K);
+    if (!idx) return 2;
+    oracle_unpack_nibbles(ORACLE_CQ4, N, K, idx_bytes, idx);
+    for (int m = 0; m < M; m++)
+        for (int n = 0; n < N; n++)
+            for (int g = 0; g < G; g++) {
+                int64_t acc = 0;
+                for (int kl = 0; kl < group; kl++) {
+                    int k = g * group + kl;
+                    acc += (int64_t)codebook[idx[(size_t)n * K + k]] * a[(size_t)m * K + k];
+                }
+                P[((size_t)m * N + n) * G + g] = (int32_t)acc;
+            }
+    free(idx);
+    return 0;
+}
+
+/* Y and Ymag (sum of |terms|, the tolerance scale) for the listed rows. */
+int oracle_gemm_cq4_rows(int M, int N, int K, int group, const uint8_t* idx_bytes, const int8_t* codebook,
+                         float cb_scale, const uint16_t* sw, const int8_t* a, const float* sx, int n_rows,
+                         const int32_t* rows, double* Y, double* Ymag)
+{
+    if (M < 1 || N < 1 || K % group != 0 || n_rows < 1) return 1;
+    int G = K / group;
+    int8_t* idx = malloc((size_t)K);
+    if (!idx) return 2;
+    for (int i = 0; i < n_rows; i++) {
+        int n = rows ? rows[i] : i;
+        if (n < 0 || n >= N) { free(idx); return 1; }
+        oracle_unpack_nibbles(ORACLE_CQ4, 1, K, idx_bytes + (size_t)n * (K / 2), idx);
+        for (int m = 0; m < M; m++) {
+            double y = 0.0, mag = 0.0;
+            for (int g = 0; g < G; g++) {
+                int64_t p = 0;
+                for (int kl = 0; kl < group; kl++) {
+                    int k = g * group + kl;
+                    p += (int64_t)codebook[idx[k]] * a[(size_t)m * K + k];
+                }
+                double t = oracle_f16_to_f64(sw[(size_t)n * G + g]) * (double)cb_scale * (double)sx[(size_t)m * G + g] *
+                           (double)p;
+                y += t;
+                mag += fabs(t);
+            }
+            Y[(size_t)m * n_rows + i] = y;
+            if (Ymag) Ymag[(size_t)m * n_rows + i] = mag;
+        }
+    }
+    free(idx);
+    return 0;
 }

@@ -18,6 +18,8 @@
 
 #define ORACLE_W4A8 0
 #define ORACLE_AFFINE 1
+#define ORACLE_CQ4 2
+#define ORACLE_CQ4_TRAILER 32
 
 double oracle_f16_to_f64(uint16_t h);
 uint16_t oracle_f64_to_f16(double v);
@@ -53,5 +55,13 @@ int oracle_gemm_affine(int M, int N, int K, int group, const uint8_t* q_bytes,
 int oracle_gemm_affine_rows(int M, int N, int K, int group, const uint8_t* q_bytes,
                             const uint16_t* s, const uint16_t* b, const uint16_t* x16,
                             int n_rows, const int32_t* rows, double* Y, double* Ymag);
+
+int oracle_pack_cq4(int N, int K, int group, const uint8_t* idx_bytes, const int8_t* codebook, float cb_scale,
+                    const uint16_t* scales, uint8_t* blob);
+int oracle_partials_cq4(int M, int N, int K, int group, const uint8_t* idx_bytes, const int8_t* codebook,
+                        const int8_t* a, int32_t* P);
+int oracle_gemm_cq4_rows(int M, int N, int K, int group, const uint8_t* idx_bytes, const int8_t* codebook,
+                         float cb_scale, const uint16_t* sw, const int8_t* a, const float* sx, int n_rows,
+                         const int32_t* rows, double* Y, double* Ymag);
 
 #endif

@@ -80,6 +80,27 @@ def nibble_bytes(seed: int, stream: str, N: int, K: int) -> np.ndarray:
     return d.astype("<u8").view(np.uint8)[:nbytes].reshape(N, K // 2).copy()
 
 
+def codebook_i8(seed: int, stream: str) -> np.ndarray:
+    """16 distinct int8 levels in [-127, 127], ascending.
+
+    The first 16 distinct values of the uniform draws mapped onto [-127, 127]
+    (a non-uniform level set, so that no entry is an affine function of its
+    index).
+    """
+    d = draws(seed, stream, 256)
+    vals = (d % np.uint64(255)).astype(np.int64) - 127
+    _, first = np.unique(vals, return_index=True)
+    picked = vals[np.sort(first)[:16]]
+    assert picked.size == 16
+    return np.sort(picked).astype(np.int8)
+
+
+def uniform_f32(seed: int, stream: str, lo: float, hi: float) -> float:
+    """One fp32 U(lo, hi) draw (rounded to nearest even), as a Python float."""
+    u = unit_uniform(draws(seed, stream, 1))[0]
+    return float(np.float32(lo + (hi - lo) * u))
+
+
 def uniform_f16(seed: int, stream: str, shape, lo: float, hi: float) -> np.ndarray:
     """fp16 bit patterns (uint16) of U(lo, hi) draws rounded to nearest even."""
     n = int(np.prod(shape))
@@ -132,6 +153,7 @@ def activations_f16(seed: int, stream: str, M: int, K: int) -> np.ndarray:
 
 W4A8 = 0
 AFFINE = 1
+CQ4 = 2
 
 
 @dataclass
@@ -198,6 +220,15 @@ def layer_weights(seed: int, prefix: str, layer: Layer):
     if layer.variant == AFFINE:
         b = uniform_f16(seed, f"{prefix}/biases", (layer.N, G), layer.bias_lo, layer.bias_hi)
     return q, s, b
+
+
+def layer_codebook(seed: int, prefix: str):
+    """(codebook int8 [16], cb_scale fp32) of a codebook-4-bit layer.
+
+    cb_scale ~ U(0.04, 0.08) puts cb_scale * max|C| near the symmetric
+    variant's largest level (8), so weights span the same range.
+    """
+    return codebook_i8(seed, f"{prefix}/codebook"), uniform_f32(seed, f"{prefix}/cb_scale", 0.04, 0.08)
 
 
 def layer_activations(seed: int, prefix: str, layer: Layer, M: int):

@@ -17,7 +17,7 @@ import scipy.linalg
 import qmm_synth
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-W4A8, AFFINE = 0, 1
+W4A8, AFFINE, CQ4 = 0, 1, 2
 
 
 # ----------------------------------------------------------------- fixtures
@@ -341,6 +341,116 @@ def pin_gemm_w4a8_dequant(orc):
         assert np.array_equal(Yr, Y[:, rows]) and np.array_equal(Ymr, Ymag[:, rows])
 
 
+# ----------------------------------------------------------------- CQ4
+
+def _cq4_identity(q_bytes):
+    """Index bytes that, with C[i] = i - 8, reproduce the symmetric nibbles.
+
+    A two's-complement nibble u stands for q = u - 16*(u >= 8); its index in the
+    ascending level set -8..7 is q + 8 = u XOR 8.
+    """
+    return (q_bytes ^ 0x88).astype(np.uint8), np.arange(-8, 8, dtype=np.int8)
+
+
+def pin_cq4_identity_codebook_equals_w4a8(orc):
+    """The identity codebook with cb_scale 1 is the symmetric variant, bit for bit."""
+    for M, N, K, group, had in ((3, 70, 256, 64, 64), (2, 33, 256, 128, 0)):
+        lay = qmm_synth.Layer("w", W4A8, N, K, group, had)
+        q_bytes, sw, _ = qmm_synth.layer_weights(21, f"pin/cq4id/{group}", lay)
+        x = qmm_synth.layer_activations(21, f"pin/cq4id/{group}", lay, M)
+        a, sx, _ = orc.prep_w4a8(x, group, had)
+        idx, C = _cq4_identity(q_bytes)
+        assert np.array_equal(orc.partials_cq4(idx, C, a, group), orc.partials_w4a8(q_bytes, a, group))
+        Yc, Ymc = orc.gemm_cq4(idx, C, 1.0, sw, a, sx, group)
+        Yw, Ymw = orc.gemm_w4a8(q_bytes, sw, a, sx, group)
+        assert np.array_equal(Yc, Yw) and np.array_equal(Ymc, Ymw)
+        # the blobs agree before the trailer on whole 128-row tiles (padding
+        # rows differ: index 0 there, the symmetric q = 0 stored as 8)
+        Nt = N - N % 128 or 128
+        q_t, sw_t = np.resize(q_bytes, (Nt, K // 2)), np.resize(sw, (Nt, K // group))
+        idx_t, _ = _cq4_identity(q_t)
+        bc = orc.pack_cq4(Nt, K, group, idx_t, C, 1.0, sw_t)
+        bw = orc.pack(W4A8, Nt, K, group, q_t, sw_t)
+        assert bc.size == bw.size + 32 and np.array_equal(bc[:-32], bw)
+
+
+def pin_cq4_partials_brute_force(orc):
+    for M, N, K, group in ((2, 3, 128, 64), (1, 2, 256, 128)):
+        idx = qmm_synth.nibble_bytes(22, "pin/cq4p", N, K)
+        C = qmm_synth.codebook_i8(22, f"pin/cq4p/cb/{group}")
+        a = (qmm_synth.draws(22, "pin/cq4p/a", M * K) % np.uint64(255)).astype(np.int64) - 127
+        a = a.reshape(M, K).astype(np.int8)
+        P = orc.partials_cq4(idx, C, a, group)
+        i = _unpack(idx, K, CQ4)
+        for m in range(M):
+            for n in range(N):
+                for g in range(K // group):
+                    ref = 0
+                    for k in range(g * group, (g + 1) * group):
+                        ref += int(C[i[n, k]]) * int(a[m, k])
+                    assert P[m, n, g] == ref
+        # bound |P| <= 127 * 127 * group, reached by C = -127 everywhere, a = -127
+        worst = np.full(16, -127, dtype=np.int8)
+        Pw = orc.partials_cq4(idx[:1], worst, np.full((1, K), -127, dtype=np.int8), group)
+        assert np.all(Pw == 127 * 127 * group)
+
+
+def pin_cq4_dequant_and_invariances(orc):
+    """Integer-group form == dequantize-then-fp64-matmul; relabeling and scale laws."""
+    for M, N, K, group, had in ((4, 96, 256, 64, 64), (2, 40, 512, 128, 128)):
+        lay = qmm_synth.Layer("w", CQ4, N, K, group, had)
+        idx, sw, _ = qmm_synth.layer_weights(23, f"pin/cq4/{group}", lay)
+        C, cb = qmm_synth.layer_codebook(23, f"pin/cq4/{group}")
+        x = qmm_synth.layer_activations(23, f"pin/cq4/{group}", lay, M)
+        a, sx, _ = orc.prep_w4a8(x, group, had)
+        Y, Ymag = orc.gemm_cq4(idx, C, cb, sw, a, sx, group)
+        i = _unpack(idx, K, CQ4)
+        swf = sw.view(np.float16).astype(np.float64)
+        Wd = float(np.float32(cb)) * C.astype(np.float64)[i] * np.repeat(swf, group, axis=1)
+        Ad = a.astype(np.float64) * np.repeat(sx.astype(np.float64), group, axis=1)
+        ref = Ad @ Wd.T
+        assert np.all(np.abs(Y - ref) <= 1e-12 * Ymag + 1e-300)
+        # relabeling: permute the table and the indices with it -> same partials
+        perm = (np.arange(16) * 7 + 3) % 16                  # a permutation of 0..15
+        inv = np.argsort(perm)
+        C2 = C[perm]                                         # C2[j] = C[perm[j]]
+        i2 = inv[i]                                          # C2[i2] = C[perm[inv[i]]] = C[i]
+        idx2 = (i2[:, 0::2] | (i2[:, 1::2] << 4)).astype(np.uint8)
+        assert np.array_equal(orc.partials_cq4(idx2, C2, a, group), orc.partials_cq4(idx, C, a, group))
+        # negating the table or doubling cb_scale scales Y exactly
+        Yn, _ = orc.gemm_cq4(idx, (-C.astype(np.int16)).astype(np.int8), cb, sw, a, sx, group)
+        assert np.array_equal(Yn, -Y)
+        Y2, _ = orc.gemm_cq4(idx, C, 2.0 * cb, sw, a, sx, group)
+        assert np.array_equal(Y2, 2.0 * Y)
+        # sampled rows agree with the full result
+        rows = np.array([N - 1, 0, N // 2], dtype=np.int32)
+        Yr, Ymr = orc.gemm_cq4(idx, C, cb, sw, a, sx, group, rows=rows)
+        assert np.array_equal(Yr, Y[:, rows]) and np.array_equal(Ymr, Ymag[:, rows])
+
+
+def pin_cq4_blob_trailer_and_roundtrip(orc):
+    N, K, group = 130, 192, 64
+    idx = qmm_synth.nibble_bytes(24, "pin/cq4b", N, K)
+    sw = qmm_synth.uniform_f16(24, "pin/cq4b/s", (N, K // group), 0.005, 0.02)
+    C = qmm_synth.codebook_i8(24, "pin/cq4b/cb")
+    cb = 0.0625
+    blob = orc.pack_cq4(N, K, group, idx, C, cb, sw)
+    T, G = (N + 127) // 128, K // group
+    assert blob.size == orc.packed_size(CQ4, N, K, group) == T * G * (64 * group + 256) + 32
+    tr = blob[-32:]
+    assert np.array_equal(tr[:16].view(np.int8), C)
+    assert tr[16:20].view("<f4")[0] == np.float32(cb)
+    assert not tr[20:].any()
+    q, s, _ = orc.unpack_blob(CQ4, N, K, group, blob)
+    assert np.array_equal(q, _unpack(idx, K, CQ4)) and np.array_equal(s, sw)
+    # the nibbles are stored raw: the symmetric variant reads index i as i - 8
+    qs, _, _ = orc.unpack_blob(W4A8, N, K, group, blob)
+    assert np.array_equal(qs.astype(np.int64), _unpack(idx, K, CQ4) - 8)
+    # padding rows of the last tile hold index 0 and zero scales
+    qp, sp, _ = orc.unpack_blob(CQ4, T * 128, K, group, blob)
+    assert not qp[N:].any() and not sp[N:].any()
+
+
 # ----------------------------------------------------------------- affine
 
 def pin_group_sum_tree_fixture(orc):
@@ -392,4 +502,6 @@ ALL_PINS = [
     pin_nibble_order, pin_pack_positions, pin_pack_roundtrip_and_invariance,
     pin_partials_brute_force, pin_gemm_w4a8_dequant,
     pin_group_sum_tree_fixture, pin_group_sums_close_to_exact, pin_affine_dequant_and_bias,
+    pin_cq4_identity_codebook_equals_w4a8, pin_cq4_partials_brute_force, pin_cq4_dequant_and_invariances,
+    pin_cq4_blob_trailer_and_roundtrip,
 ]

@@ -55,6 +55,15 @@ MUTANTS = [
      "return (size_t)p * 16 + (size_t)r * 32 + 4 * j + s / 2;", [P.pin_pack_positions]),
     ("f16_exponent", "v = ldexp((double)(1024 + f), e - 25);", "v = ldexp((double)(1024 + f), e - 24);",
      [P.pin_f16_to_f64]),
+    ("cq4_cb_scale_dropped", "oracle_f16_to_f64(sw[(size_t)n * G + g]) * (double)cb_scale * (double)sx",
+     "oracle_f16_to_f64(sw[(size_t)n * G + g]) * (double)sx", [P.pin_cq4_dequant_and_invariances]),
+    ("cq4_gemm_no_lookup", "p += (int64_t)codebook[idx[k]] * a[(size_t)m * K + k];",
+     "p += (int64_t)(idx[k] - 8) * a[(size_t)m * K + k];", [P.pin_cq4_dequant_and_invariances]),
+    ("cq4_partials_signed_index", "acc += (int64_t)codebook[idx[(size_t)n * K + k]] * a[(size_t)m * K + k];",
+     "acc += (int64_t)codebook[idx[(size_t)n * K + k] ^ 8] * a[(size_t)m * K + k];",
+     [P.pin_cq4_identity_codebook_equals_w4a8, P.pin_cq4_partials_brute_force]),
+    ("cq4_trailer_scale_offset", "memcpy(tr + 16, &cb_scale, 4);", "memcpy(tr + 20, &cb_scale, 4);",
+     [P.pin_cq4_blob_trailer_and_roundtrip]),
     ("f16_round_truncate", "double q = rint(ldexp(a, 10 - E));", "double q = floor(ldexp(a, 10 - E));",
      [P.pin_f64_to_f16]),
 ]

@@ -49,3 +49,13 @@ def test_workload_catalogue():
     assert set(w) == {"gemv_k1024_n1024", "gemma_decode", "prefill_gemm", "affine_gemm", "lm_head"}
     assert [l.name for l in w["gemma_decode"].layers] == ["gate_up", "down", "q", "o"]
     assert w["lm_head"].layers[0].group == 128 and w["lm_head"].Ms == [1, 2, 4, 8, 16, 32]
+
+
+def test_codebook_levels():
+    C = qmm_synth.codebook_i8(0, "cb")
+    assert C.dtype == np.int8 and C.size == 16
+    assert np.all(np.diff(C.astype(np.int64)) > 0)            # distinct, ascending
+    assert C.min() >= -127 and C.max() <= 127
+    assert np.array_equal(C, qmm_synth.codebook_i8(0, "cb"))
+    C2, cb = qmm_synth.layer_codebook(1, "w")
+    assert 0.04 <= cb <= 0.08 and float(np.float32(cb)) == cb
