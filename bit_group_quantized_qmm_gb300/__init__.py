@@ -19,10 +19,12 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "qmm.h")
 
 QMM_W4A8 = 0
 QMM_AFFINE = 1
+QMM_CQ4 = 2
 QMM_DTYPE_F32, QMM_DTYPE_F16, QMM_DTYPE_BF16 = 0, 1, 2
 QMM_PATH_GEMV, QMM_PATH_GEMM = 0, 1
 KERNEL_IDS = {0: "none", 1: "pack", 2: "prep_w4a8", 3: "prep_affine", 4: "gemv_w4a8", 5: "gemm_w4a8",
-              6: "gemm_affine", 7: "gemv_fused", 8: "gemm_rows", 9: "gemv_fused_siblings"}
+              6: "gemm_affine", 7: "gemv_fused", 8: "gemm_rows", 9: "gemv_fused_siblings", 10: "gemv_cq4",
+              11: "gemm_cq4"}
 
 STATUS = {0: "QMM_OK", 1: "QMM_ERR_INVALID_ARG", 2: "QMM_ERR_UNSUPPORTED_SHAPE", 3: "QMM_ERR_UNSUPPORTED_DEVICE",
           4: "QMM_ERR_MISALIGNED", 5: "QMM_ERR_CUDA", 6: "QMM_ERR_TIMEOUT", 7: "QMM_ERR_WORKSPACE"}
@@ -48,6 +50,7 @@ def _load():
     sig = {
         "qmm_packed_size": (SZ, [D]),
         "qmm_pack_weights": (I32, [D, P, P, P, P, P]),
+        "qmm_pack_weights_cq4": (I32, [D, P, P, ctypes.c_float, P, P, P]),
         "qmm_prep_act": (I32, [I32, I32, I32, I32, I32, P, I32, P, P, P, P, P, P, P]),
         "qmm_gemv_workspace_size": (SZ, [D]),
         "qmm_gemv": (I32, [D, P, P, P, P, P, SZ, P]),
@@ -128,6 +131,17 @@ def qmm_packed_size(desc: qmm_weight_desc) -> int:
 def qmm_pack_weights(desc, q, scales, biases, packed, stream=None):
     _check(_L.qmm_pack_weights(ctypes.byref(desc), _ptr(q), _ptr(scales), _ptr(biases), _ptr(packed),
                                _stream(stream)), "qmm_pack_weights")
+
+
+def qmm_pack_weights_cq4(desc, idx, codebook, cb_scale, scales, packed, stream=None):
+    """codebook: 16 int8 levels on the host (anything numpy.asarray(..., int8) accepts)."""
+    import numpy as np
+    levels = np.ascontiguousarray(np.asarray(codebook, dtype=np.int8).reshape(-1))
+    if levels.size != 16:
+        raise ValueError("a CQ4 codebook has 16 levels")
+    _check(_L.qmm_pack_weights_cq4(ctypes.byref(desc), _ptr(idx), levels.ctypes.data_as(ctypes.c_void_p),
+                                   float(cb_scale), _ptr(scales), _ptr(packed), _stream(stream)),
+           "qmm_pack_weights_cq4")
 
 
 def qmm_prep_act(variant, M, K, group, hadamard, x, x_dtype, a=None, a16=None, sx=None, asum=None, gsum=None,

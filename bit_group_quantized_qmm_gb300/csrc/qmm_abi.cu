@@ -3,11 +3,13 @@
 // of every argument are in include/qmm.h.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <math.h>
 #include <string.h>
 
 #include <mutex>
 
 #include "qmm.h"
+#include "qmm_cq4.cuh"
 #include "qmm_internal.h"
 
 namespace qmm {
@@ -42,15 +44,19 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool desc_ok(const qmm_weight_desc* w)
 {
     if (!w || w->N < 1 || w->K < 1) return false;
-    if (w->variant == QMM_W4A8) return w->group == 64 || w->group == 128;
+    if (w->variant == QMM_W4A8 || w->variant == QMM_CQ4) return w->group == 64 || w->group == 128;
     if (w->variant == QMM_AFFINE) return w->group == 64;
     return false;
 }
 
+// Variants whose activations take the symmetric int8 prepass (W4A8 weights
+// and codebook weights).
+bool int8_act(int32_t variant) { return variant == QMM_W4A8 || variant == QMM_CQ4; }
+
 qmm_status shape_ok(const qmm_weight_desc* w)
 {
     if (!w) return QMM_ERR_INVALID_ARG;
-    if (w->variant != QMM_W4A8 && w->variant != QMM_AFFINE) return QMM_ERR_INVALID_ARG;
+    if (w->variant != QMM_W4A8 && w->variant != QMM_AFFINE && w->variant != QMM_CQ4) return QMM_ERR_INVALID_ARG;
     if (w->N < 1 || w->K < 1) return QMM_ERR_INVALID_ARG;
     if (!desc_ok(w)) return QMM_ERR_UNSUPPORTED_SHAPE;
     if (w->K % w->group != 0) return QMM_ERR_UNSUPPORTED_SHAPE;
@@ -168,7 +174,7 @@ size_t qmm_packed_size(const qmm_weight_desc* w)
     if (shape_ok(w) != QMM_OK) return 0;
     const size_t T = (size_t)(w->N + 127) / 128;
     const size_t CB = (size_t)64 * w->group + 256 + (w->variant == QMM_AFFINE ? 256 : 0);
-    return T * (size_t)(w->K / w->group) * CB;
+    return T * (size_t)(w->K / w->group) * CB + (w->variant == QMM_CQ4 ? (size_t)kCq4TrailerBytes : 0);
 }
 
 qmm_status qmm_pack_weights(const qmm_weight_desc* w, const uint8_t* q, const uint16_t* scales,
@@ -176,6 +182,7 @@ qmm_status qmm_pack_weights(const qmm_weight_desc* w, const uint8_t* q, const ui
 {
     qmm_status st = shape_ok(w);
     if (st != QMM_OK) return st;
+    if (w->variant == QMM_CQ4) return QMM_ERR_INVALID_ARG;   // needs its codebook: qmm_pack_weights_cq4
     if (!q || !scales || !packed) return QMM_ERR_INVALID_ARG;
     if ((w->variant == QMM_AFFINE) != (biases != nullptr)) return QMM_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(scales) || !aligned16(packed) || (biases && !aligned16(biases)))
@@ -183,6 +190,21 @@ qmm_status qmm_pack_weights(const qmm_weight_desc* w, const uint8_t* q, const ui
     LaunchCtx c;
     if ((st = device_ctx(stream, &c)) != QMM_OK) return st;
     return launched(launch_pack(c, w->variant, w->N, w->K, w->group, q, scales, biases, static_cast<uint8_t*>(packed)),
+                    QMM_KERNEL_PACK);
+}
+
+qmm_status qmm_pack_weights_cq4(const qmm_weight_desc* w, const uint8_t* idx, const int8_t* codebook,
+                                float cb_scale, const uint16_t* scales, void* packed, qmm_stream stream)
+{
+    qmm_status st = shape_ok(w);
+    if (st != QMM_OK) return st;
+    if (w->variant != QMM_CQ4) return QMM_ERR_INVALID_ARG;
+    if (!idx || !codebook || !scales || !packed || !isfinite(cb_scale)) return QMM_ERR_INVALID_ARG;
+    if (!aligned16(idx) || !aligned16(scales) || !aligned16(packed)) return QMM_ERR_MISALIGNED;
+    LaunchCtx c;
+    if ((st = device_ctx(stream, &c)) != QMM_OK) return st;
+    return launched(launch_pack_cq4(c, w->N, w->K, w->group, idx, codebook, cb_scale, scales,
+                                    static_cast<uint8_t*>(packed)),
                     QMM_KERNEL_PACK);
 }
 
@@ -195,7 +217,7 @@ qmm_status qmm_prep_act(int32_t variant, int32_t M, int32_t K, int32_t group, in
     if (!aligned16(x)) return QMM_ERR_MISALIGNED;
     qmm_status st;
     LaunchCtx c;
-    if (variant == QMM_W4A8) {
+    if (int8_act(variant)) {
         if (group != 64 && group != 128) return QMM_ERR_UNSUPPORTED_SHAPE;
         if (K % group) return QMM_ERR_UNSUPPORTED_SHAPE;
         if (hadamard != 0 && hadamard != group) return QMM_ERR_UNSUPPORTED_SHAPE;
@@ -218,7 +240,7 @@ qmm_status qmm_prep_act(int32_t variant, int32_t M, int32_t K, int32_t group, in
 
 size_t qmm_gemv_workspace_size(const qmm_weight_desc* w)
 {
-    if (shape_ok(w) != QMM_OK || w->variant != QMM_W4A8) return 0;
+    if (shape_ok(w) != QMM_OK || !int8_act(w->variant)) return 0;
     return gemv_workspace_bytes(w->N, w->K, w->group);
 }
 
@@ -227,7 +249,7 @@ qmm_status qmm_gemv(const qmm_weight_desc* w, const void* packed, const int8_t* 
 {
     qmm_status st = shape_ok(w);
     if (st != QMM_OK) return st;
-    if (w->variant != QMM_W4A8) return QMM_ERR_UNSUPPORTED_SHAPE;
+    if (!int8_act(w->variant)) return QMM_ERR_UNSUPPORTED_SHAPE;
     if (!packed || !a || !sx || !y) return QMM_ERR_INVALID_ARG;
     if (!aligned16(packed) || !aligned16(a) || !aligned16(sx) || !aligned16(y) ||
         (workspace && !aligned16(workspace)))
@@ -235,9 +257,10 @@ qmm_status qmm_gemv(const qmm_weight_desc* w, const void* packed, const int8_t* 
     if (workspace && workspace_bytes < gemv_workspace_bytes(w->N, w->K, w->group)) return QMM_ERR_WORKSPACE;
     LaunchCtx c;
     if ((st = device_ctx(stream, &c)) != QMM_OK) return st;
-    return launched(launch_gemv(c, w->N, w->K, w->group, static_cast<const uint8_t*>(packed), a, sx, y, nullptr,
-                                workspace, workspace_bytes),
-                    QMM_KERNEL_GEMV_W4A8);
+    const bool cq4 = w->variant == QMM_CQ4;
+    return launched(launch_gemv(c, cq4, w->N, w->K, w->group, static_cast<const uint8_t*>(packed), a, sx, y,
+                                nullptr, workspace, workspace_bytes),
+                    cq4 ? QMM_KERNEL_GEMV_CQ4 : QMM_KERNEL_GEMV_W4A8);
 }
 
 qmm_status qmm_gemv_fused(const qmm_weight_desc* w, const void* packed, const void* x, int32_t x_dtype,
@@ -245,7 +268,7 @@ qmm_status qmm_gemv_fused(const qmm_weight_desc* w, const void* packed, const vo
 {
     qmm_status st = shape_ok(w);
     if (st != QMM_OK) return st;
-    if (w->variant != QMM_W4A8) return QMM_ERR_UNSUPPORTED_SHAPE;
+    if (!int8_act(w->variant)) return QMM_ERR_UNSUPPORTED_SHAPE;
     if (hadamard != 0 && hadamard != w->group) return QMM_ERR_UNSUPPORTED_SHAPE;
     if (x_dtype != QMM_DTYPE_F32 && x_dtype != QMM_DTYPE_F16 && x_dtype != QMM_DTYPE_BF16) return QMM_ERR_INVALID_ARG;
     if (!packed || !x || !y) return QMM_ERR_INVALID_ARG;
@@ -256,7 +279,7 @@ qmm_status qmm_gemv_fused(const qmm_weight_desc* w, const void* packed, const vo
     if (w->K > max_k) return QMM_ERR_UNSUPPORTED_SHAPE;
     LaunchCtx c;
     if ((st = device_ctx(stream, &c)) != QMM_OK) return st;
-    return launched(launch_gemv_fused(c, w->N, w->K, w->group, hadamard, static_cast<const uint8_t*>(packed), x,
+    return launched(launch_gemv_fused(c, w->variant == QMM_CQ4, w->N, w->K, w->group, hadamard, static_cast<const uint8_t*>(packed), x,
                                       x_dtype, y, a_out, sx_out),
                     QMM_KERNEL_GEMV_FUSED);
 }
@@ -273,7 +296,8 @@ qmm_status qmm_gemv_fused_siblings(int32_t count, const qmm_weight_desc* w, cons
     for (int i = 0; i < count; ++i) {
         qmm_status st = shape_ok(&w[i]);
         if (st != QMM_OK) return st;
-        if (w[i].variant != QMM_W4A8 || w[i].K != w[0].K || w[i].group != w[0].group)
+        if (!int8_act(w[i].variant) || w[i].variant != w[0].variant || w[i].K != w[0].K ||
+            w[i].group != w[0].group)
             return QMM_ERR_UNSUPPORTED_SHAPE;
         if (!packed[i] || !y[i]) return QMM_ERR_INVALID_ARG;
         if (!aligned16(packed[i]) || !aligned16(y[i])) return QMM_ERR_MISALIGNED;
@@ -289,7 +313,7 @@ qmm_status qmm_gemv_fused_siblings(int32_t count, const qmm_weight_desc* w, cons
     LaunchCtx c;
     qmm_status st = device_ctx(stream, &c);
     if (st != QMM_OK) return st;
-    return launched(launch_gemv_fused_set(c, count, N, w[0].K, w[0].group, hadamard, blobs, x, x_dtype, ys, a_out,
+    return launched(launch_gemv_fused_set(c, w[0].variant == QMM_CQ4, count, N, w[0].K, w[0].group, hadamard, blobs, x, x_dtype, ys, a_out,
                                           sx_out),
                     QMM_KERNEL_GEMV_FUSED_SIBLINGS);
 }
@@ -307,8 +331,9 @@ static qmm_status gemm_common(const qmm_weight_desc* w, const void* packed, int3
     LaunchCtx c;
     if ((st = device_ctx(stream, &c)) != QMM_OK) return st;
     const uint8_t* blob = static_cast<const uint8_t*>(packed);
-    if (w->variant == QMM_W4A8 && !P && M <= g_rows_max) {
-        const cudaError_t e = launch_gemm_rows(c, w->group, M, w->N, w->K, blob,
+    const bool cq4 = w->variant == QMM_CQ4;
+    if (int8_act(w->variant) && !P && M <= g_rows_max) {
+        const cudaError_t e = launch_gemm_rows(c, cq4, w->group, M, w->N, w->K, blob,
                                                static_cast<const uint16_t*>(act16), act_scale, Y);
         if (e != cudaErrorNotSupported) return launched(e, QMM_KERNEL_GEMM_ROWS);
     }
@@ -318,6 +343,8 @@ static qmm_status gemm_common(const qmm_weight_desc* w, const void* packed, int3
     if (!act_tensor_map(&map, act16, M, w->K, sh.m_tile)) return QMM_ERR_CUDA;
     if (w->variant == QMM_W4A8)
         return launched(launch_gemm_w4a8(c, w->group, map, sh, blob, act_scale, Y, P, a_smem), QMM_KERNEL_GEMM_W4A8);
+    if (cq4)
+        return launched(launch_gemm_cq4(c, w->group, map, sh, blob, act_scale, Y, P, a_smem), QMM_KERNEL_GEMM_CQ4);
     if (P) return QMM_ERR_UNSUPPORTED_SHAPE;
     return launched(launch_gemm_affine(c, map, sh, blob, act_scale, Y, a_smem), QMM_KERNEL_GEMM_AFFINE);
 }
@@ -334,16 +361,17 @@ qmm_status qmm_debug_partials(const qmm_weight_desc* w, const void* packed, int3
 {
     qmm_status st = shape_ok(w);
     if (st != QMM_OK) return st;
-    if (w->variant != QMM_W4A8) return QMM_ERR_UNSUPPORTED_SHAPE;
+    if (!int8_act(w->variant)) return QMM_ERR_UNSUPPORTED_SHAPE;
     if (!packed || !act || !P || M < 1) return QMM_ERR_INVALID_ARG;
     if (path == QMM_PATH_GEMV) {
         if (M != 1) return QMM_ERR_INVALID_ARG;
         if (!aligned16(packed) || !aligned16(act) || !aligned16(P)) return QMM_ERR_MISALIGNED;
         LaunchCtx c;
         if ((st = device_ctx(stream, &c)) != QMM_OK) return st;
-        return launched(launch_gemv(c, w->N, w->K, w->group, static_cast<const uint8_t*>(packed),
+        const bool cq4 = w->variant == QMM_CQ4;
+        return launched(launch_gemv(c, cq4, w->N, w->K, w->group, static_cast<const uint8_t*>(packed),
                                     static_cast<const int8_t*>(act), nullptr, nullptr, P, nullptr, 0),
-                        QMM_KERNEL_GEMV_W4A8);
+                        cq4 ? QMM_KERNEL_GEMV_CQ4 : QMM_KERNEL_GEMV_W4A8);
     }
     if (path == QMM_PATH_GEMM) return gemm_common(w, packed, M, act, nullptr, nullptr, P, stream);
     return QMM_ERR_INVALID_ARG;

@@ -6,7 +6,8 @@
 // "native W*A8 int8 GEMM for prefill" (no fp32 intermediate, no dequantized
 // weights in DRAM); TensorFold PR #3215 "simd_qmm on Metal: X's group sums and
 // half operands from a prepass" (affine tiles on the prepass's group sums and
-// half X).
+// half X). Codebook (CQ4) weights: cactus PR #697, Summary (in-engine 4-bit
+// codebook expansion, cb_scale folded into one fp32 rescale).
 //
 // GB300 design. The tensor cores of sm_103a have no int8 MMA kind, so both
 // variants use tcgen05.mma kind::f16 with operands that carry the integers
@@ -51,11 +52,15 @@
 
 #include <cuda_fp16.h>
 
+#include "qmm_cq4.cuh"
 #include "qmm_internal.h"
 #include "qmm_ptx.cuh"
 
 namespace qmm {
 
+// VARIANT: 0 symmetric W4A8, 1 affine, 2 codebook (CQ4: the symmetric
+// variant's layout and rescale with looked-up levels, times cb_scale at the
+// store).
 constexpr int kGemmThreads = 512;
 // Register budgets after setmaxnreg: the expand and single-role warpgroups drop
 // to 80 per thread, the epilogue warpgroups rise to 176 (a whole group's 64
@@ -140,6 +145,27 @@ __device__ __forceinline__ void expand_word(uint32_t w, uint32_t* out)
     out[1] = *reinterpret_cast<uint32_t*>(&r1);
     out[2] = *reinterpret_cast<uint32_t*>(&r2);
     out[3] = *reinterpret_cast<uint32_t*>(&r3);
+}
+
+// fp16 pairs (k, k+1) of one packed word of codebook indices. The levels are
+// looked up as unsigned bytes u = c + 128 (the book is loaded with its bytes
+// XOR 0x80), placed under the fp16 exponent of 1024 (1024 + u is exact) and
+// offset by 1152: exact integers c in [-128, 127].
+__device__ __forceinline__ void expand_word_cq4(const Cq4Book& book, uint32_t w, uint32_t* out)
+{
+    uint32_t lo, hi;   // u of k = 0, 2, 4, 6 and of k = 1, 3, 5, 7
+    cq4_expand(book, w, lo, hi);
+    constexpr uint32_t kExp = 0x64646464u;
+    const uint32_t t0 = prmt(lo, hi, 0x5140u);   // u0 u1 u2 u3
+    const uint32_t t1 = prmt(lo, hi, 0x7362u);   // u4 u5 u6 u7
+    uint32_t f[4] = {prmt(t0, kExp, 0x4140u), prmt(t0, kExp, 0x4342u), prmt(t1, kExp, 0x4140u),
+                     prmt(t1, kExp, 0x4342u)};
+    const uint32_t off = 0x64806480u;   // fp16 1152, 1152
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __half2 r = __hsub2(*reinterpret_cast<__half2*>(&f[i]), *reinterpret_cast<const __half2*>(&off));
+        out[i] = *reinterpret_cast<uint32_t*>(&r);
+    }
 }
 
 // Running sums of two columns as one packed fp32 pair.
@@ -393,6 +419,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int wq = warp & 3;           // tensor-memory lane quadrant
         const int r = 32 * wq + lane;      // weight row within the tile == tensor-memory lane
         const int set = warp >> 2;         // with two sets, set s takes the groups g % 2 == s
+        Cq4Book book = {};
+        if (VARIANT == 2) book = cq4_load(blob + cq4_trailer_offset(sh.N, sh.K, GROUP), 0x80808080u);
         int rs = 0, ks = 0, turn = 0;
         uint32_t rph = 0, kph = 0;
         bool ok = true;
@@ -422,15 +450,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const uint4 p0 = *reinterpret_cast<const uint4*>(ch + (2 * j) * 2048 + r * 16);
                     const uint4 p1 = *reinterpret_cast<const uint4*>(ch + (2 * j + 1) * 2048 + r * 16);
                     uint32_t hv[32];
-                    constexpr int OFF = VARIANT == 0 ? 8 : 0;
-                    expand_word<OFF>(p0.x, hv + 0);
-                    expand_word<OFF>(p0.y, hv + 4);
-                    expand_word<OFF>(p0.z, hv + 8);
-                    expand_word<OFF>(p0.w, hv + 12);
-                    expand_word<OFF>(p1.x, hv + 16);
-                    expand_word<OFF>(p1.y, hv + 20);
-                    expand_word<OFF>(p1.z, hv + 24);
-                    expand_word<OFF>(p1.w, hv + 28);
+                    if (VARIANT == 2) {
+                        expand_word_cq4(book, p0.x, hv + 0);
+                        expand_word_cq4(book, p0.y, hv + 4);
+                        expand_word_cq4(book, p0.z, hv + 8);
+                        expand_word_cq4(book, p0.w, hv + 12);
+                        expand_word_cq4(book, p1.x, hv + 16);
+                        expand_word_cq4(book, p1.y, hv + 20);
+                        expand_word_cq4(book, p1.z, hv + 24);
+                        expand_word_cq4(book, p1.w, hv + 28);
+                    } else {
+                        constexpr int OFF = VARIANT == 0 ? 8 : 0;
+                        expand_word<OFF>(p0.x, hv + 0);
+                        expand_word<OFF>(p0.y, hv + 4);
+                        expand_word<OFF>(p0.z, hv + 8);
+                        expand_word<OFF>(p0.w, hv + 12);
+                        expand_word<OFF>(p1.x, hv + 16);
+                        expand_word<OFF>(p1.y, hv + 20);
+                        expand_word<OFF>(p1.z, hv + 24);
+                        expand_word<OFF>(p1.w, hv + 28);
+                    }
                     if (j == KSG - 1) {
                         // the chunk's words are all in registers (the decode used them)
                         __syncwarp();
@@ -467,6 +506,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         int db = 0, xs = 0;
         uint32_t dph = 0, xph = 0;
         bool ok = true;
+        const float out_scale =
+            VARIANT == 2 ? *reinterpret_cast<const float*>(blob + cq4_trailer_offset(sh.N, sh.K, GROUP) + 16) : 1.f;
         pdl_wait();   // outputs may still be read by the previous kernel
         for (int tile = blockIdx.x; ok && tile < sh.num_tiles; tile += gridDim.x) {
             const int nt = tile / sh.mt_count, mt = tile - nt * sh.mt_count;
@@ -513,7 +554,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         } else {
                             const float4 s4 = *reinterpret_cast<const float4*>(sxv + cb + e4);
                             const int c = (cb + e4) / 2;
-                            if (VARIANT == 0) {
+                            if (VARIANT != 1) {
                                 acc_w4a8(acc[c], v[e4], v[e4 + 1], s4.x, s4.y, w2);
                                 acc_w4a8(acc[c + 1], v[e4 + 2], v[e4 + 3], s4.z, s4.w, w2);
                             } else {
@@ -536,7 +577,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 for (int c = 0; c < MAXC; ++c) {
                     const int m = m0 + c;
                     const uint32_t bits = (uint32_t)(c & 1 ? acc[c / 2] >> 32 : acc[c / 2]);
-                    if (c < ncol && m < sh.M) Y[(size_t)m * sh.N + n] = __uint_as_float(bits);
+                    if (c < ncol && m < sh.M)
+                        Y[(size_t)m * sh.N + n] = VARIANT == 2 ? __uint_as_float(bits) * out_scale : __uint_as_float(bits);
                 }
             }
         }

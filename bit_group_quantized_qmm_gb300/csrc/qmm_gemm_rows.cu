@@ -22,10 +22,13 @@
 // expands each 16-byte nibble piece once and runs it against every row's
 // codes. The halves meet in shared memory, the slices in the cluster's first
 // CTA through distributed shared memory, in a fixed order: deterministic, no
-// workspace, no atomics.
+// workspace, no atomics. Codebook (CQ4) blobs take the same loop with each
+// piece's indices looked up in the matrix's 16 int8 levels, the codes staged
+// in the lookup's order and cb_scale applied once per output.
 #include <cuda_fp16.h>
 
 #include "qmm.h"
+#include "qmm_cq4.cuh"
 #include "qmm_internal.h"
 #include "qmm_ptx.cuh"
 
@@ -76,7 +79,7 @@ __device__ __forceinline__ uint32_t code_byte(uint16_t h)
 
 // Grid (T, ksplit), cluster (1, ksplit): CTA (t, s) handles groups [g0, g1) of
 // tile t for all M (<= MR) rows.
-template <int GROUP, int MR>
+template <int GROUP, int MR, bool CQ>
 __global__ void __launch_bounds__(kThreads)
     gemm_rows_kernel(int M, int N, int K, int ksplit, int ng_max, const uint8_t* __restrict__ blob,
                      const uint16_t* __restrict__ act16, const float* __restrict__ sx, float* __restrict__ Y,
@@ -133,6 +136,8 @@ __global__ void __launch_bounds__(kThreads)
     }
 
     // ---------------------------------------------------------- stage codes
+    Cq4Book book = {};
+    if (CQ) book = cq4_load(blob + cq4_trailer_offset(N, K, GROUP));
     // warm the slice's codes in L2 first (a prefetch returns no data, so it
     // may run before the dependency wait)
     if (tid < M)
@@ -151,8 +156,12 @@ __global__ void __launch_bounds__(kThreads)
                 const uint32_t b2 = code_byte((uint16_t)hv.y), b3 = code_byte((uint16_t)(hv.y >> 16));
                 const uint32_t b4 = code_byte((uint16_t)hv.z), b5 = code_byte((uint16_t)(hv.z >> 16));
                 const uint32_t b6 = code_byte((uint16_t)hv.w), b7 = code_byte((uint16_t)(hv.w >> 16));
-                // dp4a order of an 8-block: k = 0, 4, 1, 5 | 2, 6, 3, 7
-                perm = make_uint2(b0 | (b4 << 8) | (b1 << 16) | (b5 << 24), b2 | (b6 << 8) | (b3 << 16) | (b7 << 24));
+                if (CQ)   // lookup order of an 8-block: k = 0, 2, 4, 6 | 1, 3, 5, 7
+                    perm = make_uint2(b0 | (b2 << 8) | (b4 << 16) | (b6 << 24),
+                                      b1 | (b3 << 8) | (b5 << 16) | (b7 << 24));
+                else      // dp4a order of an 8-block: k = 0, 4, 1, 5 | 2, 6, 3, 7
+                    perm = make_uint2(b0 | (b4 << 8) | (b1 << 16) | (b5 << 24),
+                                      b2 | (b6 << 8) | (b3 << 16) | (b7 << 24));
             }
             *reinterpret_cast<uint2*>(aperm + ((size_t)i * MR + m) * GROUP + (size_t)c8 * 8) = perm;
         }
@@ -171,18 +180,36 @@ __global__ void __launch_bounds__(kThreads)
     for (int i = h; i < ng; i += 2) {
         if (!mbar_wait(&full[i], 0, status, abort)) break;
         const uint8_t* c = stages + (size_t)i * C::CB;
-        int wv[8 * C::PP];   // 16 * q bytes of the row's GROUP weights, in the blob's slot order
+        // the row's GROUP weights as bytes: 16 * q in the blob's slot order
+        // (symmetric) or the looked-up levels (codebook)
+        int wv[8 * C::PP];
 #pragma unroll
         for (int p = 0; p < C::PP; ++p) {
             const uint4 w = *reinterpret_cast<const uint4*>(c + p * 2048 + r * 16);
-            wv[8 * p + 0] = nib_lo16(w.x);
-            wv[8 * p + 1] = nib_hi16(w.x);
-            wv[8 * p + 2] = nib_lo16(w.y);
-            wv[8 * p + 3] = nib_hi16(w.y);
-            wv[8 * p + 4] = nib_lo16(w.z);
-            wv[8 * p + 5] = nib_hi16(w.z);
-            wv[8 * p + 6] = nib_lo16(w.w);
-            wv[8 * p + 7] = nib_hi16(w.w);
+            if (CQ) {
+                uint32_t lo, hi;
+                cq4_expand(book, w.x, lo, hi);
+                wv[8 * p + 0] = (int)lo;
+                wv[8 * p + 1] = (int)hi;
+                cq4_expand(book, w.y, lo, hi);
+                wv[8 * p + 2] = (int)lo;
+                wv[8 * p + 3] = (int)hi;
+                cq4_expand(book, w.z, lo, hi);
+                wv[8 * p + 4] = (int)lo;
+                wv[8 * p + 5] = (int)hi;
+                cq4_expand(book, w.w, lo, hi);
+                wv[8 * p + 6] = (int)lo;
+                wv[8 * p + 7] = (int)hi;
+            } else {
+                wv[8 * p + 0] = nib_lo16(w.x);
+                wv[8 * p + 1] = nib_hi16(w.x);
+                wv[8 * p + 2] = nib_lo16(w.y);
+                wv[8 * p + 3] = nib_hi16(w.y);
+                wv[8 * p + 4] = nib_lo16(w.z);
+                wv[8 * p + 5] = nib_hi16(w.z);
+                wv[8 * p + 6] = nib_lo16(w.w);
+                wv[8 * p + 7] = nib_hi16(w.w);
+            }
         }
         const float sw = __half2float(reinterpret_cast<const __half*>(c + 64 * GROUP)[r]);
         // one dp4a chain per row, interleaved piece by piece
@@ -206,7 +233,7 @@ __global__ void __launch_bounds__(kThreads)
             }
         }
 #pragma unroll
-        for (int m = 0; m < MR; ++m) acc[m] = fmaf((float)(dp[m] >> 4), sw * sxs[i * MR + m], acc[m]);
+        for (int m = 0; m < MR; ++m) acc[m] = fmaf((float)(CQ ? dp[m] : dp[m] >> 4), sw * sxs[i * MR + m], acc[m]);
     }
 
     // ---------------------------------------------------------- reduce, store
@@ -221,7 +248,7 @@ __global__ void __launch_bounds__(kThreads)
         for (int m = 0; m < MR; ++m) {
             const float v = acc[m] + red[m * 128 + r];
             if (ksplit == 1) {
-                if (m < M && n < N) Y[(size_t)m * N + n] = v;
+                if (m < M && n < N) Y[(size_t)m * N + n] = CQ ? v * book.scale : v;
             } else {
                 parts[((size_t)s * MR + m) * 128 + r] = v;   // this slice's sums, locally first
             }
@@ -243,18 +270,18 @@ __global__ void __launch_bounds__(kThreads)
             for (int m = 0; m < MR; ++m) {
                 float v = 0.f;
                 for (int k = 0; k < ksplit; ++k) v += parts[((size_t)k * MR + m) * 128 + tid];
-                if (m < M && t * 128 + tid < N) Y[(size_t)m * N + t * 128 + tid] = v;
+                if (m < M && t * 128 + tid < N) Y[(size_t)m * N + t * 128 + tid] = CQ ? v * book.scale : v;
             }
         }
     }
 }
 
-template <int GROUP, int MR>
+template <int GROUP, int MR, bool CQ>
 cudaError_t run(const LaunchCtx& c, int M, int N, int K, const uint8_t* blob, const uint16_t* act16,
                 const float* sx, float* Y)
 {
     using C = Cfg<GROUP, MR>;
-    auto kern = gemm_rows_kernel<GROUP, MR>;
+    auto kern = gemm_rows_kernel<GROUP, MR, CQ>;
     const int T = (N + 127) / 128, G = K / GROUP;
     int ks = (kTargetCtas + T - 1) / T;
     const int ks_ng = (G + C::NG_CAP - 1) / C::NG_CAP;
@@ -294,24 +321,28 @@ cudaError_t run(const LaunchCtx& c, int M, int N, int K, const uint8_t* blob, co
     return cudaLaunchKernelEx(&cfg, kern, M, N, K, ks, ng_max, blob, act16, sx, Y, c.status);
 }
 
-template <int GROUP>
+template <int GROUP, bool CQ>
 cudaError_t dispatch(const LaunchCtx& c, int M, int N, int K, const uint8_t* blob, const uint16_t* act16,
                      const float* sx, float* Y)
 {
-    if (M <= 2) return run<GROUP, 2>(c, M, N, K, blob, act16, sx, Y);
-    if (M <= 4) return run<GROUP, 4>(c, M, N, K, blob, act16, sx, Y);
-    if (M <= 8) return run<GROUP, 8>(c, M, N, K, blob, act16, sx, Y);
-    if (M <= 16) return run<GROUP, 16>(c, M, N, K, blob, act16, sx, Y);
+    if (M <= 2) return run<GROUP, 2, CQ>(c, M, N, K, blob, act16, sx, Y);
+    if (M <= 4) return run<GROUP, 4, CQ>(c, M, N, K, blob, act16, sx, Y);
+    if (M <= 8) return run<GROUP, 8, CQ>(c, M, N, K, blob, act16, sx, Y);
+    if (M <= 16) return run<GROUP, 16, CQ>(c, M, N, K, blob, act16, sx, Y);
     return cudaErrorNotSupported;
 }
 
 }  // namespace
 
-cudaError_t launch_gemm_rows(const LaunchCtx& c, int group, int M, int N, int K, const uint8_t* blob,
+cudaError_t launch_gemm_rows(const LaunchCtx& c, bool cq4, int group, int M, int N, int K, const uint8_t* blob,
                              const uint16_t* act16, const float* sx, float* Y)
 {
-    if (group == 64) return dispatch<64>(c, M, N, K, blob, act16, sx, Y);
-    if (group == 128) return dispatch<128>(c, M, N, K, blob, act16, sx, Y);
+    if (group == 64)
+        return cq4 ? dispatch<64, true>(c, M, N, K, blob, act16, sx, Y)
+                   : dispatch<64, false>(c, M, N, K, blob, act16, sx, Y);
+    if (group == 128)
+        return cq4 ? dispatch<128, true>(c, M, N, K, blob, act16, sx, Y)
+                   : dispatch<128, false>(c, M, N, K, blob, act16, sx, Y);
     return cudaErrorInvalidValue;
 }
 

@@ -18,8 +18,11 @@
 // dp4a against activations staged once per CTA in the order the expansion
 // consumes them. Each group partial is rescaled once in fp32. Split-K slices
 // are combined by the last CTA of a tile in a fixed order (deterministic).
+// Codebook (CQ4) blobs take the same loop with the nibbles looked up in the
+// matrix's 16 int8 levels instead (cb_scale folded into the staged sx).
 #include <cuda_fp16.h>
 
+#include "qmm_cq4.cuh"
 #include "qmm_internal.h"
 #include "qmm_ptx.cuh"
 
@@ -50,7 +53,7 @@ static size_t gemv_smem_bytes(int ring, int cb, int ng, int group)
 __device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 // Grid (T, ksplit); CTA (t, s) handles groups [g0, g1) of row tile t.
-template <int GROUP, bool DEBUG>
+template <int GROUP, bool DEBUG, bool CQ>
 __global__ void __launch_bounds__(kGemvThreads)
     gemv_kernel(int N, int K, int ksplit, const uint8_t* __restrict__ blob, const int8_t* __restrict__ a,
                 const float* __restrict__ sx, float* __restrict__ y, int32_t* __restrict__ P,
@@ -107,16 +110,23 @@ __global__ void __launch_bounds__(kGemvThreads)
     }
 
     // compute warps: stage activations (permuted for the dp4a pairing) and scales
+    Cq4Book book = {};
+    if (CQ) book = cq4_load(blob + cq4_trailer_offset(N, K, GROUP));
     pdl_wait();
     {
         const uint2* src = reinterpret_cast<const uint2*>(a + (size_t)g0 * GROUP);
         for (int i = tid; i < ng * GROUP / 8; i += kGemvComputeThreads) {
             const uint2 w = src[i];
-            aperm[2 * i] = __byte_perm(w.x, w.y, 0x5140);       // k = 0, 4, 1, 5
-            aperm[2 * i + 1] = __byte_perm(w.x, w.y, 0x7362);   // k = 2, 6, 3, 7
+            if (CQ) {
+                aperm[2 * i] = __byte_perm(w.x, w.y, 0x6420);       // k = 0, 2, 4, 6
+                aperm[2 * i + 1] = __byte_perm(w.x, w.y, 0x7531);   // k = 1, 3, 5, 7
+            } else {
+                aperm[2 * i] = __byte_perm(w.x, w.y, 0x5140);       // k = 0, 4, 1, 5
+                aperm[2 * i + 1] = __byte_perm(w.x, w.y, 0x7362);   // k = 2, 6, 3, 7
+            }
         }
         if (!DEBUG)   // the partials hook passes no scales
-            for (int i = tid; i < ng; i += kGemvComputeThreads) sxs[i] = sx[g0 + i];
+            for (int i = tid; i < ng; i += kGemvComputeThreads) sxs[i] = CQ ? sx[g0 + i] * book.scale : sx[g0 + i];
     }
     compute_sync();
 
@@ -133,16 +143,32 @@ __global__ void __launch_bounds__(kGemvThreads)
             const uint4 w = *reinterpret_cast<const uint4*>(c + p * 2048 + r * 16);
             const uint4* ap = reinterpret_cast<const uint4*>(aperm + (i * GROUP + 32 * p) / 4);
             const uint4 a0 = ap[0], a1 = ap[1];
-            dp = __dp4a(nib_lo16(w.x), (int)a0.x, dp);
-            dp = __dp4a(nib_hi16(w.x), (int)a0.y, dp);
-            dp = __dp4a(nib_lo16(w.y), (int)a0.z, dp);
-            dp = __dp4a(nib_hi16(w.y), (int)a0.w, dp);
-            dp = __dp4a(nib_lo16(w.z), (int)a1.x, dp);
-            dp = __dp4a(nib_hi16(w.z), (int)a1.y, dp);
-            dp = __dp4a(nib_lo16(w.w), (int)a1.z, dp);
-            dp = __dp4a(nib_hi16(w.w), (int)a1.w, dp);
+            if (CQ) {
+                uint32_t lo, hi;
+                cq4_expand(book, w.x, lo, hi);
+                dp = __dp4a((int)lo, (int)a0.x, dp);
+                dp = __dp4a((int)hi, (int)a0.y, dp);
+                cq4_expand(book, w.y, lo, hi);
+                dp = __dp4a((int)lo, (int)a0.z, dp);
+                dp = __dp4a((int)hi, (int)a0.w, dp);
+                cq4_expand(book, w.z, lo, hi);
+                dp = __dp4a((int)lo, (int)a1.x, dp);
+                dp = __dp4a((int)hi, (int)a1.y, dp);
+                cq4_expand(book, w.w, lo, hi);
+                dp = __dp4a((int)lo, (int)a1.z, dp);
+                dp = __dp4a((int)hi, (int)a1.w, dp);
+            } else {
+                dp = __dp4a(nib_lo16(w.x), (int)a0.x, dp);
+                dp = __dp4a(nib_hi16(w.x), (int)a0.y, dp);
+                dp = __dp4a(nib_lo16(w.y), (int)a0.z, dp);
+                dp = __dp4a(nib_hi16(w.y), (int)a0.w, dp);
+                dp = __dp4a(nib_lo16(w.z), (int)a1.x, dp);
+                dp = __dp4a(nib_hi16(w.z), (int)a1.y, dp);
+                dp = __dp4a(nib_lo16(w.w), (int)a1.z, dp);
+                dp = __dp4a(nib_hi16(w.w), (int)a1.w, dp);
+            }
         }
-        const int Pg = dp >> 4;   // exact: every product carried a factor 16
+        const int Pg = CQ ? dp : dp >> 4;   // symmetric: exact, every product carried a factor 16
         if (DEBUG) {
             if (n < N) P[(size_t)n * G + g0 + i] = Pg;
         } else {
@@ -202,7 +228,7 @@ size_t gemv_workspace_bytes(int N, int K, int group)
     return (size_t)ks * T * 128 * sizeof(float) + T * sizeof(unsigned);
 }
 
-template <int GROUP, bool DEBUG>
+template <int GROUP, bool DEBUG, bool CQ>
 static cudaError_t launch_gemv_t(const LaunchCtx& c, int N, int K, int ksplit, const uint8_t* blob, const int8_t* a,
                                  const float* sx, float* y, int32_t* P, float* ws_part, unsigned* ws_count)
 {
@@ -211,7 +237,7 @@ static cudaError_t launch_gemv_t(const LaunchCtx& c, int N, int K, int ksplit, c
     const int ng_max = (G + ksplit - 1) / ksplit;
     const int ring = ng_max < C::RING ? ng_max : C::RING;
     const size_t smem = gemv_smem_bytes(ring, C::CB, ng_max, GROUP);
-    auto kern = gemv_kernel<GROUP, DEBUG>;
+    auto kern = gemv_kernel<GROUP, DEBUG, CQ>;
     static size_t configured = 0;
     if (smem > configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -222,7 +248,15 @@ static cudaError_t launch_gemv_t(const LaunchCtx& c, int N, int K, int ksplit, c
                   ws_count, c.status);
 }
 
-cudaError_t launch_gemv(const LaunchCtx& c, int N, int K, int group, const uint8_t* blob, const int8_t* a,
+template <int GROUP, bool CQ>
+static cudaError_t launch_gemv_g(const LaunchCtx& c, int N, int K, int ks, const uint8_t* blob, const int8_t* a,
+                                 const float* sx, float* y, int32_t* P_debug, float* part, unsigned* count)
+{
+    if (P_debug) return launch_gemv_t<GROUP, true, CQ>(c, N, K, 1, blob, a, sx, y, P_debug, nullptr, nullptr);
+    return launch_gemv_t<GROUP, false, CQ>(c, N, K, ks, blob, a, sx, y, nullptr, part, count);
+}
+
+cudaError_t launch_gemv(const LaunchCtx& c, bool cq4, int N, int K, int group, const uint8_t* blob, const int8_t* a,
                         const float* sx, float* y, int32_t* P_debug, void* ws, size_t ws_bytes)
 {
     int ks = 1;
@@ -237,14 +271,12 @@ cudaError_t launch_gemv(const LaunchCtx& c, int N, int K, int group, const uint8
             count = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + (size_t)ks * T * 128 * sizeof(float));
         }
     }
-    if (group == 64) {
-        if (P_debug) return launch_gemv_t<64, true>(c, N, K, 1, blob, a, sx, y, P_debug, nullptr, nullptr);
-        return launch_gemv_t<64, false>(c, N, K, ks, blob, a, sx, y, nullptr, part, count);
-    }
-    if (group == 128) {
-        if (P_debug) return launch_gemv_t<128, true>(c, N, K, 1, blob, a, sx, y, P_debug, nullptr, nullptr);
-        return launch_gemv_t<128, false>(c, N, K, ks, blob, a, sx, y, nullptr, part, count);
-    }
+    if (group == 64)
+        return cq4 ? launch_gemv_g<64, true>(c, N, K, ks, blob, a, sx, y, P_debug, part, count)
+                   : launch_gemv_g<64, false>(c, N, K, ks, blob, a, sx, y, P_debug, part, count);
+    if (group == 128)
+        return cq4 ? launch_gemv_g<128, true>(c, N, K, ks, blob, a, sx, y, P_debug, part, count)
+                   : launch_gemv_g<128, false>(c, N, K, ks, blob, a, sx, y, P_debug, part, count);
     return cudaErrorInvalidValue;
 }
 

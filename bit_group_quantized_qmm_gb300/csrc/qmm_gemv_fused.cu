@@ -19,10 +19,15 @@
 // K-slices of a tile form one thread-block cluster and are summed through
 // distributed shared memory in a fixed order by the cluster's first CTA: no
 // global workspace, no atomics, deterministic results.
+//
+// Codebook (CQ4) blobs run the same kernel: phase A writes the codes in the
+// order the table lookup consumes them, phase B looks the nibbles up in the
+// matrix's 16 int8 levels, and the sum is multiplied by cb_scale once.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "qmm.h"
+#include "qmm_cq4.cuh"
 #include "qmm_internal.h"
 #include "qmm_ptx.cuh"
 
@@ -76,7 +81,7 @@ size_t smem_bytes(int ring, int cb, int ng, int group)
 // handles groups [g0, g1) of tile t of the matrix that owns grid row b.
 // EPL inputs per lane in phase A: 8 for long slices; GROUP/32 (a whole warp per
 // group, fewer serial divisions per lane) for short ones.
-template <int GROUP, int XDT, int EPL>
+template <int GROUP, int XDT, int EPL, bool CQ>
 __global__ void __launch_bounds__(kThreads)
     gemv_fused_kernel(const __grid_constant__ FusedSet set, int K, int ksplit, int hadamard, float rot_scale,
                       const void* __restrict__ x, int8_t* __restrict__ a_out, float* __restrict__ sx_out, int* status)
@@ -141,6 +146,8 @@ __global__ void __launch_bounds__(kThreads)
         }
         __syncwarp();
     } else {
+        Cq4Book book = {};
+        if (CQ) book = cq4_load(blob + cq4_trailer_offset(N, K, GROUP));
         // ---------------------------------------------------------- phase A
         // LPG lanes per group, EPL consecutive inputs per lane; GPW groups per
         // warp. Transform stages below EPL run inside the lane, the others
@@ -218,17 +225,21 @@ __global__ void __launch_bounds__(kThreads)
             }
             if (valid) {
                 uint8_t* blk = aperm + (size_t)i * GROUP + (size_t)(cl * EPL / 8) * 8;
-                if (EPL == 8) {
+                if (EPL == 8 && CQ) {
+                    // lookup order of an 8-block: k = 0, 2, 4, 6 | 1, 3, 5, 7
+                    *reinterpret_cast<uint2*>(blk) = make_uint2(b[0] | (b[2] << 8) | (b[4] << 16) | (b[6] << 24),
+                                                                b[1] | (b[3] << 8) | (b[5] << 16) | (b[7] << 24));
+                } else if (EPL == 8) {
                     // dp4a order of an 8-block: k = 0, 4, 1, 5 | 2, 6, 3, 7
                     *reinterpret_cast<uint2*>(blk) = make_uint2(b[0] | (b[4] << 8) | (b[1] << 16) | (b[5] << 24),
                                                                 b[2] | (b[6] << 8) | (b[3] << 16) | (b[7] << 24));
                 } else {
                     // this lane's EPL inputs k = k0 .. k0+EPL-1 of an 8-block, at
-                    // their positions in the dp4a order
+                    // their positions in the dp4a (or lookup) order
 #pragma unroll
                     for (int e = 0; e < EPL; ++e) {
                         const int k = (cl * EPL + e) & 7;
-                        blk[2 * (k & 3) + (k >> 2)] = (uint8_t)b[e];
+                        blk[CQ ? 4 * (k & 1) + (k >> 1) : 2 * (k & 3) + (k >> 2)] = (uint8_t)b[e];
                     }
                 }
                 if (a_out) {
@@ -259,16 +270,32 @@ __global__ void __launch_bounds__(kThreads)
                 const uint4 w = *reinterpret_cast<const uint4*>(c + p * 2048 + r * 16);
                 const uint4* ap = reinterpret_cast<const uint4*>(aperm + (size_t)i * GROUP + 32 * p);
                 const uint4 a0 = ap[0], a1 = ap[1];
-                dp = __dp4a(nib_lo16(w.x), (int)a0.x, dp);
-                dp = __dp4a(nib_hi16(w.x), (int)a0.y, dp);
-                dp = __dp4a(nib_lo16(w.y), (int)a0.z, dp);
-                dp = __dp4a(nib_hi16(w.y), (int)a0.w, dp);
-                dp = __dp4a(nib_lo16(w.z), (int)a1.x, dp);
-                dp = __dp4a(nib_hi16(w.z), (int)a1.y, dp);
-                dp = __dp4a(nib_lo16(w.w), (int)a1.z, dp);
-                dp = __dp4a(nib_hi16(w.w), (int)a1.w, dp);
+                if (CQ) {
+                    uint32_t lo, hi;
+                    cq4_expand(book, w.x, lo, hi);
+                    dp = __dp4a((int)lo, (int)a0.x, dp);
+                    dp = __dp4a((int)hi, (int)a0.y, dp);
+                    cq4_expand(book, w.y, lo, hi);
+                    dp = __dp4a((int)lo, (int)a0.z, dp);
+                    dp = __dp4a((int)hi, (int)a0.w, dp);
+                    cq4_expand(book, w.z, lo, hi);
+                    dp = __dp4a((int)lo, (int)a1.x, dp);
+                    dp = __dp4a((int)hi, (int)a1.y, dp);
+                    cq4_expand(book, w.w, lo, hi);
+                    dp = __dp4a((int)lo, (int)a1.z, dp);
+                    dp = __dp4a((int)hi, (int)a1.w, dp);
+                } else {
+                    dp = __dp4a(nib_lo16(w.x), (int)a0.x, dp);
+                    dp = __dp4a(nib_hi16(w.x), (int)a0.y, dp);
+                    dp = __dp4a(nib_lo16(w.y), (int)a0.z, dp);
+                    dp = __dp4a(nib_hi16(w.y), (int)a0.w, dp);
+                    dp = __dp4a(nib_lo16(w.z), (int)a1.x, dp);
+                    dp = __dp4a(nib_hi16(w.z), (int)a1.y, dp);
+                    dp = __dp4a(nib_lo16(w.w), (int)a1.z, dp);
+                    dp = __dp4a(nib_hi16(w.w), (int)a1.w, dp);
+                }
             }
-            return dp;
+            return CQ ? dp : dp >> 4;   // symmetric: every product carried a factor 16
         };
         // two groups per step (independent dp4a chains), added in group order
         for (int i = h; i < ng; i += 4) {
@@ -278,11 +305,11 @@ __global__ void __launch_bounds__(kThreads)
             const int dp0 = partial(i);
             const int dp1 = two ? partial(i + 2) : 0;
             const float sw0 = __half2float(reinterpret_cast<const __half*>(stages + (size_t)i * C::CB + 64 * GROUP)[r]);
-            acc = fmaf((float)(dp0 >> 4), sw0 * sxs[i], acc);
+            acc = fmaf((float)dp0, sw0 * sxs[i], acc);
             if (two) {
                 const float sw1 =
                     __half2float(reinterpret_cast<const __half*>(stages + (size_t)(i + 2) * C::CB + 64 * GROUP)[r]);
-                acc = fmaf((float)(dp1 >> 4), sw1 * sxs[i + 2], acc);
+                acc = fmaf((float)dp1, sw1 * sxs[i + 2], acc);
             }
         }
         if (h == 1) red[r] = acc;
@@ -290,7 +317,7 @@ __global__ void __launch_bounds__(kThreads)
         if (h == 0) {
             const float v = acc + red[r];
             if (ksplit == 1) {
-                if (t * 128 + r < N) y[t * 128 + r] = v;
+                if (t * 128 + r < N) y[t * 128 + r] = CQ ? v * book.scale : v;
             } else {
                 parts[s * 128 + r] = v;   // this slice's sums, locally first
             }
@@ -310,7 +337,7 @@ __global__ void __launch_bounds__(kThreads)
                 mbar_wait_cluster(sums_in, 0, status);
                 float v = 0.f;
                 for (int k = 0; k < ksplit; ++k) v += parts[k * 128 + tid];
-                if (t * 128 + tid < N) y[t * 128 + tid] = v;
+                if (t * 128 + tid < N) y[t * 128 + tid] = CQ ? v * book.scale : v;
             }
         }
     }
@@ -331,12 +358,12 @@ int fused_ksplit(int T, int K, int group)
     return ks;
 }
 
-template <int GROUP, int XDT, int EPL>
+template <int GROUP, int XDT, int EPL, bool CQ>
 cudaError_t run(const LaunchCtx& c, const FusedSet& set, int K, int hadamard, const void* x, int8_t* a_out,
                 float* sx_out)
 {
     using C = Cfg<GROUP>;
-    auto kern = gemv_fused_kernel<GROUP, XDT, EPL>;
+    auto kern = gemv_fused_kernel<GROUP, XDT, EPL, CQ>;
     const int G = K / GROUP, T = set.tile0[set.count];
     const int ks = fused_ksplit(T, K, GROUP);
     const int ng_max = (G + ks - 1) / ks;
@@ -374,18 +401,34 @@ cudaError_t run(const LaunchCtx& c, const FusedSet& set, int K, int hadamard, co
     return cudaLaunchKernelEx(&cfg, kern, set, K, ks, hadamard, rot, x, a_out, sx_out, c.status);
 }
 
-template <int GROUP, int EPL>
+template <int GROUP, int EPL, bool CQ>
 cudaError_t run_dtype(const LaunchCtx& c, const FusedSet& set, int K, int hadamard, const void* x, int x_dtype,
                       int8_t* a_out, float* sx_out)
 {
-    if (x_dtype == 0) return run<GROUP, 0, EPL>(c, set, K, hadamard, x, a_out, sx_out);
-    if (x_dtype == 1) return run<GROUP, 1, EPL>(c, set, K, hadamard, x, a_out, sx_out);
-    return run<GROUP, 2, EPL>(c, set, K, hadamard, x, a_out, sx_out);
+    if (x_dtype == 0) return run<GROUP, 0, EPL, CQ>(c, set, K, hadamard, x, a_out, sx_out);
+    if (x_dtype == 1) return run<GROUP, 1, EPL, CQ>(c, set, K, hadamard, x, a_out, sx_out);
+    return run<GROUP, 2, EPL, CQ>(c, set, K, hadamard, x, a_out, sx_out);
+}
+
+template <bool CQ>
+cudaError_t run_group(const LaunchCtx& c, const FusedSet& set, int K, int group, int hadamard, const void* x,
+                      int x_dtype, int8_t* a_out, float* sx_out)
+{
+    // short slices (at most 16 groups per CTA) quantize with a warp per group
+    const int ks = fused_ksplit(set.tile0[set.count], K, group);
+    const bool short_slice = (K / group + ks - 1) / ks <= 16;
+    if (group == 64)
+        return short_slice ? run_dtype<64, 2, CQ>(c, set, K, hadamard, x, x_dtype, a_out, sx_out)
+                           : run_dtype<64, 8, CQ>(c, set, K, hadamard, x, x_dtype, a_out, sx_out);
+    if (group == 128)
+        return short_slice ? run_dtype<128, 4, CQ>(c, set, K, hadamard, x, x_dtype, a_out, sx_out)
+                           : run_dtype<128, 8, CQ>(c, set, K, hadamard, x, x_dtype, a_out, sx_out);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-cudaError_t launch_gemv_fused_set(const LaunchCtx& c, int count, const int* N, int K, int group, int hadamard,
+cudaError_t launch_gemv_fused_set(const LaunchCtx& c, bool cq4, int count, const int* N, int K, int group, int hadamard,
                                   const uint8_t* const* blob, const void* x, int x_dtype, float* const* y,
                                   int8_t* a_out, float* sx_out)
 {
@@ -399,22 +442,14 @@ cudaError_t launch_gemv_fused_set(const LaunchCtx& c, int count, const int* N, i
         set.y[i] = y[i];
         set.tile0[i + 1] = set.tile0[i] + (N[i] + 127) / 128;
     }
-    // short slices (at most 16 groups per CTA) quantize with a warp per group
-    const int ks = fused_ksplit(set.tile0[count], K, group);
-    const bool short_slice = (K / group + ks - 1) / ks <= 16;
-    if (group == 64)
-        return short_slice ? run_dtype<64, 2>(c, set, K, hadamard, x, x_dtype, a_out, sx_out)
-                           : run_dtype<64, 8>(c, set, K, hadamard, x, x_dtype, a_out, sx_out);
-    if (group == 128)
-        return short_slice ? run_dtype<128, 4>(c, set, K, hadamard, x, x_dtype, a_out, sx_out)
-                           : run_dtype<128, 8>(c, set, K, hadamard, x, x_dtype, a_out, sx_out);
-    return cudaErrorInvalidValue;
+    return cq4 ? run_group<true>(c, set, K, group, hadamard, x, x_dtype, a_out, sx_out)
+               : run_group<false>(c, set, K, group, hadamard, x, x_dtype, a_out, sx_out);
 }
 
-cudaError_t launch_gemv_fused(const LaunchCtx& c, int N, int K, int group, int hadamard, const uint8_t* blob,
+cudaError_t launch_gemv_fused(const LaunchCtx& c, bool cq4, int N, int K, int group, int hadamard, const uint8_t* blob,
                               const void* x, int x_dtype, float* y, int8_t* a_out, float* sx_out)
 {
-    return launch_gemv_fused_set(c, 1, &N, K, group, hadamard, &blob, x, x_dtype, &y, a_out, sx_out);
+    return launch_gemv_fused_set(c, cq4, 1, &N, K, group, hadamard, &blob, x, x_dtype, &y, a_out, sx_out);
 }
 
 }  // namespace qmm

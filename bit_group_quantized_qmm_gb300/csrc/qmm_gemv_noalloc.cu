@@ -67,13 +67,13 @@ extern "C" qmm_status qmm_gemv_static_scratch(const qmm_weight_desc* w, const vo
     using namespace qmm;
     if (!w) return QMM_ERR_INVALID_ARG;
     const size_t need = qmm_gemv_workspace_size(w);
-    if (qmm_packed_size(w) == 0) return w->variant == QMM_W4A8 || w->variant == QMM_AFFINE
-                                            ? QMM_ERR_UNSUPPORTED_SHAPE
-                                            : QMM_ERR_INVALID_ARG;
+    if (qmm_packed_size(w) == 0)
+        return w->variant == QMM_W4A8 || w->variant == QMM_AFFINE || w->variant == QMM_CQ4 ? QMM_ERR_UNSUPPORTED_SHAPE
+                                                                                           : QMM_ERR_INVALID_ARG;
     if (need > kStaticScratchBytes) return QMM_ERR_WORKSPACE;
     if (need == 0) return qmm_gemv(w, packed, a, sx, y, nullptr, 0, stream);   // no split: no scratch used
     // validate everything qmm_gemv validates before touching the device
-    if (w->variant != QMM_W4A8) return QMM_ERR_UNSUPPORTED_SHAPE;
+    if (w->variant != QMM_W4A8 && w->variant != QMM_CQ4) return QMM_ERR_UNSUPPORTED_SHAPE;
     if (!packed || !a || !sx || !y) return QMM_ERR_INVALID_ARG;
     for (const void* p : {packed, static_cast<const void*>(a), static_cast<const void*>(sx),
                           static_cast<const void*>(y)})

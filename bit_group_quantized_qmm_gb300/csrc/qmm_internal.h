@@ -39,6 +39,10 @@ cudaError_t launch(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, 
 cudaError_t launch_pack(const LaunchCtx& c, int variant, int N, int K, int group, const uint8_t* q,
                         const uint16_t* scales, const uint16_t* biases, uint8_t* blob);
 
+// Codebook 4-bit weights: raw index nibbles + trailer (16 host levels, cb_scale).
+cudaError_t launch_pack_cq4(const LaunchCtx& c, int N, int K, int group, const uint8_t* idx, const int8_t* levels,
+                            float cb_scale, const uint16_t* scales, uint8_t* blob);
+
 cudaError_t launch_prep_w4a8(const LaunchCtx& c, int M, int K, int group, int hadamard, const void* x, int x_dtype,
                              int8_t* a, uint16_t* a16, float* sx, int32_t* asum);
 
@@ -50,7 +54,8 @@ int gemv_ksplit(int N, int K, int group);
 size_t gemv_workspace_bytes(int N, int K, int group);
 
 // y = W a (M = 1). P_debug != nullptr: write raw group partials instead.
-cudaError_t launch_gemv(const LaunchCtx& c, int N, int K, int group, const uint8_t* blob, const int8_t* a,
+// cq4: the blob holds codebook indices and a trailer (else symmetric W4A8).
+cudaError_t launch_gemv(const LaunchCtx& c, bool cq4, int N, int K, int group, const uint8_t* blob, const int8_t* a,
                         const float* sx, float* y, int32_t* P_debug, void* ws, size_t ws_bytes);
 
 // Largest activation-row tile of the tensor-core GEMM (MMA N).
@@ -60,10 +65,10 @@ constexpr int kMaxMTile = 128;
 // Fused prepass + GEMV over up to kMaxSiblings weight matrices that share x,
 // K and the group size (one launch; matrix i writes y[i]).
 constexpr int kMaxSiblings = 8;
-cudaError_t launch_gemv_fused_set(const LaunchCtx& c, int count, const int* N, int K, int group, int hadamard,
+cudaError_t launch_gemv_fused_set(const LaunchCtx& c, bool cq4, int count, const int* N, int K, int group, int hadamard,
                                   const uint8_t* const* blob, const void* x, int x_dtype, float* const* y,
                                   int8_t* a_out, float* sx_out);
-cudaError_t launch_gemv_fused(const LaunchCtx& c, int N, int K, int group, int hadamard, const uint8_t* blob,
+cudaError_t launch_gemv_fused(const LaunchCtx& c, bool cq4, int N, int K, int group, int hadamard, const uint8_t* blob,
                               const void* x, int x_dtype, float* y, int8_t* a_out, float* sx_out);
 
 struct GemmShape {
@@ -78,9 +83,11 @@ struct GemmShape {
 
 cudaError_t launch_gemm_w4a8(const LaunchCtx& c, int group, const CUtensorMap& map, const GemmShape& sh,
                              const uint8_t* blob, const float* sx, float* Y, int32_t* P, bool a_in_smem);
-// W4A8 GEMM for M <= 16 on the CUDA cores; cudaErrorNotSupported when the
+cudaError_t launch_gemm_cq4(const LaunchCtx& c, int group, const CUtensorMap& map, const GemmShape& sh,
+                            const uint8_t* blob, const float* sx, float* Y, int32_t* P, bool a_in_smem);
+// W4A8 / CQ4 GEMM for M <= 16 on the CUDA cores; cudaErrorNotSupported when the
 // shape does not fit it (the caller then uses the tensor-core kernel).
-cudaError_t launch_gemm_rows(const LaunchCtx& c, int group, int M, int N, int K, const uint8_t* blob,
+cudaError_t launch_gemm_rows(const LaunchCtx& c, bool cq4, int group, int M, int N, int K, const uint8_t* blob,
                              const uint16_t* act16, const float* sx, float* Y);
 cudaError_t launch_gemm_affine(const LaunchCtx& c, const CUtensorMap& map, const GemmShape& sh,
                                const uint8_t* blob, const float* gsum, float* Y, bool a_in_smem);

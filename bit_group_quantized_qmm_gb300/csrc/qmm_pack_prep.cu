@@ -10,6 +10,7 @@
 // this changes (group sums by the tiles' tree, X written once as half).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <string.h>
 
 #include "qmm_internal.h"
 #include "qmm_ptx.cuh"
@@ -34,10 +35,13 @@ __device__ __forceinline__ uint32_t repack_word(uint32_t w)
 }
 
 // One thread per 16-byte piece of the blob (row r, piece p, group g, tile t).
+// VARIANT 0 symmetric, 1 affine, 2 codebook (CQ4: raw indices, and the first
+// thread writes the trailer: levels, cb_scale, zero padding).
 template <int VARIANT, int GROUP>
 __global__ void __launch_bounds__(256) pack_kernel(int N, int K, const uint8_t* __restrict__ q,
                                                    const uint16_t* __restrict__ scales,
-                                                   const uint16_t* __restrict__ biases, uint8_t* __restrict__ blob)
+                                                   const uint16_t* __restrict__ biases, uint8_t* __restrict__ blob,
+                                                   uint4 levels, float cb_scale)
 {
     constexpr int PP = GROUP / 32;
     constexpr int CB = 64 * GROUP + 256 + (VARIANT == 1 ? 256 : 0);
@@ -50,6 +54,11 @@ __global__ void __launch_bounds__(256) pack_kernel(int N, int K, const uint8_t* 
     const long long total = (long long)T * G * PP * 128;
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= total) return;
+    if (VARIANT == 2 && idx == 0) {
+        uint4* tr = reinterpret_cast<uint4*>(blob + (size_t)T * G * CB);   // after the T*G chunks
+        tr[0] = levels;
+        tr[1] = make_uint4(__float_as_uint(cb_scale), 0u, 0u, 0u);
+    }
     const int r = (int)(idx % 128);
     long long rest = idx / 128;
     const int p = (int)(rest % PP);
@@ -85,12 +94,13 @@ __global__ void __launch_bounds__(256) pack_kernel(int N, int K, const uint8_t* 
 
 template <int VARIANT, int GROUP>
 static cudaError_t launch_pack_t(const LaunchCtx& c, int N, int K, const uint8_t* q, const uint16_t* s,
-                                 const uint16_t* b, uint8_t* blob)
+                                 const uint16_t* b, uint8_t* blob, uint4 levels = uint4{}, float cb_scale = 0.f)
 {
     const long long total = (long long)((N + 127) / 128) * (K / GROUP) * (GROUP / 32) * 128;
     const int threads = 256;
     const long long blocks = (total + threads - 1) / threads;
-    return launch(pack_kernel<VARIANT, GROUP>, dim3((unsigned)blocks), dim3(threads), 0, c, N, K, q, s, b, blob);
+    return launch(pack_kernel<VARIANT, GROUP>, dim3((unsigned)blocks), dim3(threads), 0, c, N, K, q, s, b, blob,
+                  levels, cb_scale);
 }
 
 cudaError_t launch_pack(const LaunchCtx& c, int variant, int N, int K, int group, const uint8_t* q,
@@ -99,6 +109,16 @@ cudaError_t launch_pack(const LaunchCtx& c, int variant, int N, int K, int group
     if (variant == 0 && group == 64) return launch_pack_t<0, 64>(c, N, K, q, scales, biases, blob);
     if (variant == 0 && group == 128) return launch_pack_t<0, 128>(c, N, K, q, scales, biases, blob);
     if (variant == 1 && group == 64) return launch_pack_t<1, 64>(c, N, K, q, scales, biases, blob);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_pack_cq4(const LaunchCtx& c, int N, int K, int group, const uint8_t* idx, const int8_t* levels,
+                            float cb_scale, const uint16_t* scales, uint8_t* blob)
+{
+    uint4 lv;
+    memcpy(&lv, levels, 16);
+    if (group == 64) return launch_pack_t<2, 64>(c, N, K, idx, scales, nullptr, blob, lv, cb_scale);
+    if (group == 128) return launch_pack_t<2, 128>(c, N, K, idx, scales, nullptr, blob, lv, cb_scale);
     return cudaErrorInvalidValue;
 }
 

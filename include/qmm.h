@@ -25,8 +25,21 @@
  *              (TensorFold PR #3215 "simd_qmm on Metal: X's group sums and
  *              half operands from a prepass": What this changes.)
  *
- * Calls:  qmm_pack_weights (once per weight) -> qmm_prep_act (per call) ->
- *         qmm_gemv (M == 1, W4A8) or qmm_gemm (any M, both variants).
+ *   QMM_CQ4    codebook 4-bit weights: each weight is a 4-bit index i into
+ *              one 16-entry int8 codebook C of the matrix, scaled by one fp32
+ *              cb_scale per matrix and the per-group fp16 scale sw. The
+ *              activation side is exactly the W4A8 one (same prepass), the
+ *              partials stay integer and cb_scale folds into the rescale:
+ *                  Y[m][n] = cb_scale * sum_g sw[n][g] * sx[m][g] * P[m][n][g]
+ *                  P[m][n][g] = sum_{k in g} C[i[n][k]] * a[m][k]
+ *              (cactus PR #697, Summary: 4-bit codebook expansion inside the
+ *              GEMV leaf by table lookup; follow-up "single runtime weight
+ *              format": the codebook scale is folded into the per-row norms.)
+ *
+ * Calls:  qmm_pack_weights / qmm_pack_weights_cq4 (once per weight) ->
+ *         qmm_prep_act (per call) -> qmm_gemv (M == 1, W4A8 and CQ4) or
+ *         qmm_gemm (any M, all variants); qmm_gemv_fused does the prepass and
+ *         the GEMV in one launch.
  *
  * Conventions for every entry point:
  *   - All pointers named "device" are CUDA device pointers in the current
@@ -71,7 +84,7 @@ typedef enum {
     QMM_ERR_WORKSPACE = 7           /* workspace too small */
 } qmm_status;
 
-typedef enum { QMM_W4A8 = 0, QMM_AFFINE = 1 } qmm_variant;
+typedef enum { QMM_W4A8 = 0, QMM_AFFINE = 1, QMM_CQ4 = 2 } qmm_variant;
 
 typedef enum { QMM_DTYPE_F32 = 0, QMM_DTYPE_F16 = 1, QMM_DTYPE_BF16 = 2 } qmm_dtype;
 
@@ -89,13 +102,15 @@ typedef enum {
     QMM_KERNEL_GEMM_AFFINE = 6,
     QMM_KERNEL_GEMV_FUSED = 7,
     QMM_KERNEL_GEMM_ROWS = 8,
-    QMM_KERNEL_GEMV_FUSED_SIBLINGS = 9
+    QMM_KERNEL_GEMV_FUSED_SIBLINGS = 9,
+    QMM_KERNEL_GEMV_CQ4 = 10,
+    QMM_KERNEL_GEMM_CQ4 = 11
 } qmm_kernel_id;
 
 typedef void* qmm_stream; /* cudaStream_t */
 
 /* A quantized weight matrix W [N][K].
- *   variant: QMM_W4A8 (group 64 or 128) or QMM_AFFINE (group 64).
+ *   variant: QMM_W4A8 or QMM_CQ4 (group 64 or 128), QMM_AFFINE (group 64).
  *   N >= 1, K >= group, K % group == 0. */
 typedef struct {
     int32_t variant;
@@ -112,7 +127,7 @@ typedef struct {
  *
  * With T = ceil(N/128) row tiles, G = K/group groups and PP = group/32 pieces
  * per group, the blob is T*G chunks of CB bytes,
- *     CB = 64*group + 256            (QMM_W4A8)
+ *     CB = 64*group + 256            (QMM_W4A8, QMM_CQ4)
  *     CB = 64*group + 512            (QMM_AFFINE),
  * chunk (t, g) at byte (t*G + g)*CB. Inside a chunk:
  *     [0, 64*group)           nibbles: piece p (0..PP-1), row r (0..127) at
@@ -122,10 +137,15 @@ typedef struct {
  *                             k = 8j..8j+7 of the piece. In word j, nibble slot
  *                             s (bits 4s..4s+3) holds local k = 8j + 2s for
  *                             s < 4 and 8j + 2(s-4) + 1 for s >= 4.
- *                             Nibble value: q + 8 (QMM_W4A8), q (QMM_AFFINE).
+ *                             Nibble value: q + 8 (QMM_W4A8), q (QMM_AFFINE),
+ *                             the codebook index i (QMM_CQ4).
  *     [64*group, +256)        scales: 128 fp16, row r at 2r (sw[n][g]).
  *     [64*group+256, +256)    biases (QMM_AFFINE only): 128 fp16, row r at 2r.
- * Rows n >= N of the last tile hold q = 0 and zero scales and biases.
+ * QMM_CQ4 appends a 32-byte trailer at byte T*G*CB: the 16 codebook levels
+ * (int8, level j at byte j), cb_scale (fp32, little-endian, bytes 16-19) and
+ * 12 zero bytes.
+ * Rows n >= N of the last tile hold q = 0 (index 0 for QMM_CQ4) and zero
+ * scales and biases.
  * The blob depends only on the logical values of q, scales and biases.
  */
 size_t qmm_packed_size(const qmm_weight_desc* w);
@@ -140,16 +160,33 @@ size_t qmm_packed_size(const qmm_weight_desc* w);
  *   biases  device, [N][G] fp16; QMM_AFFINE only (must be NULL for QMM_W4A8).
  *   packed  device, qmm_packed_size(w) bytes, written entirely.
  * K must be a multiple of 32 and of group. The sources may be freed once the
- * stream has passed this call.
+ * stream has passed this call. QMM_CQ4 weights need their codebook: they are
+ * packed by qmm_pack_weights_cq4 (QMM_ERR_INVALID_ARG here).
  */
 qmm_status qmm_pack_weights(const qmm_weight_desc* w, const uint8_t* q, const uint16_t* scales,
                             const uint16_t* biases, void* packed, qmm_stream stream);
 
 /*
+ * Repack QMM_CQ4 weights (device kernel, on `stream`).
+ *   idx       device, [N][K/2] bytes of 4-bit codebook indices, low nibble
+ *             first (the layout of qmm_pack_weights' q).
+ *   codebook  HOST pointer, 16 int8 levels C[0..15] (read during the call).
+ *   cb_scale  the matrix's codebook scale; must be finite (QMM_ERR_INVALID_ARG).
+ *   scales    device, [N][G] fp16 sw.
+ *   packed    device, qmm_packed_size(w) bytes (chunks + trailer), written
+ *             entirely.
+ * The codebook is the matrix's own: the integer partials use its levels as
+ * given (no assumption of order or symmetry), so any relabelling of indices
+ * and levels gives the same results.
+ */
+qmm_status qmm_pack_weights_cq4(const qmm_weight_desc* w, const uint8_t* idx, const int8_t* codebook,
+                                float cb_scale, const uint16_t* scales, void* packed, qmm_stream stream);
+
+/*
  * Activation prepass (device kernel, on `stream`).
  *
- * QMM_W4A8 (cactus PR #697, Summary: "phase A does parallel Hadamard + int8
- * activation quantization"; geistlib issue #500, Design sketch item 4: one
+ * QMM_W4A8 and QMM_CQ4 (cactus PR #697, Summary: phase A rotates and quantizes
+ * the activations to int8 in parallel; geistlib issue #500, Design sketch item 4: one
  * activation quantization shared by the GEMV and GEMM paths). For each row m
  * and group g, with v = x[m][g*group .. +group) in fp32:
  *   if hadamard == group: v <- H v, the unnormalised Sylvester-order
@@ -196,9 +233,11 @@ qmm_status qmm_prep_act(int32_t variant, int32_t M, int32_t K, int32_t group, in
 size_t qmm_gemv_workspace_size(const qmm_weight_desc* w);
 
 /*
- * M = 1 decode GEMV, QMM_W4A8 (cactus PR #697, Summary: hybrid fused GEMV,
- * "stream packed nibbles ... half the weight bytes"; the op is DRAM-bound):
+ * M = 1 decode GEMV, QMM_W4A8 or QMM_CQ4 (cactus PR #697, Summary: the hybrid
+ * fused GEMV streams the packed nibbles, half the weight bytes, and is
+ * DRAM-bound):
  *   y[n] = sum_g sw[n][g] * sx[g] * P[n][g],  P[n][g] = sum_{k in g} q[n][k] a[k]
+ *   (QMM_CQ4: q[n][k] = C[i[n][k]] and y is multiplied by cb_scale)
  *   packed     device blob from qmm_pack_weights
  *   a          device int8 [K] (qmm_prep_act output a, row 0)
  *   sx         device fp32 [G]
@@ -212,7 +251,7 @@ qmm_status qmm_gemv(const qmm_weight_desc* w, const void* packed, const int8_t* 
                     float* y, void* workspace, size_t workspace_bytes, qmm_stream stream);
 
 /*
- * One-kernel M = 1 decode GEMV, QMM_W4A8: the activation prepass and the GEMV
+ * One-kernel M = 1 decode GEMV, QMM_W4A8 or QMM_CQ4: the activation prepass and the GEMV
  * in a single launch (cactus PR #697, Summary: the M = 1 path is one dispatch
  * whose phase A rotates and quantizes the activations and whose phase B
  * streams the packed nibbles through the integer partials).
@@ -231,12 +270,13 @@ qmm_status qmm_gemv_fused(const qmm_weight_desc* w, const void* packed, const vo
                           int32_t hadamard, float* y, int8_t* a_out, float* sx_out, qmm_stream stream);
 
 /*
- * Fused sibling GEMVs, QMM_W4A8: up to QMM_MAX_SIBLINGS weight matrices that
+ * Fused sibling GEMVs, QMM_W4A8 or QMM_CQ4: up to QMM_MAX_SIBLINGS weight matrices that
  * read the same input (q|k|v, gate|up) in one launch, x rotated and quantized
  * once per K-slice for all of them (cactus engine PR #750 "Metal Support":
  * sibling quantized GEMVs fused into one batched dispatch; geistlib issue #500,
  * Design sketch item 5: paired linears share one activation quantization).
- *   w[i], packed[i]  the matrices: same variant (W4A8), K and group; any N[i]
+ *   w[i], packed[i]  the matrices: one variant (all W4A8 or all CQ4, each CQ4
+ *                    matrix with its own codebook), same K and group; any N[i]
  *   x, x_dtype, hadamard, a_out, sx_out   as qmm_gemv_fused
  *   y[i]             device fp32 [w[i].N]
  * Each y[i] matches qmm_gemv_fused on matrix i within the W4A8 tolerance (the
@@ -274,10 +314,10 @@ qmm_status qmm_gemv_static_scratch(const qmm_weight_desc* w, const void* packed,
                                    const float* sx, float* y, qmm_stream stream);
 
 /*
- * GEMM, any M >= 1, both variants, on the tcgen05 tensor cores
+ * GEMM, any M >= 1, all variants, on the tcgen05 tensor cores
  * (cactus PR #697, Summary: fused GEMM with raw int32 partials and a separate
  * fp32 rescale; TensorFold PR #3215 for the affine tiles on the prepass sums).
- * A W4A8 call with M at or below the limit set by qmm_set_gemm_rows_max
+ * A W4A8 or CQ4 call with M at or below the limit set by qmm_set_gemm_rows_max
  * (default 8) runs instead on the CUDA cores: exact int32 partials with dp4a,
  * each weight read once for all rows (qmm_last_kernel_id reports
  * QMM_KERNEL_GEMM_ROWS); same inputs, same outputs within the W4A8 tolerance.
@@ -285,6 +325,8 @@ qmm_status qmm_gemv_static_scratch(const qmm_weight_desc* w, const void* packed,
  * 24 groups of 64, or 12 of 128) stay on the tensor cores.
  *   QMM_W4A8:   act16 = qmm_prep_act a16 [M][K] fp16 codes, act_scale = sx [M][G]
  *               Y[m][n] = sum_g sw[n][g] * sx[m][g] * P[m][n][g]
+ *   QMM_CQ4:    as QMM_W4A8, with q[n][k] = C[i[n][k]], times cb_scale
+ *               (qmm_last_kernel_id: QMM_KERNEL_GEMM_CQ4 on the tensor cores)
  *   QMM_AFFINE: act16 = x as fp16 [M][K],     act_scale = S  [M][G]
  *               Y[m][n] = sum_g ( s[n][g] * sum_{k in g} q[n][k] x[m][k] + b[n][g] * S[m][g] )
  *   Y          device fp32 [M][N], row-major; rows m < M written, nothing else.
@@ -296,9 +338,10 @@ qmm_status qmm_gemm(const qmm_weight_desc* w, const void* packed, int32_t M, con
                     const float* act_scale, float* Y, qmm_stream stream);
 
 /*
- * Test hook (QMM_W4A8 only): run the GEMV or GEMM kernel of `path` with its
- * epilogue replaced by a store of the raw group partials
- *   P[m][n][g] = sum_{k in g} q[n][k] * a[m][k]   (int32, [M][N][G])
+ * Test hook (QMM_W4A8 and QMM_CQ4): run the GEMV or GEMM kernel of `path`
+ * with its epilogue replaced by a store of the raw group partials
+ *   P[m][n][g] = sum_{k in g} q[n][k] * a[m][k]   (int32, [M][N][G];
+ *   QMM_CQ4: q[n][k] = C[i[n][k]], no cb_scale)
  * (the per-group partials contract of cactus PR #697: partials_out holds raw
  * dot products, the caller applies the scales).
  *   path QMM_PATH_GEMV: M must be 1, act = int8 a [K].
@@ -331,7 +374,7 @@ void qmm_set_pdl(int32_t enable);
  * give the same partials; the choice only moves on-chip traffic. */
 void qmm_set_gemm_weight_operand(int32_t in_shared_memory);
 
-/* Largest M for which a W4A8 qmm_gemm runs on the CUDA-core (dp4a) kernel
+/* Largest M for which a W4A8 or CQ4 qmm_gemm runs on the CUDA-core (dp4a) kernel
  * (process-wide, launches after the call): 0 sends every call to the tensor
  * cores; values above 16 are treated as 16. Default 8 (above it the tensor
  * cores are as fast or faster on the measured shapes). */

@@ -7,7 +7,7 @@ import numpy as np
 
 import qmm_synth
 
-W4A8, AFFINE = 0, 1
+W4A8, AFFINE, CQ4 = 0, 1, 2
 
 
 def lib():
@@ -33,6 +33,16 @@ def pack(variant, N, K, group, q_bytes, scales, biases=None):
     d = q.weight_desc(variant, N, K, group)
     packed = torch.empty(q.qmm_packed_size(d), dtype=torch.uint8, device=dev())
     q.qmm_pack_weights(d, t(q_bytes), t(scales), None if biases is None else t(biases), packed)
+    assert q.qmm_last_kernel_id() == 1
+    return d, packed
+
+
+def pack_cq4(N, K, group, idx_bytes, codebook, cb_scale, scales):
+    import torch
+    q = lib()
+    d = q.weight_desc(CQ4, N, K, group)
+    packed = torch.empty(q.qmm_packed_size(d), dtype=torch.uint8, device=dev())
+    q.qmm_pack_weights_cq4(d, t(idx_bytes), codebook, cb_scale, t(scales), packed)
     assert q.qmm_last_kernel_id() == 1
     return d, packed
 
@@ -67,13 +77,14 @@ def gemv(d, packed, a, sx, workspace=True):
         if nbytes:
             ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev())
     q.qmm_gemv(d, packed, a, sx, y, ws)
-    assert q.qmm_last_kernel_id() == 4
+    assert q.qmm_last_kernel_id() == (10 if d.variant == CQ4 else 4)
     return y
 
 
 def gemm(d, packed, M, act16, act_scale, kernel=None):
     """qmm_gemm into a NaN-filled Y; checks which kernel ran (W4A8: the
-    tensor-core kernel 5 or the CUDA-core small-M kernel 8; affine: 6)."""
+    tensor-core kernel 5 or the CUDA-core small-M kernel 8; CQ4: 11 or 8;
+    affine: 6)."""
     import torch
     q = lib()
     Y = torch.full((M, d.N), float("nan"), dtype=torch.float32, device=dev())
@@ -82,7 +93,7 @@ def gemm(d, packed, M, act16, act_scale, kernel=None):
     if kernel is not None:
         assert kid == kernel, kid
     else:
-        assert kid in ((5, 8) if d.variant == W4A8 else (6,)), kid
+        assert kid in {W4A8: (5, 8), CQ4: (11, 8), AFFINE: (6,)}[d.variant], kid
     return Y
 
 
@@ -100,6 +111,15 @@ def w4a8_case(seed, name, N, K, group, hadamard, M, outlier_frac=0.0):
     qb, sw, _ = qmm_synth.layer_weights(seed, name, lay)
     x = qmm_synth.layer_activations(seed, name, lay, M)
     return qb, sw, x
+
+
+def cq4_case(seed, name, N, K, group, hadamard, M, outlier_frac=0.0):
+    """(index bytes, sw, codebook, cb_scale, x) of a codebook-4-bit layer."""
+    lay = qmm_synth.Layer(name, CQ4, N, K, group, hadamard, outlier_frac=outlier_frac)
+    idx, sw, _ = qmm_synth.layer_weights(seed, name, lay)
+    C, cb = qmm_synth.layer_codebook(seed, name)
+    x = qmm_synth.layer_activations(seed, name, lay, M)
+    return idx, sw, C, cb, x
 
 
 def within_w4a8(y, Y, Ym):

@@ -31,7 +31,8 @@ def test_exports_every_declared_symbol(q):
 
 
 @pytest.mark.parametrize("variant,N,K,group", [(0, 1024, 1024, 64), (0, 1, 64, 64), (0, 130, 512, 128),
-                                               (1, 34816, 5120, 64), (0, 262144, 1536, 128), (1, 129, 192, 64)])
+                                               (1, 34816, 5120, 64), (0, 262144, 1536, 128), (1, 129, 192, 64),
+                                               (2, 12288, 1536, 64), (2, 130, 256, 128), (2, 1, 64, 64)])
 def test_packed_size_matches_oracle(q, variant, N, K, group):
     d = q.weight_desc(variant, N, K, group)
     assert q.qmm_packed_size(d) == oracle.packed_size(variant, N, K, group)
@@ -42,6 +43,7 @@ def test_packed_size_rejects(q):
     assert q.qmm_packed_size(q.weight_desc(1, 128, 256, 128)) == 0    # affine group 128
     assert q.qmm_packed_size(q.weight_desc(0, 0, 256, 64)) == 0
     assert q.qmm_packed_size(q.weight_desc(5, 128, 256, 64)) == 0
+    assert q.qmm_packed_size(q.weight_desc(2, 128, 256, 32)) == 0     # CQ4 group 32
 
 
 def test_host_validation(q):
@@ -81,6 +83,20 @@ def test_host_validation(q):
     assert L.qmm_gemv_fused_siblings(2, grp, ptrs, A, 0, 64, ptrs, None, None, None) == SHAPE
     nulls = (ctypes.c_void_p * 3)(A, None, A)
     assert L.qmm_gemv_fused_siblings(3, descs, nulls, A, 0, 64, ptrs, None, None, None) == INV
+    # codebook weights: packed only with their codebook, one variant per sibling launch
+    c = q.weight_desc(2, 256, 256, 64)
+    book = (ctypes.c_int8 * 16)(*range(-8, 8))
+    assert L.qmm_pack_weights(D(c), A, A, None, A, None) == INV
+    assert L.qmm_pack_weights_cq4(D(d), A, book, 1.0, A, A, None) == INV          # not a CQ4 desc
+    assert L.qmm_pack_weights_cq4(D(c), A, None, 1.0, A, A, None) == INV         # no codebook
+    assert L.qmm_pack_weights_cq4(D(c), A, book, float("nan"), A, A, None) == INV
+    assert L.qmm_pack_weights_cq4(D(c), A, book, float("inf"), A, A, None) == INV
+    assert L.qmm_pack_weights_cq4(D(c), A + 2, book, 1.0, A, A, None) == MIS
+    assert L.qmm_pack_weights_cq4(D(q.weight_desc(2, 256, 250, 64)), A, book, 1.0, A, A, None) == SHAPE
+    assert L.qmm_gemv(D(c), A, A, A, A + 4, None, 0, None) == MIS
+    assert L.qmm_gemv_workspace_size(D(c)) == L.qmm_gemv_workspace_size(D(d))
+    mixv = (q.qmm_weight_desc * 2)(q.weight_desc(0, 256, 256, 64), q.weight_desc(2, 256, 256, 64))
+    assert L.qmm_gemv_fused_siblings(2, mixv, ptrs, A, 0, 64, ptrs, None, None, None) == SHAPE
 
 
 def test_valid_arguments_reach_the_device_probe(q):
@@ -92,6 +108,10 @@ def test_valid_arguments_reach_the_device_probe(q):
     A = 1 << 20
     assert L.qmm_pack_weights(ctypes.byref(d), A, A, None, A, None) == 3
     assert L.qmm_gemm(ctypes.byref(d), A, 4, A, A, A, None) == 3
+    c = q.weight_desc(2, 256, 256, 64)
+    book = (ctypes.c_int8 * 16)(*range(-8, 8))
+    assert L.qmm_pack_weights_cq4(ctypes.byref(c), A, book, 0.5, A, A, None) == 3
+    assert L.qmm_gemm(ctypes.byref(c), A, 4, A, A, A, None) == 3
 
 
 def test_status_strings(q):
