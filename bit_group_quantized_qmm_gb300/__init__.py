@@ -51,6 +51,7 @@ def _load():
         "qmm_packed_size": (SZ, [D]),
         "qmm_pack_weights": (I32, [D, P, P, P, P, P]),
         "qmm_pack_weights_cq4": (I32, [D, P, P, ctypes.c_float, P, P, P]),
+        "qmm_pack_weights_interleaved4": (I32, [D, I32, P, P, P, P, ctypes.c_float, P, P]),
         "qmm_prep_act": (I32, [I32, I32, I32, I32, I32, P, I32, P, P, P, P, P, P, P]),
         "qmm_gemv_workspace_size": (SZ, [D]),
         "qmm_gemv": (I32, [D, P, P, P, P, P, SZ, P]),
@@ -142,6 +143,21 @@ def qmm_pack_weights_cq4(desc, idx, codebook, cb_scale, scales, packed, stream=N
     _check(_L.qmm_pack_weights_cq4(ctypes.byref(desc), _ptr(idx), levels.ctypes.data_as(ctypes.c_void_p),
                                    float(cb_scale), _ptr(scales), _ptr(packed), _stream(stream)),
            "qmm_pack_weights_cq4")
+
+
+def qmm_pack_weights_interleaved4(desc, chunk_k, panels, scales, biases, packed, codebook=None, cb_scale=1.0,
+                                  stream=None):
+    """Weights in 4-row panels; codebook (16 int8 host levels) for QMM_CQ4 only."""
+    import numpy as np
+    cb = None
+    if codebook is not None:
+        levels = np.ascontiguousarray(np.asarray(codebook, dtype=np.int8).reshape(-1))
+        if levels.size != 16:
+            raise ValueError("a CQ4 codebook has 16 levels")
+        cb = levels.ctypes.data_as(ctypes.c_void_p)
+    _check(_L.qmm_pack_weights_interleaved4(ctypes.byref(desc), int(chunk_k), _ptr(panels), _ptr(scales),
+                                            _ptr(biases), cb, float(cb_scale), _ptr(packed), _stream(stream)),
+           "qmm_pack_weights_interleaved4")
 
 
 def qmm_prep_act(variant, M, K, group, hadamard, x, x_dtype, a=None, a16=None, sx=None, asum=None, gsum=None,

@@ -208,6 +208,28 @@ qmm_status qmm_pack_weights_cq4(const qmm_weight_desc* w, const uint8_t* idx, co
                     QMM_KERNEL_PACK);
 }
 
+qmm_status qmm_pack_weights_interleaved4(const qmm_weight_desc* w, int32_t chunk_k, const uint8_t* panels,
+                                        const uint16_t* scales, const uint16_t* biases, const int8_t* codebook,
+                                        float cb_scale, void* packed, qmm_stream stream)
+{
+    qmm_status st = shape_ok(w);
+    if (st != QMM_OK) return st;
+    if (chunk_k != 8 && chunk_k != 16 && chunk_k != 32 && chunk_k != 64 && chunk_k != 128)
+        return QMM_ERR_INVALID_ARG;
+    if (w->K % chunk_k != 0) return QMM_ERR_UNSUPPORTED_SHAPE;
+    if (!panels || !scales || !packed) return QMM_ERR_INVALID_ARG;
+    if ((w->variant == QMM_AFFINE) != (biases != nullptr)) return QMM_ERR_INVALID_ARG;
+    if ((w->variant == QMM_CQ4) != (codebook != nullptr)) return QMM_ERR_INVALID_ARG;
+    if (w->variant == QMM_CQ4 && !isfinite(cb_scale)) return QMM_ERR_INVALID_ARG;
+    if (!aligned16(panels) || !aligned16(scales) || !aligned16(packed) || (biases && !aligned16(biases)))
+        return QMM_ERR_MISALIGNED;
+    LaunchCtx c;
+    if ((st = device_ctx(stream, &c)) != QMM_OK) return st;
+    return launched(launch_pack_il4(c, w->variant, w->N, w->K, w->group, chunk_k, panels, scales, biases, codebook,
+                                    cb_scale, static_cast<uint8_t*>(packed)),
+                    QMM_KERNEL_PACK);
+}
+
 qmm_status qmm_prep_act(int32_t variant, int32_t M, int32_t K, int32_t group, int32_t hadamard, const void* x,
                         int32_t x_dtype, int8_t* a, uint16_t* a16, float* sx, int32_t* asum, float* gsum,
                         uint16_t* x16, qmm_stream stream)

@@ -43,6 +43,11 @@ cudaError_t launch_pack(const LaunchCtx& c, int variant, int N, int K, int group
 cudaError_t launch_pack_cq4(const LaunchCtx& c, int N, int K, int group, const uint8_t* idx, const int8_t* levels,
                             float cb_scale, const uint16_t* scales, uint8_t* blob);
 
+// 4-row panel input (any variant): chunk_k weights per row per k-chunk.
+cudaError_t launch_pack_il4(const LaunchCtx& c, int variant, int N, int K, int group, int chunk_k,
+                            const uint8_t* panels, const uint16_t* scales, const uint16_t* biases,
+                            const int8_t* levels, float cb_scale, uint8_t* blob);
+
 cudaError_t launch_prep_w4a8(const LaunchCtx& c, int M, int K, int group, int hadamard, const void* x, int x_dtype,
                              int8_t* a, uint16_t* a16, float* sx, int32_t* asum);
 

@@ -34,6 +34,25 @@ __device__ __forceinline__ uint32_t repack_word(uint32_t w)
     return lo | (hi << 16);
 }
 
+// Source layouts. il4_cb == 0: row-major nibble bytes [N][K/2] and scales
+// [N][G]. il4_cb > 0: 4-row panels (cactus PR #697, follow-up on the
+// orthogonal lm_head: the production INTERLEAVED_4ROW layout keeps rows in
+// blocks of four, block nb at byte nb*2K, its bytes ordered by k-chunk; scales
+// of block nb, group g, row ni at (nb*G + g)*4 + ni). Chunk c of a block holds
+// the four rows' il4_cb bytes (2*il4_cb weights) in row order.
+__device__ __forceinline__ size_t src_byte(int n, int kb, int K, int il4_cb)
+{
+    if (il4_cb == 0) return (size_t)n * (K / 2) + kb;
+    return (size_t)(n >> 2) * (2 * K) + (size_t)(kb / il4_cb) * (4 * il4_cb) + (size_t)(n & 3) * il4_cb +
+           (size_t)(kb % il4_cb);
+}
+
+__device__ __forceinline__ size_t src_scale(int n, int g, int G, int il4_cb)
+{
+    if (il4_cb == 0) return (size_t)n * G + g;
+    return ((size_t)(n >> 2) * G + g) * 4 + (size_t)(n & 3);
+}
+
 // One thread per 16-byte piece of the blob (row r, piece p, group g, tile t).
 // VARIANT 0 symmetric, 1 affine, 2 codebook (CQ4: raw indices, and the first
 // thread writes the trailer: levels, cb_scale, zero padding).
@@ -41,7 +60,7 @@ template <int VARIANT, int GROUP>
 __global__ void __launch_bounds__(256) pack_kernel(int N, int K, const uint8_t* __restrict__ q,
                                                    const uint16_t* __restrict__ scales,
                                                    const uint16_t* __restrict__ biases, uint8_t* __restrict__ blob,
-                                                   uint4 levels, float cb_scale)
+                                                   uint4 levels, float cb_scale, int il4_cb)
 {
     constexpr int PP = GROUP / 32;
     constexpr int CB = 64 * GROUP + 256 + (VARIANT == 1 ? 256 : 0);
@@ -72,8 +91,18 @@ __global__ void __launch_bounds__(256) pack_kernel(int N, int K, const uint8_t* 
     const uint32_t flip = VARIANT == 0 ? 0x88888888u : 0u;
     uint4 out;
     if (n < N) {
-        const uint4 in =
-            *reinterpret_cast<const uint4*>(q + (size_t)n * (K / 2) + (size_t)(g * GROUP + 32 * p) / 2);
+        const int kb = (g * GROUP + 32 * p) / 2;
+        uint4 in;
+        if (il4_cb == 0 || il4_cb >= 16) {
+            // the piece's 16 bytes are contiguous (16-byte aligned) in the source
+            in = *reinterpret_cast<const uint4*>(q + src_byte(n, kb, K, il4_cb));
+        } else {
+            // narrow chunks: each aligned 4-byte word lies inside one chunk
+            in.x = *reinterpret_cast<const uint32_t*>(q + src_byte(n, kb, K, il4_cb));
+            in.y = *reinterpret_cast<const uint32_t*>(q + src_byte(n, kb + 4, K, il4_cb));
+            in.z = *reinterpret_cast<const uint32_t*>(q + src_byte(n, kb + 8, K, il4_cb));
+            in.w = *reinterpret_cast<const uint32_t*>(q + src_byte(n, kb + 12, K, il4_cb));
+        }
         out.x = repack_word(in.x) ^ flip;
         out.y = repack_word(in.y) ^ flip;
         out.z = repack_word(in.z) ^ flip;
@@ -83,10 +112,10 @@ __global__ void __launch_bounds__(256) pack_kernel(int N, int K, const uint8_t* 
     }
     *reinterpret_cast<uint4*>(chunk + p * 2048 + r * 16) = out;
     if (p == 0) {
-        const uint16_t s = n < N ? scales[(size_t)n * G + g] : 0;
+        const uint16_t s = n < N ? scales[src_scale(n, g, G, il4_cb)] : 0;
         *reinterpret_cast<uint16_t*>(chunk + 64 * GROUP + 2 * r) = s;
         if (VARIANT == 1) {
-            const uint16_t b = n < N ? biases[(size_t)n * G + g] : 0;
+            const uint16_t b = n < N ? biases[src_scale(n, g, G, il4_cb)] : 0;
             *reinterpret_cast<uint16_t*>(chunk + 64 * GROUP + 256 + 2 * r) = b;
         }
     }
@@ -94,22 +123,33 @@ __global__ void __launch_bounds__(256) pack_kernel(int N, int K, const uint8_t* 
 
 template <int VARIANT, int GROUP>
 static cudaError_t launch_pack_t(const LaunchCtx& c, int N, int K, const uint8_t* q, const uint16_t* s,
-                                 const uint16_t* b, uint8_t* blob, uint4 levels = uint4{}, float cb_scale = 0.f)
+                                 const uint16_t* b, uint8_t* blob, uint4 levels, float cb_scale, int il4_cb)
 {
     const long long total = (long long)((N + 127) / 128) * (K / GROUP) * (GROUP / 32) * 128;
     const int threads = 256;
     const long long blocks = (total + threads - 1) / threads;
     return launch(pack_kernel<VARIANT, GROUP>, dim3((unsigned)blocks), dim3(threads), 0, c, N, K, q, s, b, blob,
-                  levels, cb_scale);
+                  levels, cb_scale, il4_cb);
+}
+
+static cudaError_t launch_pack_any(const LaunchCtx& c, int variant, int N, int K, int group, const uint8_t* q,
+                                   const uint16_t* scales, const uint16_t* biases, uint8_t* blob, uint4 lv,
+                                   float cb_scale, int il4_cb)
+{
+    if (variant == 0 && group == 64) return launch_pack_t<0, 64>(c, N, K, q, scales, biases, blob, lv, 0.f, il4_cb);
+    if (variant == 0 && group == 128) return launch_pack_t<0, 128>(c, N, K, q, scales, biases, blob, lv, 0.f, il4_cb);
+    if (variant == 1 && group == 64) return launch_pack_t<1, 64>(c, N, K, q, scales, biases, blob, lv, 0.f, il4_cb);
+    if (variant == 2 && group == 64) return launch_pack_t<2, 64>(c, N, K, q, scales, nullptr, blob, lv, cb_scale, il4_cb);
+    if (variant == 2 && group == 128)
+        return launch_pack_t<2, 128>(c, N, K, q, scales, nullptr, blob, lv, cb_scale, il4_cb);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_pack(const LaunchCtx& c, int variant, int N, int K, int group, const uint8_t* q,
                         const uint16_t* scales, const uint16_t* biases, uint8_t* blob)
 {
-    if (variant == 0 && group == 64) return launch_pack_t<0, 64>(c, N, K, q, scales, biases, blob);
-    if (variant == 0 && group == 128) return launch_pack_t<0, 128>(c, N, K, q, scales, biases, blob);
-    if (variant == 1 && group == 64) return launch_pack_t<1, 64>(c, N, K, q, scales, biases, blob);
-    return cudaErrorInvalidValue;
+    if (variant == 2) return cudaErrorInvalidValue;
+    return launch_pack_any(c, variant, N, K, group, q, scales, biases, blob, uint4{}, 0.f, 0);
 }
 
 cudaError_t launch_pack_cq4(const LaunchCtx& c, int N, int K, int group, const uint8_t* idx, const int8_t* levels,
@@ -117,9 +157,16 @@ cudaError_t launch_pack_cq4(const LaunchCtx& c, int N, int K, int group, const u
 {
     uint4 lv;
     memcpy(&lv, levels, 16);
-    if (group == 64) return launch_pack_t<2, 64>(c, N, K, idx, scales, nullptr, blob, lv, cb_scale);
-    if (group == 128) return launch_pack_t<2, 128>(c, N, K, idx, scales, nullptr, blob, lv, cb_scale);
-    return cudaErrorInvalidValue;
+    return launch_pack_any(c, 2, N, K, group, idx, scales, nullptr, blob, lv, cb_scale, 0);
+}
+
+cudaError_t launch_pack_il4(const LaunchCtx& c, int variant, int N, int K, int group, int chunk_k,
+                            const uint8_t* panels, const uint16_t* scales, const uint16_t* biases,
+                            const int8_t* levels, float cb_scale, uint8_t* blob)
+{
+    uint4 lv{};
+    if (variant == 2) memcpy(&lv, levels, 16);
+    return launch_pack_any(c, variant, N, K, group, panels, scales, biases, blob, lv, cb_scale, chunk_k / 2);
 }
 
 // ------------------------------------------------------------------ loads

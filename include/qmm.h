@@ -183,6 +183,35 @@ qmm_status qmm_pack_weights_cq4(const qmm_weight_desc* w, const uint8_t* idx, co
                                 float cb_scale, const uint16_t* scales, void* packed, qmm_stream stream);
 
 /*
+ * Repack weights given in 4-row panels (device kernel, on `stream`); any
+ * variant. The blob is byte-identical to the one qmm_pack_weights (or
+ * qmm_pack_weights_cq4) builds from the same weights in row-major order
+ * (cactus PR #697: the packed weight cache builds from row-major or from the
+ * production INTERLEAVED_4ROW layout with identical bytes; follow-up on the
+ * orthogonal lm_head: rows in blocks of four, block nb at byte nb*2K, its
+ * bytes ordered by k-chunk so that every 128-wide k range of a block is one
+ * contiguous 256-byte sub-panel at nb*2K + g*256, and the per-row norms at
+ * [(nb*G + g)*4 + ni]).
+ *   chunk_k   weights per row in one k-chunk of a panel: 8, 16, 32, 64 or 128
+ *             (the pages do not state the width; every divisor of 128 from 8
+ *             up is accepted). K % chunk_k != 0: QMM_ERR_UNSUPPORTED_SHAPE.
+ *   panels    device, ceil(N/4)*2K bytes. Row n = 4*nb + ni, weights
+ *             k = c*chunk_k + 0..chunk_k-1 (c = k-chunk) are the chunk_k/2
+ *             bytes at nb*2K + c*2*chunk_k + ni*chunk_k/2, low nibble = even k,
+ *             nibble values as for qmm_pack_weights (indices for QMM_CQ4).
+ *   scales    device, ceil(N/4)*G*4 fp16: row n, group g at ((n/4)*G + g)*4 + n%4.
+ *   biases    device, the same layout; QMM_AFFINE only (NULL otherwise).
+ *   codebook  HOST pointer, 16 int8 levels; QMM_CQ4 only (NULL otherwise).
+ *   cb_scale  QMM_CQ4's codebook scale (finite); ignored otherwise.
+ *   packed    device, qmm_packed_size(w) bytes, written entirely.
+ * Rows of the last block beyond N are never read. Pointers must be 16-byte
+ * aligned (QMM_ERR_MISALIGNED).
+ */
+qmm_status qmm_pack_weights_interleaved4(const qmm_weight_desc* w, int32_t chunk_k, const uint8_t* panels,
+                                        const uint16_t* scales, const uint16_t* biases, const int8_t* codebook,
+                                        float cb_scale, void* packed, qmm_stream stream);
+
+/*
  * Activation prepass (device kernel, on `stream`).
  *
  * QMM_W4A8 and QMM_CQ4 (cactus PR #697, Summary: phase A rotates and quantizes

@@ -69,6 +69,7 @@ def _bind(path: str):
     L.oracle_pack.argtypes = [i, i, i, i, P, P, P, P]
     L.oracle_pack_from_values.argtypes = [i, i, i, i, P, P, P, P]
     L.oracle_unpack_blob.argtypes = [i, i, i, i, P, P, P, P]
+    L.oracle_interleaved4_to_rows.argtypes = [i, i, i, i, P, P, P, P, P, P]
     L.oracle_prep_w4a8.argtypes = [i, i, i, i, P, P, P, P]
     L.oracle_partials_w4a8.argtypes = [i, i, i, i, P, P, P]
     L.oracle_gemm_w4a8_rows.argtypes = [i, i, i, i, P, P, P, P, i, P, P, P]
@@ -149,6 +150,18 @@ class Oracle:
                                               _p(out)),
                "pack_from_values")
         return out
+
+    def interleaved4_to_rows(self, N, K, group, chunk_k, panels, pscales, pbiases=None):
+        """4-row panels -> (q_bytes [N][K/2], scales [N][G], biases [N][G] or None)."""
+        G = K // group
+        q = np.empty((N, K // 2), dtype=np.uint8)
+        s = np.empty((N, G), dtype=np.uint16)
+        b = np.empty((N, G), dtype=np.uint16) if pbiases is not None else None
+        _check(self.L.oracle_interleaved4_to_rows(N, K, group, chunk_k, _p(_c(panels, np.uint8)),
+                                                  _p(_c(pscales, np.uint16)),
+                                                  _p(None if pbiases is None else _c(pbiases, np.uint16)),
+                                                  _p(q), _p(s), _p(b)), "interleaved4_to_rows")
+        return q, s, b
 
     def unpack_blob(self, variant, N, K, group, blob):
         G = K // group

@@ -208,6 +208,43 @@ int oracle_pack(int variant, int N, int K, int group, const uint8_t* q_bytes,
     return rc;
 }
 
+/*
+ * 4-row panels -> the row-major input of oracle_pack, from the panel's index
+ * formula. [P1] Summary: the weight cache builds from row-major or from the
+ * production INTERLEAVED_4ROW layout with byte-identical output; follow-up on
+ * the orthogonal lm_head: rows come in blocks of four, block nb starting at
+ * byte nb*2K (four rows of K/2 bytes), the block's bytes ordered by k-chunk so
+ * that each 128-wide k range is one contiguous 256-byte sub-panel at
+ * nb*2K + g*256, and the per-row norms at [(nb*G + g)*4 + ni].
+ * The width of a k-chunk is not stated; it is the parameter chunk_k (8, 16,
+ * 32, 64 or 128 weights, dividing K): chunk c of block nb holds the four rows'
+ * chunk_k/2 bytes one row after the other. Row n = 4*nb + ni; rows of the last
+ * block at or beyond N are not read. biases / pbiases may both be NULL.
+ */
+int oracle_interleaved4_to_rows(int N, int K, int group, int chunk_k, const uint8_t* panels,
+                                const uint16_t* pscales, const uint16_t* pbiases, uint8_t* q_bytes,
+                                uint16_t* scales, uint16_t* biases)
+{
+    if (N < 1 || K < 2 || group < 1 || K % group) return 1;
+    if (chunk_k != 8 && chunk_k != 16 && chunk_k != 32 && chunk_k != 64 && chunk_k != 128) return 1;
+    if (K % chunk_k) return 1;
+    int G = K / group, cb = chunk_k / 2;
+    for (int n = 0; n < N; n++) {
+        int nb = n / 4, ni = n % 4;
+        const uint8_t* block = panels + (size_t)nb * 2 * K;
+        for (int c = 0; c < K / chunk_k; c++) {
+            const uint8_t* piece = block + (size_t)c * 4 * cb + (size_t)ni * cb;
+            for (int i = 0; i < cb; i++) q_bytes[(size_t)n * (K / 2) + (size_t)c * cb + i] = piece[i];
+        }
+        for (int g = 0; g < G; g++) {
+            size_t at = ((size_t)nb * G + g) * 4 + ni;
+            scales[(size_t)n * G + g] = pscales[at];
+            if (biases && pbiases) biases[(size_t)n * G + g] = pbiases[at];
+        }
+    }
+    return 0;
+}
+
 /* Inverse of the blob formula: recover values, scales and biases. */
 int oracle_unpack_blob(int variant, int N, int K, int group, const uint8_t* blob,
                        int8_t* q, uint16_t* scales, uint16_t* biases)

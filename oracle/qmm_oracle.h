@@ -34,6 +34,9 @@ int oracle_pack(int variant, int N, int K, int group, const uint8_t* q_bytes,
                 const uint16_t* scales, const uint16_t* biases, uint8_t* blob);
 int oracle_pack_from_values(int variant, int N, int K, int group, const int8_t* q_nk,
                             const uint16_t* scales, const uint16_t* biases, uint8_t* blob);
+int oracle_interleaved4_to_rows(int N, int K, int group, int chunk_k, const uint8_t* panels,
+                                const uint16_t* pscales, const uint16_t* pbiases, uint8_t* q_bytes,
+                                uint16_t* scales, uint16_t* biases);
 int oracle_unpack_blob(int variant, int N, int K, int group, const uint8_t* blob,
                        int8_t* q, uint16_t* scales, uint16_t* biases);
 

@@ -286,6 +286,63 @@ def pin_pack_roundtrip_and_invariance(orc):
         assert not qpad[N:].any() and not spad[N:].any()
 
 
+def pin_interleaved4_fixture(orc):
+    """Hand-worked 4-row panels (tests/golden/interleaved4_panels.txt)."""
+    for case in read_cases("interleaved4_panels.txt"):
+        N, K, group, ck = (int(case[k]) for k in ("N", "K", "group", "chunk_k"))
+        G = K // group
+        nblk = (N + 3) // 4
+        panels = np.arange(nblk * 2 * K, dtype=np.int64).astype(np.uint8)
+        pscales = np.arange(nblk * G * 4, dtype=np.uint16)
+        q, s, b = orc.interleaved4_to_rows(N, K, group, ck, panels, pscales, pscales)
+        for n in range(N):
+            left, _, right = case[f"row{n}"].partition("|")
+            assert list(q[n]) == [int(t, 16) for t in left.split()], (case["name"], n)
+            assert list(s[n]) == [int(t) for t in right.split()], (case["name"], n)
+            assert list(b[n]) == list(s[n])
+
+
+def pin_interleaved4_layout(orc):
+    """4-row panels against a numpy reshape/transpose of the row-major bytes
+    (every chunk width, N not a multiple of 4), and the page's statement that
+    each 128-wide k range of block nb is the 256-byte sub-panel at
+    nb*2K + g*256."""
+    rng = np.random.default_rng(11)
+    for N, K, group in ((8, 256, 64), (6, 384, 128), (13, 128, 64)):
+        G = K // group
+        nblk = (N + 3) // 4
+        q = rng.integers(0, 256, size=(nblk * 4, K // 2), dtype=np.uint8)
+        sc = rng.integers(0, 65536, size=(nblk * 4, G), dtype=np.uint16)
+        for ck in (8, 16, 32, 64, 128):
+            if K % ck:
+                continue
+            cb = ck // 2
+            panels = q.reshape(nblk, 4, K // ck, cb).transpose(0, 2, 1, 3).reshape(-1)
+            psc = sc.reshape(nblk, 4, G).transpose(0, 2, 1).reshape(-1)
+            q2, s2, _ = orc.interleaved4_to_rows(N, K, group, ck, panels, psc)
+            assert np.array_equal(q2, q[:N]), (N, K, ck)
+            assert np.array_equal(s2, sc[:N]), (N, K, ck)
+            # rows of the last block beyond N are never read
+            if N % 4:
+                junk = panels.copy().reshape(nblk, K // ck, 4, cb)
+                junk[-1, :, N % 4:, :] ^= 0x5A
+                q3, _, _ = orc.interleaved4_to_rows(N, K, group, ck, junk.reshape(-1), psc)
+                assert np.array_equal(q3, q[:N])
+            if K % 128 == 0 and 128 % ck == 0:
+                vng = K // 128
+                for nb in range(nblk):
+                    for g in range(vng):
+                        only = np.zeros_like(panels)
+                        at = (nb * vng + g) * 256
+                        assert at == nb * 2 * K + g * 256
+                        only[at:at + 256] = 0xFF
+                        Nf = nblk * 4
+                        q4, _, _ = orc.interleaved4_to_rows(Nf, K, group, ck, only, psc)
+                        rows, cols = np.nonzero(q4)
+                        assert set(rows) == set(range(4 * nb, 4 * nb + 4))
+                        assert set(cols) == set(range(64 * g, 64 * g + 64)) and len(rows) == 256
+
+
 # ----------------------------------------------------------------- W4A8 GEMM
 
 def _unpack(q_bytes, K, variant):
@@ -504,4 +561,5 @@ ALL_PINS = [
     pin_group_sum_tree_fixture, pin_group_sums_close_to_exact, pin_affine_dequant_and_bias,
     pin_cq4_identity_codebook_equals_w4a8, pin_cq4_partials_brute_force, pin_cq4_dequant_and_invariances,
     pin_cq4_blob_trailer_and_roundtrip,
+    pin_interleaved4_fixture, pin_interleaved4_layout,
 ]

@@ -97,6 +97,20 @@ def test_host_validation(q):
     assert L.qmm_gemv_workspace_size(D(c)) == L.qmm_gemv_workspace_size(D(d))
     mixv = (q.qmm_weight_desc * 2)(q.weight_desc(0, 256, 256, 64), q.weight_desc(2, 256, 256, 64))
     assert L.qmm_gemv_fused_siblings(2, mixv, ptrs, A, 0, 64, ptrs, None, None, None) == SHAPE
+    # 4-row panel input: chunk width, K divisible by it, per-variant pointers, alignment
+    il4 = L.qmm_pack_weights_interleaved4
+    aff = q.weight_desc(1, 256, 256, 64)
+    for bad in (0, 4, 24, 256):
+        assert il4(D(d), bad, A, A, None, None, 1.0, A, None) == INV
+    assert il4(D(q.weight_desc(0, 256, 320, 64)), 128, A, A, None, None, 1.0, A, None) == SHAPE
+    assert il4(D(d), 32, None, A, None, None, 1.0, A, None) == INV
+    assert il4(D(d), 32, A, A, A, None, 1.0, A, None) == INV          # biases on a symmetric desc
+    assert il4(D(aff), 32, A, A, None, None, 1.0, A, None) == INV     # affine needs biases
+    assert il4(D(d), 32, A, A, None, book, 1.0, A, None) == INV       # codebook on a W4A8 desc
+    assert il4(D(c), 32, A, A, None, None, 1.0, A, None) == INV       # CQ4 needs its codebook
+    assert il4(D(c), 32, A, A, None, book, float("nan"), A, None) == INV
+    assert il4(D(d), 32, A + 4, A, None, None, 1.0, A, None) == MIS
+    assert il4(D(aff), 32, A, A, A + 2, None, 1.0, A, None) == MIS
 
 
 def test_valid_arguments_reach_the_device_probe(q):
@@ -112,6 +126,8 @@ def test_valid_arguments_reach_the_device_probe(q):
     book = (ctypes.c_int8 * 16)(*range(-8, 8))
     assert L.qmm_pack_weights_cq4(ctypes.byref(c), A, book, 0.5, A, A, None) == 3
     assert L.qmm_gemm(ctypes.byref(c), A, 4, A, A, A, None) == 3
+    assert L.qmm_pack_weights_interleaved4(ctypes.byref(d), 8, A, A, None, None, 1.0, A, None) == 3
+    assert L.qmm_pack_weights_interleaved4(ctypes.byref(c), 128, A, A, None, book, 0.5, A, None) == 3
 
 
 def test_status_strings(q):

@@ -64,6 +64,13 @@ MUTANTS = [
      [P.pin_cq4_identity_codebook_equals_w4a8, P.pin_cq4_partials_brute_force]),
     ("cq4_trailer_scale_offset", "memcpy(tr + 16, &cb_scale, 4);", "memcpy(tr + 20, &cb_scale, 4);",
      [P.pin_cq4_blob_trailer_and_roundtrip]),
+    ("il4_rows_not_interleaved", "const uint8_t* piece = block + (size_t)c * 4 * cb + (size_t)ni * cb;",
+     "const uint8_t* piece = block + (size_t)ni * (K / 2) + (size_t)c * cb;",
+     [P.pin_interleaved4_fixture, P.pin_interleaved4_layout]),
+    ("il4_block_stride", "const uint8_t* block = panels + (size_t)nb * 2 * K;",
+     "const uint8_t* block = panels + (size_t)nb * K;", [P.pin_interleaved4_fixture, P.pin_interleaved4_layout]),
+    ("il4_norms_row_major", "size_t at = ((size_t)nb * G + g) * 4 + ni;", "size_t at = (size_t)n * G + g;",
+     [P.pin_interleaved4_fixture, P.pin_interleaved4_layout]),
     ("f16_round_truncate", "double q = rint(ldexp(a, 10 - E));", "double q = floor(ldexp(a, 10 - E));",
      [P.pin_f64_to_f16]),
 ]
