@@ -71,6 +71,7 @@ def _bind(path: str):
     L.oracle_unpack_blob.argtypes = [i, i, i, i, P, P, P, P]
     L.oracle_interleaved4_to_rows.argtypes = [i, i, i, i, P, P, P, P, P, P]
     L.oracle_prep_w4a8.argtypes = [i, i, i, i, P, P, P, P]
+    L.oracle_prep_rotated.argtypes = [i, i, i, P, P, P, P, P, P]
     L.oracle_partials_w4a8.argtypes = [i, i, i, i, P, P, P]
     L.oracle_gemm_w4a8_rows.argtypes = [i, i, i, i, P, P, P, P, i, P, P, P]
     L.oracle_group_sums_affine.argtypes = [i, i, i, P, P]
@@ -184,6 +185,20 @@ class Oracle:
         _check(self.L.oracle_prep_w4a8(M, K, group, hadamard, _p(x), _p(a), _p(sx), _p(asum)),
                "prep_w4a8")
         return a, sx, asum
+
+    def prep_rotated(self, R, x, group: int):
+        """(a int8 [M][K], sx float32 [M][G], asum int32 [M][G], z float32 [M][K])."""
+        x = _c(np.atleast_2d(x), np.float32)
+        R = _c(R, np.float32)
+        M, K = x.shape
+        G = K // group
+        a = np.empty((M, K), dtype=np.int8)
+        sx = np.empty((M, G), dtype=np.float32)
+        asum = np.empty((M, G), dtype=np.int32)
+        z = np.empty((M, K), dtype=np.float32)
+        _check(self.L.oracle_prep_rotated(M, K, group, _p(R), _p(x), _p(a), _p(sx), _p(asum), _p(z)),
+               "prep_rotated")
+        return a, sx, asum, z
 
     def partials_w4a8(self, q_bytes, a, group) -> np.ndarray:
         """P int32 [M][N][G]."""

@@ -328,6 +328,39 @@ int oracle_prep_w4a8(int M, int K, int group, int hadamard, const float* x,
     return 0;
 }
 
+/*
+ * Activation prepass with a full K x K orthogonal rotation ([P1] Summary: the
+ * orthogonal-rotation CQ4 lm_head runs on the same fused GEMV through an exact
+ * virtual 128-wide group view, the rotation applied in phase A; [P1]
+ * orthogonal embedding dequantization: the rotation is a K x K matvec with
+ * fp32 accumulation). For each row m:
+ *   1. z[i] = sum_k R[i][k] * x[m][k] in fp32: one fused multiply-add per
+ *      term, k = 0, 1, ..., K-1 in that order (the pages fix no order; this
+ *      is the plain one);
+ *   2. the per-group quantization of oracle_prep_w4a8 on z with no in-group
+ *      transform (R is orthonormal, so the scale carries no further factor).
+ * z_out (nullable) receives z [M][K].
+ */
+int oracle_prep_rotated(int M, int K, int group, const float* R, const float* x,
+                        int8_t* a, float* sx, int32_t* asum, float* z_out)
+{
+    if (M < 1 || K < 1 || group < 2 || K % group != 0) return 1;
+    float* z = malloc(sizeof(float) * (size_t)M * K);
+    if (!z) return 2;
+    for (int m = 0; m < M; m++)
+        for (int i = 0; i < K; i++) {
+            const float* Ri = R + (size_t)i * K;
+            const float* xm = x + (size_t)m * K;
+            float acc = 0.0f;
+            for (int k = 0; k < K; k++) acc = fmaf(Ri[k], xm[k], acc);
+            z[(size_t)m * K + i] = acc;
+        }
+    int rc = oracle_prep_w4a8(M, K, group, 0, z, a, sx, asum);
+    if (z_out) memcpy(z_out, z, sizeof(float) * (size_t)M * K);
+    free(z);
+    return rc;
+}
+
 /* ------------------------------------------------------------ W4A8 GEMM */
 
 /*

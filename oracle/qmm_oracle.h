@@ -42,6 +42,8 @@ int oracle_unpack_blob(int variant, int N, int K, int group, const uint8_t* blob
 
 int oracle_prep_w4a8(int M, int K, int group, int hadamard, const float* x,
                      int8_t* a, float* sx, int32_t* asum);
+int oracle_prep_rotated(int M, int K, int group, const float* R, const float* x,
+                        int8_t* a, float* sx, int32_t* asum, float* z_out);
 int oracle_partials_w4a8(int M, int N, int K, int group, const uint8_t* q_bytes,
                          const int8_t* a, int32_t* P);
 int oracle_gemm_w4a8(int M, int N, int K, int group, const uint8_t* q_bytes,

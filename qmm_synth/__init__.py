@@ -122,6 +122,15 @@ def normal(seed: int, stream: str, n: int) -> np.ndarray:
     return z[:n]
 
 
+def orthogonal_f32(seed: int, stream: str, K: int) -> np.ndarray:
+    """[K][K] float32 random orthogonal matrix: Q of the QR factorization of a
+    matrix of N(0,1) draws (signs fixed by diag(R) > 0), rounded to fp32."""
+    A = normal(seed, stream, K * K).reshape(K, K)
+    Q, Rm = np.linalg.qr(A)
+    Q = Q * np.where(np.diag(Rm) < 0, -1.0, 1.0)[None, :]
+    return Q.astype(np.float32)
+
+
 def activations_f32(seed: int, stream: str, M: int, K: int, outlier_frac: float = 0.0,
                     outlier_mag: float = 20.0) -> np.ndarray:
     """[M][K] float32 activations: N(0,1), plus optional outliers.

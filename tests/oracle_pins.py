@@ -343,6 +343,80 @@ def pin_interleaved4_layout(orc):
                         assert set(cols) == set(range(64 * g, 64 * g + 64)) and len(rows) == 256
 
 
+# ----------------------------------------------------------------- full-K rotation
+
+def _rotation_cases():
+    cases, cur = [], None
+    with open(os.path.join(GOLDEN, "rotation_order.txt")) as f:
+        for raw in f:
+            line = raw.strip()
+            if not line or line.startswith("#"):
+                continue
+            if line.startswith("case "):
+                cur = {"name": line.split()[1]}
+                cases.append(cur)
+                continue
+            key, _, val = line.partition("=")
+            cur[key.strip()] = [float(t) for t in val.split()]
+    out = []
+    for c in cases:
+        K, group = int(c["K"][0]), int(c["group"][0])
+        R = np.array([c[f"R{i}"] for i in range(K)], dtype=np.float64)
+        out.append((c["name"], K, group, R, np.array(c["x"]), np.array(c["z"])))
+    return out
+
+
+def pin_rotation_fixture(orc):
+    """Hand-worked z = R x: summation order, fused rounding, orientation
+    (tests/golden/rotation_order.txt); codes are the pinned quantization of z."""
+    for name, K, group, R, x, z in _rotation_cases():
+        assert np.array_equal(R.astype(np.float32).astype(np.float64), R), name   # exact fp32 inputs
+        a, sx, asum, z2 = orc.prep_rotated(R.astype(np.float32), x.astype(np.float32)[None], group)
+        assert np.array_equal(z2[0].astype(np.float64), z), (name, z2[0], z)
+        a0, sx0, asum0 = orc.prep_w4a8(z.astype(np.float32)[None], group, 0)
+        assert np.array_equal(a, a0) and np.array_equal(sx, sx0) and np.array_equal(asum, asum0), name
+
+
+def pin_rotation_properties(orc):
+    """Random orthogonal R (fp32): z within the fp32 dot-product error bound of
+    fp64 R x; identity R = no rotation; a signed permutation moves values
+    exactly (orientation R x, not R^T x); rotating both W (W R^T) and x leaves
+    W x unchanged within the bound; codes = the pinned quantization of z."""
+    u = 2.0 ** -24
+    for K, group, M in ((256, 64, 3), (384, 128, 2)):
+        R = qmm_synth.orthogonal_f32(0, f"pin/rot/{K}", K)
+        R64 = R.astype(np.float64)
+        assert np.allclose(R64 @ R64.T, np.eye(K), atol=1e-5)
+        x = qmm_synth.activations_f32(0, f"pin/rot/x/{K}", M, K, 0.01)
+        x64 = x.astype(np.float64)
+        a, sx, asum, z = orc.prep_rotated(R, x, group)
+        gam = K * u / (1 - K * u)
+        bound = gam * (np.abs(x64) @ np.abs(R64).T)
+        assert np.all(np.abs(z - x64 @ R64.T) <= bound)
+        a0, sx0, asum0 = orc.prep_w4a8(z, group, 0)
+        assert np.array_equal(a, a0) and np.array_equal(sx, sx0) and np.array_equal(asum, asum0)
+        # identity: the plain prepass without rotation
+        aI, sxI, asumI, zI = orc.prep_rotated(np.eye(K, dtype=np.float32), x, group)
+        aP, sxP, asumP = orc.prep_w4a8(x, group, 0)
+        assert np.array_equal(zI, x) and np.array_equal(aI, aP) and np.array_equal(sxI, sxP)
+        # signed permutation: z[i] = sign[i] * x[perm[i]] exactly
+        rng = np.random.default_rng(K)
+        perm = rng.permutation(K)
+        sign = rng.choice([-1.0, 1.0], size=K)
+        Pm = np.zeros((K, K), dtype=np.float32)
+        Pm[np.arange(K), perm] = sign
+        assert not np.array_equal(Pm, Pm.T)
+        _, _, _, zp = orc.prep_rotated(Pm, x, group)
+        assert np.array_equal(zp, (x[:, perm] * sign).astype(np.float32))
+        # W x == (W R^T)(R x) up to the rotation's rounding
+        W = qmm_synth.normal(0, f"pin/rot/W/{K}", 5 * K).reshape(5, K)
+        Wr = W @ R64.T
+        y0 = x64 @ W.T
+        y1 = z.astype(np.float64) @ Wr.T
+        tol = bound @ np.abs(Wr).T + 1e-9 * (np.abs(x64) @ np.abs(W).T)
+        assert np.all(np.abs(y1 - y0) <= tol)
+
+
 # ----------------------------------------------------------------- W4A8 GEMM
 
 def _unpack(q_bytes, K, variant):
@@ -562,4 +636,5 @@ ALL_PINS = [
     pin_cq4_identity_codebook_equals_w4a8, pin_cq4_partials_brute_force, pin_cq4_dequant_and_invariances,
     pin_cq4_blob_trailer_and_roundtrip,
     pin_interleaved4_fixture, pin_interleaved4_layout,
+    pin_rotation_fixture, pin_rotation_properties,
 ]

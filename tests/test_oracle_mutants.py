@@ -71,6 +71,15 @@ MUTANTS = [
      "const uint8_t* block = panels + (size_t)nb * K;", [P.pin_interleaved4_fixture, P.pin_interleaved4_layout]),
     ("il4_norms_row_major", "size_t at = ((size_t)nb * G + g) * 4 + ni;", "size_t at = (size_t)n * G + g;",
      [P.pin_interleaved4_fixture, P.pin_interleaved4_layout]),
+    ("rot_transposed", "for (int k = 0; k < K; k++) acc = fmaf(Ri[k], xm[k], acc);",
+     "for (int k = 0; k < K; k++) acc = fmaf(R[(size_t)k * K + i], xm[k], acc);",
+     [P.pin_rotation_fixture, P.pin_rotation_properties]),
+    ("rot_mul_then_add", "for (int k = 0; k < K; k++) acc = fmaf(Ri[k], xm[k], acc);",
+     "for (int k = 0; k < K; k++) acc = acc + Ri[k] * xm[k];", [P.pin_rotation_fixture]),
+    ("rot_reverse_order", "for (int k = 0; k < K; k++) acc = fmaf(Ri[k], xm[k], acc);",
+     "for (int k = K - 1; k >= 0; k--) acc = fmaf(Ri[k], xm[k], acc);", [P.pin_rotation_fixture]),
+    ("rot_skipped", "for (int k = 0; k < K; k++) acc = fmaf(Ri[k], xm[k], acc);",
+     "acc = xm[i] + 0.0f * Ri[0];", [P.pin_rotation_fixture, P.pin_rotation_properties]),
     ("f16_round_truncate", "double q = rint(ldexp(a, 10 - E));", "double q = floor(ldexp(a, 10 - E));",
      [P.pin_f64_to_f16]),
 ]

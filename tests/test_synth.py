@@ -59,3 +59,12 @@ def test_codebook_levels():
     assert np.array_equal(C, qmm_synth.codebook_i8(0, "cb"))
     C2, cb = qmm_synth.layer_codebook(1, "w")
     assert 0.04 <= cb <= 0.08 and float(np.float32(cb)) == cb
+
+
+def test_orthogonal_draw_is_seeded_and_orthogonal():
+    R = qmm_synth.orthogonal_f32(0, "t/orth", 128)
+    assert R.dtype == np.float32 and R.shape == (128, 128)
+    assert np.array_equal(R, qmm_synth.orthogonal_f32(0, "t/orth", 128))
+    assert not np.array_equal(R, qmm_synth.orthogonal_f32(1, "t/orth", 128))
+    R64 = R.astype(np.float64)
+    assert np.abs(R64 @ R64.T - np.eye(128)).max() < 1e-5
