@@ -44,7 +44,7 @@ import qmm_synth  # noqa: E402
 LAYERS = 32
 PROJ = [("gate_up", 12288, 1536), ("down", 1536, 6144), ("q", 2048, 1536), ("o", 1536, 2048)]
 GROUP = 64
-W4A8, AFFINE = 0, 1
+W4A8, AFFINE, CQ4 = 0, 1, 2
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "gemv_fused_w4a8_gemma_decode.txt")
 GEMV_SOURCE = os.path.join(ROOT, "bit_group_quantized_qmm_gb300", "csrc", "qmm_gemv_fused.cu")
 
@@ -516,6 +516,48 @@ def sweep(world):
             entry["gemv"] = {"us_per_call": t * 1e6, "weight_GBps": size / t / 1e9}
         res[str(M)] = entry
     out["lm_head"] = res
+    del pool
+
+    # orthogonal lm_head: full-K rotation prepass + CQ4 GEMV/GEMM on weights
+    # stored rotated, one norm per row viewed as 128-wide groups
+    N, K = 262144, 1536
+    lay = qmm_synth.Layer("lm_head_orth", CQ4, N, K, 128, 0)
+    idx, _, _ = qmm_synth.layer_weights(0, "lm_head_orth", lay)
+    C, cb = qmm_synth.layer_codebook(0, "lm_head_orth")
+    norms = qmm_synth.uniform_f16(0, "lm_head_orth/norms", (N, 1), 0.005, 0.02)
+    sw = np.ascontiguousarray(np.repeat(norms, K // 128, axis=1))
+    d = q.weight_desc(CQ4, N, K, 128)
+    size = q.qmm_packed_size(d)
+    first = torch.empty(size, dtype=torch.uint8, device=dev)
+    q.qmm_pack_weights_cq4(d, torch.from_numpy(idx).to(dev), C, cb, torch.from_numpy(sw.view(np.int16)).to(dev),
+                           first)
+    pool = [first] + [first.clone() for _ in range(max(1, math.ceil(pool_bytes / size)) - 1)]
+    R = torch.from_numpy(qmm_synth.orthogonal_f32(0, "lm_head_orth/R", K)).to(dev)
+    res = {}
+    for M in (1, 8):
+        x = torch.from_numpy(qmm_synth.layer_activations(0, f"lm_head_orth/x{M}", lay, M)).to(dev)
+        a = torch.empty((M, K), dtype=torch.int8, device=dev)
+        a16 = torch.empty((M, K), dtype=torch.float16, device=dev)
+        sxm = torch.empty((M, K // 128), dtype=torch.float32, device=dev)
+        Y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        ws1 = torch.zeros(max(16, q.qmm_gemv_workspace_size(d)), dtype=torch.uint8, device=dev)
+
+        def prep_only():
+            for _ in pool:
+                q.qmm_prep_act_rotated(M, K, 128, R, x, 0, a=a, a16=a16, sx=sxm)
+
+        def prep_and_matmul():
+            for p in pool:
+                q.qmm_prep_act_rotated(M, K, 128, R, x, 0, a=a, a16=a16, sx=sxm)
+                if M == 1:
+                    q.qmm_gemv(d, p, a, sxm, Y, ws1, ws1.numel())
+                else:
+                    q.qmm_gemm(d, p, M, a16, sxm, Y)
+        tp = timed(prep_only) / len(pool)
+        t = timed(prep_and_matmul) / len(pool)
+        res[str(M)] = {"prep_rotated_us": tp * 1e6, "us_per_call": t * 1e6, "weight_GBps": size / t / 1e9,
+                       "rotation_GBps": K * K * 4 / tp / 1e9}
+    out["lm_head_orth"] = res
     del pool
     torch.cuda.empty_cache()
     return out

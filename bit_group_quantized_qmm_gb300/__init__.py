@@ -24,7 +24,7 @@ QMM_DTYPE_F32, QMM_DTYPE_F16, QMM_DTYPE_BF16 = 0, 1, 2
 QMM_PATH_GEMV, QMM_PATH_GEMM = 0, 1
 KERNEL_IDS = {0: "none", 1: "pack", 2: "prep_w4a8", 3: "prep_affine", 4: "gemv_w4a8", 5: "gemm_w4a8",
               6: "gemm_affine", 7: "gemv_fused", 8: "gemm_rows", 9: "gemv_fused_siblings", 10: "gemv_cq4",
-              11: "gemm_cq4"}
+              11: "gemm_cq4", 12: "prep_rotated"}
 
 STATUS = {0: "QMM_OK", 1: "QMM_ERR_INVALID_ARG", 2: "QMM_ERR_UNSUPPORTED_SHAPE", 3: "QMM_ERR_UNSUPPORTED_DEVICE",
           4: "QMM_ERR_MISALIGNED", 5: "QMM_ERR_CUDA", 6: "QMM_ERR_TIMEOUT", 7: "QMM_ERR_WORKSPACE"}
@@ -53,6 +53,7 @@ def _load():
         "qmm_pack_weights_cq4": (I32, [D, P, P, ctypes.c_float, P, P, P]),
         "qmm_pack_weights_interleaved4": (I32, [D, I32, P, P, P, P, ctypes.c_float, P, P]),
         "qmm_prep_act": (I32, [I32, I32, I32, I32, I32, P, I32, P, P, P, P, P, P, P]),
+        "qmm_prep_act_rotated": (I32, [I32, I32, I32, P, P, I32, P, P, P, P, P]),
         "qmm_gemv_workspace_size": (SZ, [D]),
         "qmm_gemv": (I32, [D, P, P, P, P, P, SZ, P]),
         "qmm_gemv_static_scratch": (I32, [D, P, P, P, P, P]),
@@ -164,6 +165,11 @@ def qmm_prep_act(variant, M, K, group, hadamard, x, x_dtype, a=None, a16=None, s
                  x16=None, stream=None):
     _check(_L.qmm_prep_act(variant, M, K, group, hadamard, _ptr(x), x_dtype, _ptr(a), _ptr(a16), _ptr(sx),
                            _ptr(asum), _ptr(gsum), _ptr(x16), _stream(stream)), "qmm_prep_act")
+
+
+def qmm_prep_act_rotated(M, K, group, R, x, x_dtype, a=None, a16=None, sx=None, asum=None, stream=None):
+    _check(_L.qmm_prep_act_rotated(M, K, group, _ptr(R), _ptr(x), x_dtype, _ptr(a), _ptr(a16), _ptr(sx),
+                                   _ptr(asum), _stream(stream)), "qmm_prep_act_rotated")
 
 
 def qmm_gemv_workspace_size(desc) -> int:

@@ -140,6 +140,22 @@ bool act_tensor_map(CUtensorMap* map, const void* act16, int M, int K, int m_til
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 [K][K] rotation viewed as 32 floats x K rows x K/32 k-chunks (strides
+// 4 B, 4K B, 128 B), boxes of 32 x 16 rows x 16 chunks, 128-byte swizzle: one
+// box is 16 rows x 512 k laid out chunk by chunk; k beyond K reads zeros.
+bool rotation_tensor_map(CUtensorMap* map, const float* R, int K)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {32, (cuuint64_t)K, (cuuint64_t)(K / 32)};
+    cuuint64_t strides[2] = {(cuuint64_t)K * 4, 128};
+    cuuint32_t box[3] = {32, 16, 16};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(R), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Tile shape of the tensor-core GEMM for M activation rows.
 GemmShape gemm_shape(int M, int N, int K, bool a_in_smem)
 {
@@ -258,6 +274,25 @@ qmm_status qmm_prep_act(int32_t variant, int32_t M, int32_t K, int32_t group, in
         return launched(launch_prep_affine(c, M, K, x, x_dtype, gsum, x16), QMM_KERNEL_PREP_AFFINE);
     }
     return QMM_ERR_INVALID_ARG;
+}
+
+qmm_status qmm_prep_act_rotated(int32_t M, int32_t K, int32_t group, const float* R, const void* x,
+                                int32_t x_dtype, int8_t* a, uint16_t* a16, float* sx, int32_t* asum,
+                                qmm_stream stream)
+{
+    if (M < 1 || K < 1 || !R || !x || !sx) return QMM_ERR_INVALID_ARG;
+    if (x_dtype != QMM_DTYPE_F32 && x_dtype != QMM_DTYPE_F16 && x_dtype != QMM_DTYPE_BF16) return QMM_ERR_INVALID_ARG;
+    if (group != 64 && group != 128) return QMM_ERR_UNSUPPORTED_SHAPE;
+    if (K % 128 != 0) return QMM_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(R) || !aligned16(x) || !aligned16(sx) || (a && !aligned16(a)) || (a16 && !aligned16(a16)) ||
+        (asum && !aligned16(asum)))
+        return QMM_ERR_MISALIGNED;
+    qmm_status st;
+    LaunchCtx c;
+    if ((st = device_ctx(stream, &c)) != QMM_OK) return st;
+    CUtensorMap map;
+    if (!rotation_tensor_map(&map, R, K)) return QMM_ERR_CUDA;
+    return launched(launch_prep_rotated(c, map, M, K, group, x, x_dtype, a, a16, sx, asum), QMM_KERNEL_PREP_ROTATED);
 }
 
 size_t qmm_gemv_workspace_size(const qmm_weight_desc* w)

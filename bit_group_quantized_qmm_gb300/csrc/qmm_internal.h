@@ -51,6 +51,12 @@ cudaError_t launch_pack_il4(const LaunchCtx& c, int variant, int N, int K, int g
 cudaError_t launch_prep_w4a8(const LaunchCtx& c, int M, int K, int group, int hadamard, const void* x, int x_dtype,
                              int8_t* a, uint16_t* a16, float* sx, int32_t* asum);
 
+// Full-K rotation z = R x (fp32, ascending fused multiply-adds), then per-group
+// int8 quantization. K % 128 == 0, group 64 or 128.
+// r_map: qmm_abi's rotation_tensor_map of R.
+cudaError_t launch_prep_rotated(const LaunchCtx& c, const CUtensorMap& r_map, int M, int K, int group,
+                                const void* x, int x_dtype, int8_t* a, uint16_t* a16, float* sx, int32_t* asum);
+
 cudaError_t launch_prep_affine(const LaunchCtx& c, int M, int K, const void* x, int x_dtype, float* gsum,
                                uint16_t* x16);
 

@@ -428,4 +428,11 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr)
     return v;
 }
 
+__device__ __forceinline__ int ld_shared_cluster_s32(uint32_t addr)
+{
+    int v;
+    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 }  // namespace qmm

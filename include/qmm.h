@@ -104,7 +104,8 @@ typedef enum {
     QMM_KERNEL_GEMM_ROWS = 8,
     QMM_KERNEL_GEMV_FUSED_SIBLINGS = 9,
     QMM_KERNEL_GEMV_CQ4 = 10,
-    QMM_KERNEL_GEMM_CQ4 = 11
+    QMM_KERNEL_GEMM_CQ4 = 11,
+    QMM_KERNEL_PREP_ROTATED = 12
 } qmm_kernel_id;
 
 typedef void* qmm_stream; /* cudaStream_t */
@@ -251,6 +252,36 @@ qmm_status qmm_prep_act(int32_t variant, int32_t M, int32_t K, int32_t group, in
                         const void* x, int32_t x_dtype,
                         int8_t* a, uint16_t* a16, float* sx, int32_t* asum,
                         float* gsum, uint16_t* x16, qmm_stream stream);
+
+/*
+ * Activation prepass with a full K x K orthogonal rotation, for weights stored
+ * rotated (QMM_W4A8 and QMM_CQ4 codes; device kernel, on `stream`).
+ * cactus PR #697, Summary: the orthogonal-rotation CQ4 lm_head runs on the same
+ * fused GEMV through an exact virtual 128-wide group view, the rotation applied
+ * in phase A; "Orthogonal embedding dequantization": a K x K matvec with fp32
+ * accumulation. For each row m:
+ *   z[m][i] = sum_k R[i][k] * x[m][k], accumulated in fp32 with one fused
+ *             multiply-add per term, k = 0, 1, ..., K-1 in that order;
+ *   then per group g of z, as qmm_prep_act without an in-group transform:
+ *   amax, s = amax/127, a = clamp(rint(z/s), -127, 127), sx = s (R is
+ *   orthonormal: no further factor), asum = sum of a.
+ * Weights W stored as W' = W R^T (one norm per row, the single group of
+ * width K) are used through the virtual view: pack W' with group 128 (or 64)
+ * and the row's norm repeated in every group; then W x = W' z, computed by
+ * qmm_gemv / qmm_gemm on these codes.
+ *   M >= 1; K % 128 == 0 (QMM_ERR_UNSUPPORTED_SHAPE); group 64 or 128.
+ *   R      device, [K][K] fp32 row-major (a constant: it is read before the
+ *          dependency wait on the previous kernel).
+ *   x      device, [M][K] fp32 / fp16 / bf16 (x_dtype), widened exactly.
+ *   a      device, [M][K] int8 codes, or NULL.
+ *   a16    device, [M][K] fp16 image of the codes (the GEMM's operand), or NULL.
+ *   sx     device, [M][G] fp32 (required).
+ *   asum   device, [M][G] int32 code sums, or NULL.
+ * Pointers 16-byte aligned (QMM_ERR_MISALIGNED).
+ */
+qmm_status qmm_prep_act_rotated(int32_t M, int32_t K, int32_t group, const float* R, const void* x,
+                                int32_t x_dtype, int8_t* a, uint16_t* a16, float* sx, int32_t* asum,
+                                qmm_stream stream);
 
 /*
  * Bytes of workspace qmm_gemv wants for split-K over `w` (0 if none).

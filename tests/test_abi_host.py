@@ -97,6 +97,16 @@ def test_host_validation(q):
     assert L.qmm_gemv_workspace_size(D(c)) == L.qmm_gemv_workspace_size(D(d))
     mixv = (q.qmm_weight_desc * 2)(q.weight_desc(0, 256, 256, 64), q.weight_desc(2, 256, 256, 64))
     assert L.qmm_gemv_fused_siblings(2, mixv, ptrs, A, 0, 64, ptrs, None, None, None) == SHAPE
+    # full-K rotation prepass: shapes, required outputs, dtypes, alignment
+    rot = L.qmm_prep_act_rotated
+    assert rot(0, 256, 64, A, A, 0, A, A, A, A, None) == INV
+    assert rot(1, 256, 64, None, A, 0, A, A, A, A, None) == INV
+    assert rot(1, 256, 64, A, A, 0, A, A, None, A, None) == INV       # sx required
+    assert rot(1, 256, 64, A, A, 5, A, A, A, A, None) == INV
+    assert rot(1, 320, 64, A, A, 0, A, A, A, A, None) == SHAPE        # K % 128
+    assert rot(1, 256, 32, A, A, 0, A, A, A, A, None) == SHAPE
+    assert rot(1, 256, 64, A + 4, A, 0, A, A, A, A, None) == MIS
+    assert rot(1, 256, 64, A, A, 0, A, A + 2, A, A, None) == MIS
     # 4-row panel input: chunk width, K divisible by it, per-variant pointers, alignment
     il4 = L.qmm_pack_weights_interleaved4
     aff = q.weight_desc(1, 256, 256, 64)
@@ -127,6 +137,7 @@ def test_valid_arguments_reach_the_device_probe(q):
     assert L.qmm_pack_weights_cq4(ctypes.byref(c), A, book, 0.5, A, A, None) == 3
     assert L.qmm_gemm(ctypes.byref(c), A, 4, A, A, A, None) == 3
     assert L.qmm_pack_weights_interleaved4(ctypes.byref(d), 8, A, A, None, None, 1.0, A, None) == 3
+    assert L.qmm_prep_act_rotated(1, 1536, 128, A, A, 0, A, A, A, A, None) == 3
     assert L.qmm_pack_weights_interleaved4(ctypes.byref(c), 128, A, A, None, book, 0.5, A, None) == 3
 
 
