@@ -11,7 +11,7 @@ bytes streamed per second.
 The per-step weights (> 2x L2) are larger than L2, so no flush is needed.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--no-sweep]
-  python bench.py --profile-case prefill_gemm:1068     (a few GEMM launches, for ncu)
+  python bench.py --profile-case prefill_gemm:1068     (a few GEMM launches, for ncu; also prep_rotated:M)
 
 The step is captured once in a CUDA graph (the kernels are launched with
 programmatic dependent launch, so each GEMV streams its weights while the
@@ -61,7 +61,7 @@ def parse_args():
     p.add_argument("--no-sweep", action="store_true", help="skip the other workloads' extra figures")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
-    p.add_argument("--profile-case", default=None, metavar="prefill_gemm:M",
+    p.add_argument("--profile-case", default=None, metavar="prefill_gemm:M|prep_rotated:M",
                    help="run one prefill GEMM shape a few times and exit (for profilers; prints one JSON line)")
     return p.parse_args()
 
@@ -570,8 +570,29 @@ def profile_case(spec):
     import torch
     import bit_group_quantized_qmm_gb300 as q
     name, _, m = spec.partition(":")
-    if name != "prefill_gemm" or not m.isdigit():
-        raise SystemExit(f"unknown profile case {spec!r} (expected prefill_gemm:M)")
+    if name not in ("prefill_gemm", "prep_rotated") or not m.isdigit():
+        raise SystemExit(f"unknown profile case {spec!r} (expected prefill_gemm:M or prep_rotated:M)")
+    if name == "prep_rotated":
+        # full-K rotation prepass of the orthogonal lm_head (K = 1536, group 128)
+        M, K = int(m), 1536
+        dev = torch.device("cuda", torch.cuda.current_device())
+        R = torch.from_numpy(qmm_synth.orthogonal_f32(0, "lm_head_orth/R", K)).to(dev)
+        x = torch.from_numpy(qmm_synth.activations_f32(0, f"lm_head_orth/x{M}", M, K, 0.01)).to(dev)
+        a = torch.empty((M, K), dtype=torch.int8, device=dev)
+        sx = torch.empty((M, K // 128), dtype=torch.float32, device=dev)
+        for _ in range(2):
+            q.qmm_prep_act_rotated(M, K, 128, R, x, 0, a=a, sx=sx)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(3):
+            q.qmm_prep_act_rotated(M, K, 128, R, x, 0, a=a, sx=sx)
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / 3
+        print(json.dumps({"profile_case": spec, "us_per_call": us, "rotation_GBps": K * K * 4 / us / 1e3,
+                          "device_status": q.qmm_device_status()}))
+        return
     M, N, K, g = int(m), 12288, 1536, 64
     dev = torch.device("cuda", torch.cuda.current_device())
     lay = qmm_synth.Layer("prefill_gemm", W4A8, N, K, g, g)
