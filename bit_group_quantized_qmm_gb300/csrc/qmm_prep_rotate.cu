@@ -45,14 +45,20 @@ constexpr int kRotChunks = 16;                    // 32-wide k-chunks per stage
 constexpr int kRotCK = 32 * kRotChunks;           // k per stage
 constexpr int kRotStages = 3;
 constexpr int kRotRBytes = kRotChunks * kRotRows * 128;   // one TMA box
-constexpr int kRotXBytes = kRotMB * kRotCK * 4;           // room for fp32 x rows
-constexpr int kRotStageBytes = kRotRBytes + kRotXBytes;
-static_assert(kRotRBytes % 1024 == 0 && kRotStageBytes % 1024 == 0, "swizzle alignment");
+static_assert(kRotRBytes % 1024 == 0, "swizzle alignment");
 static_assert(kRotThreads == kRotRows * kRotMB, "one thread per (output, row)");
 
-constexpr size_t rot_smem_bytes()
+// A stage holds the R box and the x rows of the launch's row blocks (at most
+// kRotMB; fewer for small M, which leaves room for a second CTA per SM).
+inline int rot_stage_bytes(int M, int es)
 {
-    return 1024 + (size_t)kRotStages * kRotStageBytes + 8 * kRotStages + 2 * 4 * kRotMB + 16;
+    const int rows = M < kRotMB ? M : kRotMB;
+    return kRotRBytes + rows * kRotCK * es;   // a multiple of 1024: the next R box stays aligned
+}
+
+inline size_t rot_smem_bytes(int stage_bytes)
+{
+    return 1024 + (size_t)kRotStages * stage_bytes + 8 * kRotStages + 2 * 4 * kRotMB + 16;
 }
 
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, uint64_t* bar)
@@ -120,13 +126,14 @@ __global__ void __launch_bounds__(kRotThreads) prep_rotate_kernel(const __grid_c
                                                                   int K, const void* __restrict__ x,
                                                                   int8_t* __restrict__ a, __half* __restrict__ a16,
                                                                   float* __restrict__ sx,
-                                                                  int32_t* __restrict__ asum, int* status)
+                                                                  int32_t* __restrict__ asum, int stage_bytes,
+                                                                  int* status)
 {
     constexpr int ES = XDT == 0 ? 4 : 2;            // bytes per activation
     constexpr int CPG = GROUP / kRotRows;           // CTAs per quantization group (4 or 8)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)kRotStages * kRotStageBytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)kRotStages * stage_bytes);
     float* pamax = reinterpret_cast<float*>(full + kRotStages);   // [kRotMB] partial maxima
     int* psum = reinterpret_cast<int*>(pamax + kRotMB);            // [kRotMB] partial code sums
 
@@ -153,14 +160,14 @@ __global__ void __launch_bounds__(kRotThreads) prep_rotate_kernel(const __grid_c
     auto width = [&](int c) { return min(kRotCK, K - c * kRotCK); };
     // warp 0 fills stage c: lane 0 the R box, lanes 16.. the x rows
     auto issue_r = [&](int c) {
-        uint8_t* st = ring + (size_t)(c % kRotStages) * kRotStageBytes;
+        uint8_t* st = ring + (size_t)(c % kRotStages) * stage_bytes;
         if (lane == 0) {
             mbar_arrive_expect_tx(&full[c % kRotStages], (uint32_t)(kRotRBytes + mrows * width(c) * ES));
             tma_load_3d(st, &r_map, 0, i0, c * kRotChunks, &full[c % kRotStages]);
         }
     };
     auto issue_x = [&](int c) {
-        uint8_t* st = ring + (size_t)(c % kRotStages) * kRotStageBytes + kRotRBytes;
+        uint8_t* st = ring + (size_t)(c % kRotStages) * stage_bytes + kRotRBytes;
         const int j = lane - 16;
         if (j >= 0 && j < mrows)
             bulk_g2s(st + (size_t)j * kRotCK * ES,
@@ -178,6 +185,7 @@ __global__ void __launch_bounds__(kRotThreads) prep_rotate_kernel(const __grid_c
     }
 
     const bool active = 2 * warp < mrows;   // warp-uniform: some row of this warp is real
+    const int mx = mm < mrows ? mm : 0;      // rows past M read row 0 (the stage holds mrows rows)
     float acc = 0.f;
     int ok = 1;
     int consumed = 0;
@@ -193,14 +201,14 @@ __global__ void __launch_bounds__(kRotThreads) prep_rotate_kernel(const __grid_c
             issue_x(c - 1 + kRotStages);
         }
         if (active) {
-            const uint8_t* st = ring + (size_t)s * kRotStageBytes;
+            const uint8_t* st = ring + (size_t)s * stage_bytes;
             const int nj = width(c) / 32;   // 4, 8, 12 or 16 chunks
             float4 ra[8], xa[8], rb[8], xb[8];
-            load_chunk<XDT>(st, r, mm, 0, ra, xa);
+            load_chunk<XDT>(st, r, mx, 0, ra, xa);
             for (int j = 0; j < nj; j += 2) {   // nj is even
-                load_chunk<XDT>(st, r, mm, j + 1, rb, xb);
+                load_chunk<XDT>(st, r, mx, j + 1, rb, xb);
                 acc = fma_chunk(acc, ra, xa);
-                if (j + 2 < nj) load_chunk<XDT>(st, r, mm, j + 2, ra, xa);
+                if (j + 2 < nj) load_chunk<XDT>(st, r, mx, j + 2, ra, xa);
                 acc = fma_chunk(acc, rb, xb);
             }
         }
@@ -260,12 +268,13 @@ cudaError_t launch_rot_t(const LaunchCtx& c, const CUtensorMap& map, int M, int 
                          __half* a16, float* sx, int32_t* asum)
 {
     auto kern = prep_rotate_kernel<GROUP, XDT>;
-    const size_t smem = rot_smem_bytes();
-    static bool configured = false;
-    if (!configured) {
+    const int stage_bytes = rot_stage_bytes(M, XDT == 0 ? 4 : 2);
+    const size_t smem = rot_smem_bytes(stage_bytes);
+    static size_t configured = 0;
+    if (smem > configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        configured = true;
+        configured = smem;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(K / 128 * kRotCluster), (unsigned)((M + kRotMB - 1) / kRotMB));
@@ -286,7 +295,7 @@ cudaError_t launch_rot_t(const LaunchCtx& c, const CUtensorMap& map, int M, int 
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, kern, map, M, K, x, a, a16, sx, asum, c.status);
+    return cudaLaunchKernelEx(&cfg, kern, map, M, K, x, a, a16, sx, asum, stage_bytes, c.status);
 }
 
 template <int GROUP>
