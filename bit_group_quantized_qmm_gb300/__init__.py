@@ -65,6 +65,7 @@ def _load():
         "qmm_last_kernel_id": (I32, []),
         "qmm_device_status": (I32, [P, ctypes.POINTER(I32)]),
         "qmm_set_pdl": (None, [I32]),
+        "qmm_set_fault_injection": (None, [I32]),
         "qmm_set_gemm_weight_operand": (None, [I32]),
         "qmm_set_gemm_rows_max": (None, [I32]),
     }
@@ -231,6 +232,11 @@ def qmm_device_status(stream=None) -> int:
 
 def qmm_set_pdl(enable: bool):
     _L.qmm_set_pdl(1 if enable else 0)
+
+
+def qmm_set_fault_injection(point: int):
+    """Test-only: 1 makes the rotation prepass's bounded waits run out; 0 = off."""
+    _L.qmm_set_fault_injection(int(point))
 
 
 def qmm_set_gemm_weight_operand(in_shared_memory: bool):

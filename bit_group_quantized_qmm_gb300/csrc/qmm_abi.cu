@@ -33,6 +33,7 @@ DeviceInfo g_devices[kMaxDevices];
 thread_local int32_t g_last_kernel = QMM_KERNEL_NONE;
 int g_pdl = 1;
 int g_a_in_smem = 0;
+int g_fault = 0;   // test-only fault injection point (0: none)
 int g_rows_max = 8;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -292,7 +293,8 @@ qmm_status qmm_prep_act_rotated(int32_t M, int32_t K, int32_t group, const float
     if ((st = device_ctx(stream, &c)) != QMM_OK) return st;
     CUtensorMap map;
     if (!rotation_tensor_map(&map, R, K)) return QMM_ERR_CUDA;
-    return launched(launch_prep_rotated(c, map, M, K, group, x, x_dtype, a, a16, sx, asum), QMM_KERNEL_PREP_ROTATED);
+    return launched(launch_prep_rotated(c, map, M, K, group, x, x_dtype, a, a16, sx, asum, g_fault == 1),
+                    QMM_KERNEL_PREP_ROTATED);
 }
 
 size_t qmm_gemv_workspace_size(const qmm_weight_desc* w)
@@ -475,6 +477,8 @@ qmm_status qmm_device_status(qmm_stream stream, int32_t* flags)
 }
 
 void qmm_set_pdl(int32_t enable) { g_pdl = enable ? 1 : 0; }
+
+void qmm_set_fault_injection(int32_t point) { g_fault = point == 1 ? 1 : 0; }
 
 void qmm_set_gemm_weight_operand(int32_t in_shared_memory) { g_a_in_smem = in_shared_memory ? 1 : 0; }
 

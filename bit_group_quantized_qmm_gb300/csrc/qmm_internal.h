@@ -54,8 +54,11 @@ cudaError_t launch_prep_w4a8(const LaunchCtx& c, int M, int K, int group, int ha
 // Full-K rotation z = R x (fp32, ascending fused multiply-adds), then per-group
 // int8 quantization. K % 128 == 0, group 64 or 128.
 // r_map: qmm_abi's rotation_tensor_map of R.
+// skip_first_box: test-only fault injection (the first box of R is never
+// requested, so the kernel's bounded waits run out and it sets the timeout bit).
 cudaError_t launch_prep_rotated(const LaunchCtx& c, const CUtensorMap& r_map, int M, int K, int group,
-                                const void* x, int x_dtype, int8_t* a, uint16_t* a16, float* sx, int32_t* asum);
+                                const void* x, int x_dtype, int8_t* a, uint16_t* a16, float* sx, int32_t* asum,
+                                bool skip_first_box = false);
 
 cudaError_t launch_prep_affine(const LaunchCtx& c, int M, int K, const void* x, int x_dtype, float* gsum,
                                uint16_t* x16);

@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(kRotThreads) prep_rotate_kernel(const __grid_c
                                                                   int8_t* __restrict__ a, __half* __restrict__ a16,
                                                                   float* __restrict__ sx,
                                                                   int32_t* __restrict__ asum, int stage_bytes,
-                                                                  int* status)
+                                                                  int skip_first_box, int* status)
 {
     constexpr int ES = XDT == 0 ? 4 : 2;            // bytes per activation
     constexpr int CPG = GROUP / kRotRows;           // CTAs per quantization group (4 or 8)
@@ -163,7 +163,8 @@ __global__ void __launch_bounds__(kRotThreads) prep_rotate_kernel(const __grid_c
         uint8_t* st = ring + (size_t)(c % kRotStages) * stage_bytes;
         if (lane == 0) {
             mbar_arrive_expect_tx(&full[c % kRotStages], (uint32_t)(kRotRBytes + mrows * width(c) * ES));
-            tma_load_3d(st, &r_map, 0, i0, c * kRotChunks, &full[c % kRotStages]);
+            // fault injection (tests): the first box is expected but never requested
+            if (!(skip_first_box && c == 0)) tma_load_3d(st, &r_map, 0, i0, c * kRotChunks, &full[c % kRotStages]);
         }
     };
     auto issue_x = [&](int c) {
@@ -265,7 +266,7 @@ __global__ void __launch_bounds__(kRotThreads) prep_rotate_kernel(const __grid_c
 
 template <int GROUP, int XDT>
 cudaError_t launch_rot_t(const LaunchCtx& c, const CUtensorMap& map, int M, int K, const void* x, int8_t* a,
-                         __half* a16, float* sx, int32_t* asum)
+                         __half* a16, float* sx, int32_t* asum, int skip)
 {
     auto kern = prep_rotate_kernel<GROUP, XDT>;
     const int stage_bytes = rot_stage_bytes(M, XDT == 0 ? 4 : 2);
@@ -295,27 +296,29 @@ cudaError_t launch_rot_t(const LaunchCtx& c, const CUtensorMap& map, int M, int 
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, kern, map, M, K, x, a, a16, sx, asum, stage_bytes, c.status);
+    return cudaLaunchKernelEx(&cfg, kern, map, M, K, x, a, a16, sx, asum, stage_bytes, skip, c.status);
 }
 
 template <int GROUP>
 cudaError_t launch_rot_g(const LaunchCtx& c, const CUtensorMap& map, int M, int K, const void* x, int xdt,
-                         int8_t* a, __half* a16, float* sx, int32_t* asum)
+                         int8_t* a, __half* a16, float* sx, int32_t* asum, int skip)
 {
-    if (xdt == 0) return launch_rot_t<GROUP, 0>(c, map, M, K, x, a, a16, sx, asum);
-    if (xdt == 1) return launch_rot_t<GROUP, 1>(c, map, M, K, x, a, a16, sx, asum);
-    return launch_rot_t<GROUP, 2>(c, map, M, K, x, a, a16, sx, asum);
+    if (xdt == 0) return launch_rot_t<GROUP, 0>(c, map, M, K, x, a, a16, sx, asum, skip);
+    if (xdt == 1) return launch_rot_t<GROUP, 1>(c, map, M, K, x, a, a16, sx, asum, skip);
+    return launch_rot_t<GROUP, 2>(c, map, M, K, x, a, a16, sx, asum, skip);
 }
 
 }  // namespace
 
 cudaError_t launch_prep_rotated(const LaunchCtx& c, const CUtensorMap& r_map, int M, int K, int group,
-                                const void* x, int x_dtype, int8_t* a, uint16_t* a16, float* sx, int32_t* asum)
+                                const void* x, int x_dtype, int8_t* a, uint16_t* a16, float* sx, int32_t* asum,
+                                bool skip_first_box)
 {
     if (K % 128 != 0 || M < 1) return cudaErrorInvalidValue;
     __half* h = reinterpret_cast<__half*>(a16);
-    if (group == 64) return launch_rot_g<64>(c, r_map, M, K, x, x_dtype, a, h, sx, asum);
-    if (group == 128) return launch_rot_g<128>(c, r_map, M, K, x, x_dtype, a, h, sx, asum);
+    const int skip = skip_first_box ? 1 : 0;
+    if (group == 64) return launch_rot_g<64>(c, r_map, M, K, x, x_dtype, a, h, sx, asum, skip);
+    if (group == 128) return launch_rot_g<128>(c, r_map, M, K, x, x_dtype, a, h, sx, asum, skip);
     return cudaErrorInvalidValue;
 }
 

@@ -428,6 +428,17 @@ qmm_status qmm_device_status(qmm_stream stream, int32_t* flags);
  * launches made after the call (process-wide). */
 void qmm_set_pdl(int32_t enable);
 
+/*
+ * Test-only fault injection (process-wide; 0 = off, the default). Point 1: the
+ * next qmm_prep_act_rotated launches expect the first TMA box of R but never
+ * request it, so every CTA's bounded wait for it runs out (about 2 s), the
+ * kernel sets the timeout bit of the device error word and returns without
+ * writing its outputs; qmm_device_status then reports QMM_ERR_TIMEOUT and the
+ * context stays usable. Other values turn injection off. (The pages have no
+ * counterpart: it exercises the failure detection of the bounded waits.)
+ */
+void qmm_set_fault_injection(int32_t point);
+
 /* Where qmm_gemm expands the 4-bit weights for the tensor cores (process-wide,
  * launches after the call): 0 (default) into tensor memory, read by
  * tcgen05.mma as its A operand; 1 into 128-byte-swizzled shared memory. Both
