@@ -361,6 +361,17 @@ def test_gemm_output(torch_cuda, orc, M, N, K, group, had, operand_in_smem):
     assert ok, f"worst error / bound = {worst}"
 
 
+# Narrow tiles (at most 32 activation rows) over 305 row tiles, the last one
+# ragged: every persistent block runs two or three tiles; every output compared.
+WIDE_N = 305 * 128 - 72
+
+
+@pytest.mark.parametrize("M", [9, 17, 32])
+@pytest.mark.parametrize("operand_in_smem", [False, True])
+def test_gemm_many_tiles(torch_cuda, orc, M, operand_in_smem):
+    test_gemm_output(torch_cuda, orc, M, WIDE_N, 256, 64, 64, operand_in_smem)
+
+
 def _sample_rows(N, n=48):
     rows = np.unique(np.concatenate([[0, 1, 127, 128, N - 1], np.linspace(0, N - 1, n).astype(np.int64)]))
     return rows.astype(np.int32)
@@ -516,6 +527,11 @@ def test_affine_gemm_output(torch_cuda, orc, M, N, K, operand_in_smem):
     Y, Ym = orc.gemm_affine(qb, s, b, x16)
     ok, worst = gc.within_affine(Yg, Y, Ym)
     assert ok, f"worst error / bound = {worst}"
+
+
+@pytest.mark.parametrize("M", [9, 32])
+def test_affine_gemm_many_tiles(torch_cuda, orc, M):
+    test_affine_gemm_output(torch_cuda, orc, M, WIDE_N, 128, False)
 
 
 def test_affine_control_zero_sums_is_detected(torch_cuda, orc):

@@ -225,6 +225,12 @@ def test_gemm_output(torch_cuda, orc, M, N, K, group, had, operand_in_smem):
         assert np.array_equal(Yr.view(np.uint32), Yr2.view(np.uint32)), "not deterministic"
 
 
+@pytest.mark.parametrize("M", [9, 32])
+def test_gemm_many_tiles(torch_cuda, orc, M):
+    """Narrow tiles over 305 row tiles (several per persistent block)."""
+    test_gemm_output(torch_cuda, orc, M, 305 * 128 - 72, 256, 64, 64, False)
+
+
 def _sample_rows(N, n=48):
     rows = np.unique(np.concatenate([[0, 1, 127, 128, N - 1], np.linspace(0, N - 1, n).astype(np.int64)]))
     return rows.astype(np.int32)
