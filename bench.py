@@ -446,8 +446,14 @@ def sweep(world):
     def gemv_pool():
         for p in pool:
             q.qmm_gemv(d, p, a, sx, y, ws, ws.numel())
+
+    def fused_pool():   # quantization of x included
+        for p in pool:
+            q.qmm_gemv_fused(d, p, x[0], 0, 0, y)
     t = timed(gemv_pool) / len(pool)
-    out["gemv_k1024_n1024"] = {"us_per_call": t * 1e6, "weight_GBps": size / t / 1e9}
+    tf = timed(fused_pool) / len(pool)
+    out["gemv_k1024_n1024"] = {"us_per_call": t * 1e6, "weight_GBps": size / t / 1e9,
+                               "fused_us_per_call": tf * 1e6, "fused_weight_GBps": size / tf / 1e9}
     del pool
 
     # sibling GEMVs sharing x (q | k | v of one layer, K = 1536): one launch vs three
