@@ -36,7 +36,15 @@ template <int GROUP>
 struct GemvCfg {
     static constexpr int PP = GROUP / 32;                  // 16-byte pieces per row and group
     static constexpr int CB = 64 * GROUP + 256;            // chunk bytes (nibbles + scales)
-    static constexpr int RING = GROUP == 64 ? 12 : 6;      // stages (about 52 KB)
+    // stages (about 52 KB for group 64; group 128 keeps 34 KB so that more CTAs
+    // share an SM: measured 34.3 us against 35.0 with 6 on the lm_head GEMV)
+    static constexpr int RING = GROUP == 64 ? 12 : 4;
+    // The two compute halves take alternate groups, so stage i % RING must
+    // always be read by the same half: with an odd ring a stage's phases would
+    // alternate between the halves and a half running ahead could take a later
+    // phase of the same parity for its own (ring = ng when ng < RING has no
+    // stage reuse).
+    static_assert(RING % 2 == 0, "even ring");
 };
 
 // Signed bytes 16*q of the low / high nibble of each byte of w (offset-binary
