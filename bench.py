@@ -230,12 +230,15 @@ class DecodeModel:
         self.h2d_bytes = self.x.numel() * 4
         self.d2h_bytes = self.y.numel() * 4
 
-    def enqueue_step(self):
-        """One decode pass: one fused prepass + GEMV launch per projection."""
+    def enqueue_step(self, x_all=None, y_all=None):
+        """One decode pass: one fused prepass + GEMV launch per projection
+        (on the model's own x / y buffers unless others are given)."""
         q = self.q
+        x_all = self.x if x_all is None else x_all
+        y_all = self.y if y_all is None else y_all
         for p in self.projs:
-            x = self.x[p["x_off"]:p["x_off"] + p["K"]]
-            q.qmm_gemv_fused(p["d"], p["packed"], x, 0, GROUP, self.y[p["y_off"]:p["y_off"] + p["N"]])
+            x = x_all[p["x_off"]:p["x_off"] + p["K"]]
+            q.qmm_gemv_fused(p["d"], p["packed"], x, 0, GROUP, y_all[p["y_off"]:p["y_off"] + p["N"]])
 
     def enqueue_step_two_kernels(self):
         """The same pass through qmm_prep_act + qmm_gemv (two launches per projection)."""
@@ -688,15 +691,37 @@ def main():
     two_iters = max(10, min(args.steps, 2000))
     t_two = max_over_ranks(time_graph(g_two, two_iters, 3, world), world) / two_iters
 
-    # end to end: pinned host x in, graph, y out, every step
+    # end to end: every step copies its x in from pinned host memory and its y
+    # out to pinned host memory; two device buffer sets let the copies of one
+    # step overlap the launches of the neighbouring steps (h2d and d2h on
+    # their own streams, ordered by events)
+    xs = [model.x, model.x.clone()]
+    ys = [model.y, torch.empty_like(model.y)]
+    yh = [model.y_host, torch.empty_like(model.y_host).pin_memory()]
+    g_e2e = [g_step, capture(lambda: model.enqueue_step(xs[1], ys[1]))]
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    main = torch.cuda.current_stream()
+    ev = {k: [torch.cuda.Event(), torch.cuda.Event()] for k in ("in", "done", "out")}
     torch.cuda.synchronize()
     barrier(world)
     e2e_steps = max(10, min(args.steps, 2000))
     t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        model.x.copy_(model.x_host, non_blocking=True)
-        g_step.replay()
-        model.y_host.copy_(model.y, non_blocking=True)
+    for i in range(e2e_steps):
+        b = i & 1
+        if i >= 2:
+            h2d.wait_event(ev["done"][b])          # the graph two steps back has read x[b]
+        with torch.cuda.stream(h2d):
+            xs[b].copy_(model.x_host, non_blocking=True)
+            ev["in"][b].record(h2d)
+        main.wait_event(ev["in"][b])
+        if i >= 2:
+            main.wait_event(ev["out"][b])          # y[b] of two steps back is out
+        g_e2e[b].replay()
+        ev["done"][b].record(main)
+        d2h.wait_event(ev["done"][b])
+        with torch.cuda.stream(d2h):
+            yh[b].copy_(ys[b], non_blocking=True)
+            ev["out"][b].record(d2h)
     torch.cuda.synchronize()
     t_e2e = time.perf_counter() - t0
     barrier(world)
@@ -767,7 +792,9 @@ def main():
             },
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": model.h2d_bytes,
-                    "d2h_bytes_per_step": model.d2h_bytes, "steps": e2e_steps},
+                    "d2h_bytes_per_step": model.d2h_bytes, "steps": e2e_steps,
+                    "copies": "pinned host x in and y out every step, on their own streams, two device "
+                              "buffer sets: a step's copies overlap its neighbours' launches"},
             "gpu_launches": n_kernels_per_step * args.steps,
             "clocks": clocks,
             "device_status": status,
