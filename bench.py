@@ -594,7 +594,24 @@ def sweep(world):
     out["lm_head_orth"] = res
     del pool
     torch.cuda.empty_cache()
+    _add_fractions(out)
     return out
+
+
+def _add_fractions(node):
+    """Beside every figure of the sweep, its fraction of the measured peaks:
+    weight bytes per second over the copy bandwidth, TOPS / TFLOPS over the
+    dense bf16 rate (the rate of the kind::f16 MMAs the GEMM issues)."""
+    hbm, tflops, _ = measured_peaks()
+    if isinstance(node, dict):
+        for k in list(node):
+            v = node[k]
+            if k.endswith("weight_GBps"):
+                node[k.replace("weight_GBps", "frac_copy_bw")] = v / hbm
+            elif k in ("TOPS", "TFLOPS"):
+                node["frac_bf16_peak"] = v / tflops
+            else:
+                _add_fractions(v)
 
 
 def profile_case(spec):
