@@ -11,7 +11,7 @@ bytes streamed per second.
 The per-step weights (> 2x L2) are larger than L2, so no flush is needed.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--no-sweep]
-  python bench.py --profile-case prefill_gemm:1068     (a few GEMM launches, for ncu; also prep_rotated:M)
+  python bench.py --profile-case prefill_gemm:1068     (a few GEMM launches, for ncu; also prep_rotated:M, lm_head_gemv:1)
 
 The step is captured once in a CUDA graph (the kernels are launched with
 programmatic dependent launch, so each GEMV streams its weights while the
@@ -62,7 +62,7 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-cpu-all-cores", action="store_true", help="skip the all-core oracle figure")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
-    p.add_argument("--profile-case", default=None, metavar="prefill_gemm:M|prep_rotated:M",
+    p.add_argument("--profile-case", default=None, metavar="prefill_gemm:M|prep_rotated:M|lm_head_gemv:1",
                    help="run one prefill GEMM shape a few times and exit (for profilers; prints one JSON line)")
     return p.parse_args()
 
@@ -621,8 +621,36 @@ def profile_case(spec):
     import torch
     import bit_group_quantized_qmm_gb300 as q
     name, _, m = spec.partition(":")
-    if name not in ("prefill_gemm", "prep_rotated") or not m.isdigit():
-        raise SystemExit(f"unknown profile case {spec!r} (expected prefill_gemm:M or prep_rotated:M)")
+    if name not in ("prefill_gemm", "prep_rotated", "lm_head_gemv") or not m.isdigit():
+        raise SystemExit(f"unknown profile case {spec!r} (expected prefill_gemm:M, prep_rotated:M or lm_head_gemv:1)")
+    if name == "lm_head_gemv":
+        # the plain GEMV on prepared codes at lm_head size (K = 1536, N = 262144, group 128)
+        N, K, g = 262144, 1536, 128
+        dev = torch.device("cuda", torch.cuda.current_device())
+        lay = qmm_synth.Layer("lm_head", W4A8, N, K, g, g)
+        qb, sw, _ = qmm_synth.layer_weights(0, "lm_head", lay)
+        d = q.weight_desc(W4A8, N, K, g)
+        packed = torch.empty(q.qmm_packed_size(d), dtype=torch.uint8, device=dev)
+        q.qmm_pack_weights(d, torch.from_numpy(qb).to(dev), torch.from_numpy(sw.view(np.int16)).to(dev), None, packed)
+        x = torch.from_numpy(qmm_synth.layer_activations(0, "lm_head/x1", lay, 1)).to(dev)
+        a = torch.empty(K, dtype=torch.int8, device=dev)
+        sx = torch.empty(K // g, dtype=torch.float32, device=dev)
+        y = torch.empty(N, dtype=torch.float32, device=dev)
+        ws = torch.zeros(max(16, q.qmm_gemv_workspace_size(d)), dtype=torch.uint8, device=dev)
+        q.qmm_prep_act(W4A8, 1, K, g, g, x, 0, a=a, sx=sx)
+        for _ in range(2):
+            q.qmm_gemv(d, packed, a, sx, y, ws, ws.numel())
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(3):
+            q.qmm_gemv(d, packed, a, sx, y, ws, ws.numel())
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / 3
+        print(json.dumps({"profile_case": spec, "us_per_call": us, "weight_GBps": packed.numel() / us / 1e3,
+                          "device_status": q.qmm_device_status()}))
+        return
     if name == "prep_rotated":
         # full-K rotation prepass of the orthogonal lm_head (K = 1536, group 128)
         M, K = int(m), 1536
