@@ -25,6 +25,15 @@
 // workspace, no atomics. Codebook (CQ4) blobs take the same loop with each
 // piece's indices looked up in the matrix's 16 int8 levels, the codes staged
 // in the lookup's order and cb_scale applied once per output.
+//
+// Shapes with many row tiles (an lm_head: thousands of tiles) run a streaming
+// form instead: a grid of resident CTAs, each taking tiles t = blockIdx.x,
+// blockIdx.x + gridDim.x, ... over the whole of K. The codes of all K are
+// staged once per CTA, the producer streams the chunks of successive tiles
+// through two rings of stages (one per half of the compute threads: half h
+// takes one contiguous half of the groups of every tile), so a CTA pays its
+// set-up once and never waits for a tile's first bytes after the first.
+// The halves meet once per tile in shared memory; no K-split, no cluster.
 #include <cuda_fp16.h>
 
 #include "qmm.h"
@@ -276,6 +285,269 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+// ------------------------------------------------------------------ streaming form
+constexpr int kStreamMinTiles = 512;          // row tiles from which a launch streams
+constexpr int kStreamCodesMax = 64 * 1024;    // staged code bytes a CTA may hold (K x rows)
+
+template <int GROUP>
+struct StreamCfg {
+    static constexpr int PP = GROUP / 32;
+    static constexpr int CB = 64 * GROUP + 256;
+    static constexpr int RH = GROUP == 64 ? 6 : 3;   // stages per half (about 25 KB each)
+};
+
+// Header: the upper half's sums [2][MR][128] (double-buffered by tile), flags,
+// full and empty barriers of both rings; padded to 128 bytes.
+__host__ __device__ inline size_t stream_header_bytes(int mr, int rh)
+{
+    const size_t b = (size_t)2 * mr * 512 + 16 + (size_t)4 * rh * 8;
+    return (b + 127) / 128 * 128;
+}
+
+size_t stream_smem_bytes(int G, int mr, int group, int cb, int rh)
+{
+    return stream_header_bytes(mr, rh) + (size_t)2 * rh * cb + (size_t)G * mr * group + (size_t)G * mr * 4 + 16;
+}
+
+// Grid (P): CTA b takes row tiles b, b + P, ... with all G groups; compute
+// half h takes groups [h ? G0 : 0, h ? G : G0), G0 = ceil(G / 2), through its
+// own ring (stage i of half h is only ever read by half h).
+template <int GROUP, int MR, bool CQ>
+__global__ void __launch_bounds__(kThreads)
+    gemm_rows_stream_kernel(int M, int N, int K, const uint8_t* __restrict__ blob, const uint16_t* __restrict__ act16,
+                            const float* __restrict__ sx, float* __restrict__ Y, int* status)
+{
+    using C = StreamCfg<GROUP>;
+    constexpr int RH = C::RH;
+    const int G = K / GROUP, T = (N + 127) / 128, G0 = (G + 1) / 2;
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    float* red = reinterpret_cast<float*>(smem);                         // [2][MR][128]
+    int* flags = reinterpret_cast<int*>(red + 2 * MR * 128);              // [4]
+    uint64_t* full = reinterpret_cast<uint64_t*>(flags + 4);              // [2][RH]
+    uint64_t* empty = full + 2 * RH;                                      // [2][RH]
+    uint8_t* stages = smem + stream_header_bytes(MR, RH);                 // [2][RH][CB]
+    uint8_t* aperm = stages + (size_t)2 * RH * C::CB;                     // [G][MR][GROUP] codes, dp4a order
+    float* sxs = reinterpret_cast<float*>(aperm + (size_t)G * MR * GROUP);   // [G][MR]
+    volatile int* abort = flags;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    pdl_trigger();
+    if (tid == 0) {
+        for (int i = 0; i < 2 * RH; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 4);   // the 4 warps of one half read each stage
+        }
+        flags[0] = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kComputeThreads / 32) {
+        // producer: the chunks of both halves interleaved, tile after tile;
+        // weights do not depend on the previous kernel, so this starts before
+        // the dependency wait
+        if (lane == 0) {
+            // per half: chunks issued, next stage, parity of its next empty wait
+            uint32_t n0 = 0u, n1 = 0u, ph0 = 0u, ph1 = 0u;
+            int st0 = 0, st1 = 0;
+            bool stop = false;
+            auto issue = [&](int h, const uint8_t* src, uint32_t& n, int& st, uint32_t& ph) {
+                if (n >= (uint32_t)RH && !mbar_wait(&empty[h * RH + st], ph, status, abort)) {
+                    stop = true;
+                    return;
+                }
+                uint64_t* f = &full[h * RH + st];
+                mbar_arrive_expect_tx(f, C::CB);
+                bulk_g2s(stages + (size_t)(h * RH + st) * C::CB, src, C::CB, f);
+                ++n;
+                if (++st == RH) {
+                    st = 0;
+                    if (n > (uint32_t)RH) ph ^= 1u;
+                }
+            };
+            for (int t = blockIdx.x; t < T && !stop; t += gridDim.x) {
+                const uint8_t* tile = blob + (size_t)t * G * C::CB;
+                for (int i = 0; i < G0 && !stop; ++i) {
+                    issue(0, tile + (size_t)i * C::CB, n0, st0, ph0);
+                    if (!stop && G0 + i < G) issue(1, tile + (size_t)(G0 + i) * C::CB, n1, st1, ph1);
+                }
+            }
+            // the CTA must not exit with copies in flight: wait for the last ones
+            for (uint32_t c = n0 > (uint32_t)RH ? n0 - RH : 0u; c < n0; ++c)
+                mbar_wait(&full[c % RH], (c / RH) & 1u, status, nullptr);
+            for (uint32_t c = n1 > (uint32_t)RH ? n1 - RH : 0u; c < n1; ++c)
+                mbar_wait(&full[RH + c % RH], (c / RH) & 1u, status, nullptr);
+        }
+        __syncwarp();
+        return;
+    }
+
+    // ---------------------------------------------------------- stage codes (all of K)
+    Cq4Book book = {};
+    if (CQ) book = cq4_load(blob + cq4_trailer_offset(N, K, GROUP));
+    if (tid < M) bulk_prefetch_l2(act16 + (size_t)tid * K, (uint32_t)(K * 2));
+    pdl_wait();   // codes and scales come from the previous kernel
+    {
+        constexpr int B8 = GROUP / 8;   // 8-blocks per group
+        for (int w = tid; w < G * MR * B8; w += kComputeThreads) {
+            const int c8 = w % B8, rest = w / B8;
+            const int m = rest % MR, i = rest / MR;
+            uint2 perm = make_uint2(0u, 0u);
+            if (m < M) {
+                const uint4 hv =
+                    *reinterpret_cast<const uint4*>(act16 + (size_t)m * K + (size_t)i * GROUP + (size_t)c8 * 8);
+                const uint32_t b0 = code_byte((uint16_t)hv.x), b1 = code_byte((uint16_t)(hv.x >> 16));
+                const uint32_t b2 = code_byte((uint16_t)hv.y), b3 = code_byte((uint16_t)(hv.y >> 16));
+                const uint32_t b4 = code_byte((uint16_t)hv.z), b5 = code_byte((uint16_t)(hv.z >> 16));
+                const uint32_t b6 = code_byte((uint16_t)hv.w), b7 = code_byte((uint16_t)(hv.w >> 16));
+                if (CQ)   // lookup order of an 8-block: k = 0, 2, 4, 6 | 1, 3, 5, 7
+                    perm = make_uint2(b0 | (b2 << 8) | (b4 << 16) | (b6 << 24),
+                                      b1 | (b3 << 8) | (b5 << 16) | (b7 << 24));
+                else      // dp4a order of an 8-block: k = 0, 4, 1, 5 | 2, 6, 3, 7
+                    perm = make_uint2(b0 | (b4 << 8) | (b1 << 16) | (b5 << 24),
+                                      b2 | (b6 << 8) | (b3 << 16) | (b7 << 24));
+            }
+            *reinterpret_cast<uint2*>(aperm + ((size_t)i * MR + m) * GROUP + (size_t)c8 * 8) = perm;
+        }
+        for (int w = tid; w < G * MR; w += kComputeThreads) {
+            const int m = w % MR, i = w / MR;
+            sxs[w] = m < M ? sx[(size_t)m * G + i] : 0.f;
+        }
+    }
+    compute_sync();
+
+    // ---------------------------------------------------------- tiles
+    const int r = tid & 127, h = tid >> 7;
+    const int gb = h ? G0 : 0, nh = h ? G - G0 : G0;
+    uint64_t* fullh = full + h * RH;
+    uint64_t* emptyh = empty + h * RH;
+    const uint8_t* stagesh = stages + (size_t)h * RH * C::CB;
+    int st = 0;
+    uint32_t ph = 0u;
+    bool ok = true;
+    int lt = 0;
+    for (int t = blockIdx.x; t < T; t += gridDim.x, ++lt) {
+        float acc[MR];
+#pragma unroll
+        for (int m = 0; m < MR; ++m) acc[m] = 0.f;
+        // after a failed wait the loop still runs every tile's barrier (both
+        // halves must meet), with no further waits or stores
+        for (int i = 0; i < nh && ok; ++i) {
+            if (!mbar_wait(&fullh[st], ph, status, abort)) {
+                ok = false;
+                break;
+            }
+            const uint8_t* c = stagesh + (size_t)st * C::CB;
+            const int g = gb + i;
+            int wv[8 * C::PP];
+#pragma unroll
+            for (int p = 0; p < C::PP; ++p) {
+                const uint4 w = *reinterpret_cast<const uint4*>(c + p * 2048 + r * 16);
+                if (CQ) {
+                    uint32_t lo, hi;
+                    cq4_expand(book, w.x, lo, hi);
+                    wv[8 * p + 0] = (int)lo;
+                    wv[8 * p + 1] = (int)hi;
+                    cq4_expand(book, w.y, lo, hi);
+                    wv[8 * p + 2] = (int)lo;
+                    wv[8 * p + 3] = (int)hi;
+                    cq4_expand(book, w.z, lo, hi);
+                    wv[8 * p + 4] = (int)lo;
+                    wv[8 * p + 5] = (int)hi;
+                    cq4_expand(book, w.w, lo, hi);
+                    wv[8 * p + 6] = (int)lo;
+                    wv[8 * p + 7] = (int)hi;
+                } else {
+                    wv[8 * p + 0] = nib_lo16(w.x);
+                    wv[8 * p + 1] = nib_hi16(w.x);
+                    wv[8 * p + 2] = nib_lo16(w.y);
+                    wv[8 * p + 3] = nib_hi16(w.y);
+                    wv[8 * p + 4] = nib_lo16(w.z);
+                    wv[8 * p + 5] = nib_hi16(w.z);
+                    wv[8 * p + 6] = nib_lo16(w.w);
+                    wv[8 * p + 7] = nib_hi16(w.w);
+                }
+            }
+            const float sw = __half2float(reinterpret_cast<const __half*>(c + 64 * GROUP)[r]);
+            // the stage is free once the weights are in registers
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&emptyh[st]);
+            if (++st == RH) {
+                st = 0;
+                ph ^= 1u;
+            }
+            int dp[MR];
+#pragma unroll
+            for (int m = 0; m < MR; ++m) dp[m] = 0;
+            const uint4* ap = reinterpret_cast<const uint4*>(aperm + (size_t)g * MR * GROUP);
+#pragma unroll
+            for (int p = 0; p < C::PP; ++p) {
+#pragma unroll
+                for (int m = 0; m < MR; ++m) {
+                    const uint4 a0 = ap[m * (GROUP / 16) + 2 * p], a1 = ap[m * (GROUP / 16) + 2 * p + 1];
+                    dp[m] = __dp4a(wv[8 * p + 0], (int)a0.x, dp[m]);
+                    dp[m] = __dp4a(wv[8 * p + 1], (int)a0.y, dp[m]);
+                    dp[m] = __dp4a(wv[8 * p + 2], (int)a0.z, dp[m]);
+                    dp[m] = __dp4a(wv[8 * p + 3], (int)a0.w, dp[m]);
+                    dp[m] = __dp4a(wv[8 * p + 4], (int)a1.x, dp[m]);
+                    dp[m] = __dp4a(wv[8 * p + 5], (int)a1.y, dp[m]);
+                    dp[m] = __dp4a(wv[8 * p + 6], (int)a1.z, dp[m]);
+                    dp[m] = __dp4a(wv[8 * p + 7], (int)a1.w, dp[m]);
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < MR; ++m)
+                acc[m] = fmaf((float)(CQ ? dp[m] : dp[m] >> 4), sw * sxs[g * MR + m], acc[m]);
+        }
+        // the halves meet: the upper half parks its sums (buffer by tile
+        // parity, so a half one tile ahead never overwrites unread sums)
+        float* rb = red + (size_t)(lt & 1) * MR * 128;
+        if (h == 1) {
+#pragma unroll
+            for (int m = 0; m < MR; ++m) rb[m * 128 + r] = acc[m];
+        }
+        compute_sync();
+        if (h == 0 && ok) {
+            const int n = t * 128 + r;
+#pragma unroll
+            for (int m = 0; m < MR; ++m) {
+                const float v = acc[m] + rb[m * 128 + r];
+                if (m < M && n < N) Y[(size_t)m * N + n] = CQ ? v * book.scale : v;
+            }
+        }
+    }
+}
+
+template <int GROUP, int MR, bool CQ>
+cudaError_t run_stream(const LaunchCtx& c, int M, int N, int K, const uint8_t* blob, const uint16_t* act16,
+                       const float* sx, float* Y)
+{
+    using C = StreamCfg<GROUP>;
+    auto kern = gemm_rows_stream_kernel<GROUP, MR, CQ>;
+    const int T = (N + 127) / 128, G = K / GROUP;
+    const size_t smem = stream_smem_bytes(G, MR, GROUP, C::CB, C::RH);
+    static size_t configured = 0;
+    static int per_sm = 0;
+    cudaError_t e;
+    if (smem > configured) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        configured = smem;
+        per_sm = 0;
+    }
+    int nb = per_sm;
+    if (nb == 0) {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, kThreads, smem);
+        if (e != cudaSuccess) return e;
+        if (nb < 1) return cudaErrorNotSupported;
+        per_sm = nb;
+    }
+    const int P = T < nb * c.num_sms ? T : nb * c.num_sms;
+    return launch(kern, dim3(P), dim3(kThreads), smem, c, M, N, K, blob, act16, sx, Y, c.status);
+}
+
 template <int GROUP, int MR, bool CQ>
 cudaError_t run(const LaunchCtx& c, int M, int N, int K, const uint8_t* blob, const uint16_t* act16,
                 const float* sx, float* Y)
@@ -283,6 +555,8 @@ cudaError_t run(const LaunchCtx& c, int M, int N, int K, const uint8_t* blob, co
     using C = Cfg<GROUP, MR>;
     auto kern = gemm_rows_kernel<GROUP, MR, CQ>;
     const int T = (N + 127) / 128, G = K / GROUP;
+    if (T >= kStreamMinTiles && (size_t)K * MR <= (size_t)kStreamCodesMax)
+        return run_stream<GROUP, MR, CQ>(c, M, N, K, blob, act16, sx, Y);
     int ks = (kTargetCtas + T - 1) / T;
     const int ks_ng = (G + C::NG_CAP - 1) / C::NG_CAP;
     if (ks < ks_ng) ks = ks_ng;

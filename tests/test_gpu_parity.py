@@ -469,6 +469,39 @@ def test_gemm_rows_output(torch_cuda, orc, M, N, K, group, had):
         assert ok, f"{name}: worst error / bound = {worst}"
 
 
+# At least 512 row tiles run the dp4a kernel's streaming form: resident blocks
+# over successive tiles, all of K per block, one ring of stages per half of the
+# groups. 640 tiles, the last one ragged; odd group counts split unevenly
+# between the halves; every output compared.
+STREAM_N = 640 * 128 - 40
+STREAM_CASES = [
+    (1, 256, 64, 64),
+    (3, 192, 64, 0),       # 3 groups: halves of 2 and 1
+    (8, 384, 128, 128),    # 3 groups of 128
+    (16, 256, 64, 64),
+]
+
+
+@pytest.mark.parametrize("M,K,group,had", STREAM_CASES)
+def test_gemm_rows_stream_output(torch_cuda, orc, M, K, group, had):
+    q = gc.lib()
+    N = STREAM_N
+    qb, sw, x = gc.w4a8_case(15, f"rows_stream/{M}/{K}", N, K, group, had, M)
+    d, packed = gc.pack(W4A8, N, K, group, qb, sw)
+    _, a16, sx, _, _ = gc.prep_w4a8(x, group, had)
+    q.qmm_set_gemm_rows_max(16)
+    try:
+        Yr = gc.gemm(d, packed, M, a16, sx, kernel=8).cpu().numpy()
+        Yr2 = gc.gemm(d, packed, M, a16, sx, kernel=8).cpu().numpy()
+    finally:
+        q.qmm_set_gemm_rows_max(ROWS_DEFAULT)
+    assert np.array_equal(Yr.view(np.uint32), Yr2.view(np.uint32)), "not deterministic"
+    ra, rsx, _ = orc.prep_w4a8(x, group, had)
+    Y, Ym = orc.gemm_w4a8(qb, sw, ra, rsx, group)
+    ok, worst = gc.within_w4a8(Yr, Y, Ym)
+    assert ok, f"worst error / bound = {worst}"
+
+
 def test_gemm_rows_limit_and_fallback(torch_cuda, orc):
     """The rows limit picks the kernel; a K too long for one cluster of the
     dp4a kernel (193 groups of 64) falls back to the tensor cores."""

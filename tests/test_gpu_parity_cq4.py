@@ -231,6 +231,12 @@ def test_gemm_many_tiles(torch_cuda, orc, M):
     test_gemm_output(torch_cuda, orc, M, 305 * 128 - 72, 256, 64, 64, False)
 
 
+@pytest.mark.parametrize("M,K,group", [(4, 384, 128), (16, 256, 64)])
+def test_gemm_rows_stream(torch_cuda, orc, M, K, group):
+    """640 row tiles: the small-M kernel's streaming form (and the tensor cores)."""
+    test_gemm_output(torch_cuda, orc, M, 640 * 128 - 40, K, group, group, False)
+
+
 def _sample_rows(N, n=48):
     rows = np.unique(np.concatenate([[0, 1, 127, 128, N - 1], np.linspace(0, N - 1, n).astype(np.int64)]))
     return rows.astype(np.int32)
