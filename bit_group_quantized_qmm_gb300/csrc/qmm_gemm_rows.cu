@@ -289,55 +289,62 @@ __global__ void __launch_bounds__(kThreads)
 constexpr int kStreamMinTiles = 512;          // row tiles from which a launch streams
 constexpr int kStreamCodesMax = 64 * 1024;    // staged code bytes a CTA may hold (K x rows)
 
-template <int GROUP>
+// RPT weight rows per thread (r, r + 128 / RPT): each broadcast load of codes
+// from shared memory feeds 8 * RPT dp4a. The 256 compute threads form
+// NS = 2 * RPT group sets of 128 / RPT threads; set q takes groups
+// [G * q / NS, G * (q + 1) / NS) of every tile through its own ring of RS stages.
+template <int GROUP, int RPT>
 struct StreamCfg {
     static constexpr int PP = GROUP / 32;
     static constexpr int CB = 64 * GROUP + 256;
-    static constexpr int RH = GROUP == 64 ? 6 : 3;   // stages per half (about 25 KB each)
+    static constexpr int NS = 2 * RPT;                     // group sets
+    static constexpr int TPS = kComputeThreads / NS;       // threads per set
+    // stages per set: about 50 KB in all, at least two per set
+    static constexpr int RS = (GROUP == 64 ? 12 : 6) / NS < 2 ? 2 : (GROUP == 64 ? 12 : 6) / NS;
 };
 
-// Header: the upper half's sums [2][MR][128] (double-buffered by tile), flags,
-// full and empty barriers of both rings; padded to 128 bytes.
-__host__ __device__ inline size_t stream_header_bytes(int mr, int rh)
+// Header: the sums of sets 1 .. NS-1 [2][NS-1][MR][128] (double-buffered by
+// tile), flags, full and empty barriers of every ring; padded to 128 bytes.
+__host__ __device__ inline size_t stream_header_bytes(int mr, int ns, int rs)
 {
-    const size_t b = (size_t)2 * mr * 512 + 16 + (size_t)4 * rh * 8;
+    const size_t b = (size_t)2 * (ns - 1) * mr * 512 + 16 + (size_t)2 * ns * rs * 8;
     return (b + 127) / 128 * 128;
 }
 
-size_t stream_smem_bytes(int G, int mr, int group, int cb, int rh)
+size_t stream_smem_bytes(int G, int mr, int group, int cb, int ns, int rs)
 {
-    return stream_header_bytes(mr, rh) + (size_t)2 * rh * cb + (size_t)G * mr * group + (size_t)G * mr * 4 + 16;
+    return stream_header_bytes(mr, ns, rs) + (size_t)ns * rs * cb + (size_t)G * mr * group + (size_t)G * mr * 4 + 16;
 }
 
-// Grid (P): CTA b takes row tiles b, b + P, ... with all G groups; compute
-// half h takes groups [h ? G0 : 0, h ? G : G0), G0 = ceil(G / 2), through its
-// own ring (stage i of half h is only ever read by half h).
-template <int GROUP, int MR, bool CQ>
+// Grid (P): CTA b takes row tiles b, b + P, ... with all G groups; set q of
+// the compute threads reads only its own ring, so each ring has one consumer
+// set and the stage phases advance in order.
+template <int GROUP, int MR, int RPT, bool CQ>
 __global__ void __launch_bounds__(kThreads)
     gemm_rows_stream_kernel(int M, int N, int K, const uint8_t* __restrict__ blob, const uint16_t* __restrict__ act16,
                             const float* __restrict__ sx, float* __restrict__ Y, int* status)
 {
-    using C = StreamCfg<GROUP>;
-    constexpr int RH = C::RH;
-    const int G = K / GROUP, T = (N + 127) / 128, G0 = (G + 1) / 2;
+    using C = StreamCfg<GROUP, RPT>;
+    constexpr int NS = C::NS, RS = C::RS, RSTRIDE = 128 / RPT;
+    const int G = K / GROUP, T = (N + 127) / 128;
 
     extern __shared__ __align__(128) uint8_t smem[];
-    float* red = reinterpret_cast<float*>(smem);                         // [2][MR][128]
-    int* flags = reinterpret_cast<int*>(red + 2 * MR * 128);              // [4]
-    uint64_t* full = reinterpret_cast<uint64_t*>(flags + 4);              // [2][RH]
-    uint64_t* empty = full + 2 * RH;                                      // [2][RH]
-    uint8_t* stages = smem + stream_header_bytes(MR, RH);                 // [2][RH][CB]
-    uint8_t* aperm = stages + (size_t)2 * RH * C::CB;                     // [G][MR][GROUP] codes, dp4a order
-    float* sxs = reinterpret_cast<float*>(aperm + (size_t)G * MR * GROUP);   // [G][MR]
+    float* red = reinterpret_cast<float*>(smem);                              // [2][NS-1][MR][128]
+    int* flags = reinterpret_cast<int*>(red + 2 * (NS - 1) * MR * 128);        // [4]
+    uint64_t* full = reinterpret_cast<uint64_t*>(flags + 4);                   // [NS][RS]
+    uint64_t* empty = full + NS * RS;                                          // [NS][RS]
+    uint8_t* stages = smem + stream_header_bytes(MR, NS, RS);                  // [NS][RS][CB]
+    uint8_t* aperm = stages + (size_t)NS * RS * C::CB;                         // [G][MR][GROUP] codes, dp4a order
+    float* sxs = reinterpret_cast<float*>(aperm + (size_t)G * MR * GROUP);    // [G][MR]
     volatile int* abort = flags;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     pdl_trigger();
     if (tid == 0) {
-        for (int i = 0; i < 2 * RH; ++i) {
+        for (int i = 0; i < NS * RS; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 4);   // the 4 warps of one half read each stage
+            mbar_init(&empty[i], C::TPS / 32);   // the warps of one set read each stage
         }
         flags[0] = 0;
         fence_barrier_init();
@@ -345,40 +352,48 @@ __global__ void __launch_bounds__(kThreads)
     __syncthreads();
 
     if (warp == kComputeThreads / 32) {
-        // producer: the chunks of both halves interleaved, tile after tile;
+        // producer: the chunks of all sets interleaved, tile after tile;
         // weights do not depend on the previous kernel, so this starts before
         // the dependency wait
         if (lane == 0) {
-            // per half: chunks issued, next stage, parity of its next empty wait
-            uint32_t n0 = 0u, n1 = 0u, ph0 = 0u, ph1 = 0u;
-            int st0 = 0, st1 = 0;
+            // per ring: chunks issued, next stage, parity of its next empty wait
+            uint32_t n[NS], ph[NS];
+            int st[NS];
+#pragma unroll
+            for (int q = 0; q < NS; ++q) {
+                n[q] = 0u;
+                ph[q] = 0u;
+                st[q] = 0;
+            }
+            const int imax = (G + NS - 1) / NS;
             bool stop = false;
-            auto issue = [&](int h, const uint8_t* src, uint32_t& n, int& st, uint32_t& ph) {
-                if (n >= (uint32_t)RH && !mbar_wait(&empty[h * RH + st], ph, status, abort)) {
-                    stop = true;
-                    return;
-                }
-                uint64_t* f = &full[h * RH + st];
-                mbar_arrive_expect_tx(f, C::CB);
-                bulk_g2s(stages + (size_t)(h * RH + st) * C::CB, src, C::CB, f);
-                ++n;
-                if (++st == RH) {
-                    st = 0;
-                    if (n > (uint32_t)RH) ph ^= 1u;
-                }
-            };
             for (int t = blockIdx.x; t < T && !stop; t += gridDim.x) {
                 const uint8_t* tile = blob + (size_t)t * G * C::CB;
-                for (int i = 0; i < G0 && !stop; ++i) {
-                    issue(0, tile + (size_t)i * C::CB, n0, st0, ph0);
-                    if (!stop && G0 + i < G) issue(1, tile + (size_t)(G0 + i) * C::CB, n1, st1, ph1);
+                for (int i = 0; i < imax && !stop; ++i) {
+#pragma unroll
+                    for (int q = 0; q < NS; ++q) {
+                        const int ga = G * q / NS, gz = G * (q + 1) / NS;
+                        if (stop || ga + i >= gz) continue;
+                        if (n[q] >= (uint32_t)RS && !mbar_wait(&empty[q * RS + st[q]], ph[q], status, abort)) {
+                            stop = true;
+                            continue;
+                        }
+                        uint64_t* f = &full[q * RS + st[q]];
+                        mbar_arrive_expect_tx(f, C::CB);
+                        bulk_g2s(stages + (size_t)(q * RS + st[q]) * C::CB, tile + (size_t)(ga + i) * C::CB, C::CB, f);
+                        ++n[q];
+                        if (++st[q] == RS) {
+                            st[q] = 0;
+                            if (n[q] > (uint32_t)RS) ph[q] ^= 1u;
+                        }
+                    }
                 }
             }
             // the CTA must not exit with copies in flight: wait for the last ones
-            for (uint32_t c = n0 > (uint32_t)RH ? n0 - RH : 0u; c < n0; ++c)
-                mbar_wait(&full[c % RH], (c / RH) & 1u, status, nullptr);
-            for (uint32_t c = n1 > (uint32_t)RH ? n1 - RH : 0u; c < n1; ++c)
-                mbar_wait(&full[RH + c % RH], (c / RH) & 1u, status, nullptr);
+#pragma unroll
+            for (int q = 0; q < NS; ++q)
+                for (uint32_t c = n[q] > (uint32_t)RS ? n[q] - RS : 0u; c < n[q]; ++c)
+                    mbar_wait(&full[q * RS + c % RS], (c / RS) & 1u, status, nullptr);
         }
         __syncwarp();
         return;
@@ -419,115 +434,150 @@ __global__ void __launch_bounds__(kThreads)
     compute_sync();
 
     // ---------------------------------------------------------- tiles
-    const int r = tid & 127, h = tid >> 7;
-    const int gb = h ? G0 : 0, nh = h ? G - G0 : G0;
-    uint64_t* fullh = full + h * RH;
-    uint64_t* emptyh = empty + h * RH;
-    const uint8_t* stagesh = stages + (size_t)h * RH * C::CB;
+    const int q = tid / C::TPS, r = tid % C::TPS;   // set, first weight row
+    const int ga = G * q / NS, nq = G * (q + 1) / NS - ga;
+    uint64_t* fullq = full + q * RS;
+    uint64_t* emptyq = empty + q * RS;
+    const uint8_t* stagesq = stages + (size_t)q * RS * C::CB;
     int st = 0;
     uint32_t ph = 0u;
     bool ok = true;
     int lt = 0;
     for (int t = blockIdx.x; t < T; t += gridDim.x, ++lt) {
-        float acc[MR];
+        float acc[RPT][MR];
 #pragma unroll
-        for (int m = 0; m < MR; ++m) acc[m] = 0.f;
-        // after a failed wait the loop still runs every tile's barrier (both
-        // halves must meet), with no further waits or stores
-        for (int i = 0; i < nh && ok; ++i) {
-            if (!mbar_wait(&fullh[st], ph, status, abort)) {
+        for (int rr = 0; rr < RPT; ++rr)
+#pragma unroll
+            for (int m = 0; m < MR; ++m) acc[rr][m] = 0.f;
+        // after a failed wait the loop still runs every tile's barrier (all
+        // sets must meet), with no further waits or stores
+        for (int i = 0; i < nq && ok; ++i) {
+            if (!mbar_wait(&fullq[st], ph, status, abort)) {
                 ok = false;
                 break;
             }
-            const uint8_t* c = stagesh + (size_t)st * C::CB;
-            const int g = gb + i;
-            int wv[8 * C::PP];
+            const uint8_t* c = stagesq + (size_t)st * C::CB;
+            const int g = ga + i;
+            float sw[RPT];
 #pragma unroll
-            for (int p = 0; p < C::PP; ++p) {
-                const uint4 w = *reinterpret_cast<const uint4*>(c + p * 2048 + r * 16);
-                if (CQ) {
-                    uint32_t lo, hi;
-                    cq4_expand(book, w.x, lo, hi);
-                    wv[8 * p + 0] = (int)lo;
-                    wv[8 * p + 1] = (int)hi;
-                    cq4_expand(book, w.y, lo, hi);
-                    wv[8 * p + 2] = (int)lo;
-                    wv[8 * p + 3] = (int)hi;
-                    cq4_expand(book, w.z, lo, hi);
-                    wv[8 * p + 4] = (int)lo;
-                    wv[8 * p + 5] = (int)hi;
-                    cq4_expand(book, w.w, lo, hi);
-                    wv[8 * p + 6] = (int)lo;
-                    wv[8 * p + 7] = (int)hi;
-                } else {
-                    wv[8 * p + 0] = nib_lo16(w.x);
-                    wv[8 * p + 1] = nib_hi16(w.x);
-                    wv[8 * p + 2] = nib_lo16(w.y);
-                    wv[8 * p + 3] = nib_hi16(w.y);
-                    wv[8 * p + 4] = nib_lo16(w.z);
-                    wv[8 * p + 5] = nib_hi16(w.z);
-                    wv[8 * p + 6] = nib_lo16(w.w);
-                    wv[8 * p + 7] = nib_hi16(w.w);
-                }
-            }
-            const float sw = __half2float(reinterpret_cast<const __half*>(c + 64 * GROUP)[r]);
-            // the stage is free once the weights are in registers
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&emptyh[st]);
-            if (++st == RH) {
-                st = 0;
-                ph ^= 1u;
-            }
-            int dp[MR];
+            for (int rr = 0; rr < RPT; ++rr)
+                sw[rr] = __half2float(reinterpret_cast<const __half*>(c + 64 * GROUP)[r + RSTRIDE * rr]);
+            int dp[RPT][MR];
 #pragma unroll
-            for (int m = 0; m < MR; ++m) dp[m] = 0;
+            for (int rr = 0; rr < RPT; ++rr)
+#pragma unroll
+                for (int m = 0; m < MR; ++m) dp[rr][m] = 0;
             const uint4* ap = reinterpret_cast<const uint4*>(aperm + (size_t)g * MR * GROUP);
 #pragma unroll
             for (int p = 0; p < C::PP; ++p) {
+                // the rows' 32 weights of this piece as bytes: 16 * q in the
+                // blob's slot order (symmetric) or the looked-up levels (codebook)
+                int wv[RPT][8];
+#pragma unroll
+                for (int rr = 0; rr < RPT; ++rr) {
+                    const uint4 w = *reinterpret_cast<const uint4*>(c + p * 2048 + (r + RSTRIDE * rr) * 16);
+                    if (CQ) {
+                        uint32_t lo, hi;
+                        cq4_expand(book, w.x, lo, hi);
+                        wv[rr][0] = (int)lo;
+                        wv[rr][1] = (int)hi;
+                        cq4_expand(book, w.y, lo, hi);
+                        wv[rr][2] = (int)lo;
+                        wv[rr][3] = (int)hi;
+                        cq4_expand(book, w.z, lo, hi);
+                        wv[rr][4] = (int)lo;
+                        wv[rr][5] = (int)hi;
+                        cq4_expand(book, w.w, lo, hi);
+                        wv[rr][6] = (int)lo;
+                        wv[rr][7] = (int)hi;
+                    } else {
+                        wv[rr][0] = nib_lo16(w.x);
+                        wv[rr][1] = nib_hi16(w.x);
+                        wv[rr][2] = nib_lo16(w.y);
+                        wv[rr][3] = nib_hi16(w.y);
+                        wv[rr][4] = nib_lo16(w.z);
+                        wv[rr][5] = nib_hi16(w.z);
+                        wv[rr][6] = nib_lo16(w.w);
+                        wv[rr][7] = nib_hi16(w.w);
+                    }
+                }
+                if (p == C::PP - 1) {
+                    // every byte of the stage is in registers: release it
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&emptyq[st]);
+                }
 #pragma unroll
                 for (int m = 0; m < MR; ++m) {
                     const uint4 a0 = ap[m * (GROUP / 16) + 2 * p], a1 = ap[m * (GROUP / 16) + 2 * p + 1];
-                    dp[m] = __dp4a(wv[8 * p + 0], (int)a0.x, dp[m]);
-                    dp[m] = __dp4a(wv[8 * p + 1], (int)a0.y, dp[m]);
-                    dp[m] = __dp4a(wv[8 * p + 2], (int)a0.z, dp[m]);
-                    dp[m] = __dp4a(wv[8 * p + 3], (int)a0.w, dp[m]);
-                    dp[m] = __dp4a(wv[8 * p + 4], (int)a1.x, dp[m]);
-                    dp[m] = __dp4a(wv[8 * p + 5], (int)a1.y, dp[m]);
-                    dp[m] = __dp4a(wv[8 * p + 6], (int)a1.z, dp[m]);
-                    dp[m] = __dp4a(wv[8 * p + 7], (int)a1.w, dp[m]);
+#pragma unroll
+                    for (int rr = 0; rr < RPT; ++rr) {
+                        dp[rr][m] = __dp4a(wv[rr][0], (int)a0.x, dp[rr][m]);
+                        dp[rr][m] = __dp4a(wv[rr][1], (int)a0.y, dp[rr][m]);
+                        dp[rr][m] = __dp4a(wv[rr][2], (int)a0.z, dp[rr][m]);
+                        dp[rr][m] = __dp4a(wv[rr][3], (int)a0.w, dp[rr][m]);
+                        dp[rr][m] = __dp4a(wv[rr][4], (int)a1.x, dp[rr][m]);
+                        dp[rr][m] = __dp4a(wv[rr][5], (int)a1.y, dp[rr][m]);
+                        dp[rr][m] = __dp4a(wv[rr][6], (int)a1.z, dp[rr][m]);
+                        dp[rr][m] = __dp4a(wv[rr][7], (int)a1.w, dp[rr][m]);
+                    }
                 }
             }
+            if (++st == RS) {
+                st = 0;
+                ph ^= 1u;
+            }
 #pragma unroll
-            for (int m = 0; m < MR; ++m)
-                acc[m] = fmaf((float)(CQ ? dp[m] : dp[m] >> 4), sw * sxs[g * MR + m], acc[m]);
+            for (int rr = 0; rr < RPT; ++rr)
+#pragma unroll
+                for (int m = 0; m < MR; ++m)
+                    acc[rr][m] = fmaf((float)(CQ ? dp[rr][m] : dp[rr][m] >> 4), sw[rr] * sxs[g * MR + m], acc[rr][m]);
         }
-        // the halves meet: the upper half parks its sums (buffer by tile
-        // parity, so a half one tile ahead never overwrites unread sums)
-        float* rb = red + (size_t)(lt & 1) * MR * 128;
-        if (h == 1) {
+        // the sets meet: sets 1 .. NS-1 park their sums (buffer by tile parity,
+        // so a set one tile ahead never overwrites unread sums), set 0 adds
+        // them in set order and stores
+        float* rb = red + (size_t)(lt & 1) * (NS - 1) * MR * 128;
+        if (q > 0) {
 #pragma unroll
-            for (int m = 0; m < MR; ++m) rb[m * 128 + r] = acc[m];
+            for (int rr = 0; rr < RPT; ++rr)
+#pragma unroll
+                for (int m = 0; m < MR; ++m) rb[((size_t)(q - 1) * MR + m) * 128 + r + RSTRIDE * rr] = acc[rr][m];
         }
         compute_sync();
-        if (h == 0 && ok) {
-            const int n = t * 128 + r;
+        if (q == 0 && ok) {
 #pragma unroll
-            for (int m = 0; m < MR; ++m) {
-                const float v = acc[m] + rb[m * 128 + r];
-                if (m < M && n < N) Y[(size_t)m * N + n] = CQ ? v * book.scale : v;
+            for (int rr = 0; rr < RPT; ++rr) {
+                const int row = r + RSTRIDE * rr, n = t * 128 + row;
+#pragma unroll
+                for (int m = 0; m < MR; ++m) {
+                    float v = acc[rr][m];
+#pragma unroll
+                    for (int k = 0; k < NS - 1; ++k) v += rb[((size_t)k * MR + m) * 128 + row];
+                    if (m < M && n < N) Y[(size_t)m * N + n] = CQ ? v * book.scale : v;
+                }
             }
         }
     }
+}
+
+// Two weight rows per thread from 4 activation rows up: with one, the code
+// loads keep the shared-memory pipe about as busy as the dp4a pipe (measured
+// on the lm_head shape, M = 8: 68.8 -> 65.0 us; M = 16: 124 -> 119 us). One
+// row for M <= 2, where the weight stream is the limit.
+template <int MR>
+constexpr int stream_rpt()
+{
+    return MR >= 4 ? 2 : 1;
 }
 
 template <int GROUP, int MR, bool CQ>
 cudaError_t run_stream(const LaunchCtx& c, int M, int N, int K, const uint8_t* blob, const uint16_t* act16,
                        const float* sx, float* Y)
 {
-    using C = StreamCfg<GROUP>;
-    auto kern = gemm_rows_stream_kernel<GROUP, MR, CQ>;
+    constexpr int RPT = stream_rpt<MR>();
+    using C = StreamCfg<GROUP, RPT>;
+    auto kern = gemm_rows_stream_kernel<GROUP, MR, RPT, CQ>;
     const int T = (N + 127) / 128, G = K / GROUP;
-    const size_t smem = stream_smem_bytes(G, MR, GROUP, C::CB, C::RH);
+    const size_t smem = stream_smem_bytes(G, MR, GROUP, C::CB, C::NS, C::RS);
     static size_t configured = 0;
     static int per_sm = 0;
     cudaError_t e;
