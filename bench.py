@@ -11,7 +11,8 @@ bytes streamed per second.
 The per-step weights (> 2x L2) are larger than L2, so no flush is needed.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--no-sweep]
-  python bench.py --profile-case prefill_gemm:1068     (a few GEMM launches, for ncu; also prep_rotated:M, lm_head_gemv:1)
+  python bench.py --profile-case prefill_gemm:1068     (a few GEMM launches, for ncu; also prep_rotated:M,
+                                                        lm_head_gemv:1, lm_head_gemm:M)
 
 The step is captured once in a CUDA graph (the kernels are launched with
 programmatic dependent launch, so each GEMV streams its weights while the
@@ -62,7 +63,7 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-cpu-all-cores", action="store_true", help="skip the all-core oracle figure")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
-    p.add_argument("--profile-case", default=None, metavar="prefill_gemm:M|prep_rotated:M|lm_head_gemv:1",
+    p.add_argument("--profile-case", default=None, metavar="prefill_gemm:M|prep_rotated:M|lm_head_gemv:1|lm_head_gemm:M",
                    help="run one prefill GEMM shape a few times and exit (for profilers; prints one JSON line)")
     return p.parse_args()
 
@@ -621,8 +622,37 @@ def profile_case(spec):
     import torch
     import bit_group_quantized_qmm_gb300 as q
     name, _, m = spec.partition(":")
-    if name not in ("prefill_gemm", "prep_rotated", "lm_head_gemv") or not m.isdigit():
-        raise SystemExit(f"unknown profile case {spec!r} (expected prefill_gemm:M, prep_rotated:M or lm_head_gemv:1)")
+    if name not in ("prefill_gemm", "prep_rotated", "lm_head_gemv", "lm_head_gemm") or not m.isdigit():
+        raise SystemExit(f"unknown profile case {spec!r} (expected prefill_gemm:M, prep_rotated:M, "
+                         "lm_head_gemv:1 or lm_head_gemm:M)")
+    if name == "lm_head_gemm":
+        # the GEMM at lm_head size (K = 1536, N = 262144, group 128); M <= 8 runs
+        # the dp4a kernel's streaming form
+        M, N, K, g = int(m), 262144, 1536, 128
+        dev = torch.device("cuda", torch.cuda.current_device())
+        lay = qmm_synth.Layer("lm_head", W4A8, N, K, g, g)
+        qb, sw, _ = qmm_synth.layer_weights(0, "lm_head", lay)
+        d = q.weight_desc(W4A8, N, K, g)
+        packed = torch.empty(q.qmm_packed_size(d), dtype=torch.uint8, device=dev)
+        q.qmm_pack_weights(d, torch.from_numpy(qb).to(dev), torch.from_numpy(sw.view(np.int16)).to(dev), None, packed)
+        x = torch.from_numpy(qmm_synth.layer_activations(0, f"lm_head/x{M}", lay, M)).to(dev)
+        a16 = torch.empty((M, K), dtype=torch.float16, device=dev)
+        sx = torch.empty((M, K // g), dtype=torch.float32, device=dev)
+        Y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        q.qmm_prep_act(W4A8, M, K, g, g, x, 0, a16=a16, sx=sx)
+        for _ in range(2):
+            q.qmm_gemm(d, packed, M, a16, sx, Y)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(3):
+            q.qmm_gemm(d, packed, M, a16, sx, Y)
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / 3
+        print(json.dumps({"profile_case": spec, "us_per_call": us, "weight_GBps": packed.numel() / us / 1e3,
+                          "kernel": q.qmm_last_kernel_id(), "device_status": q.qmm_device_status()}))
+        return
     if name == "lm_head_gemv":
         # the plain GEMV on prepared codes at lm_head size (K = 1536, N = 262144, group 128)
         N, K, g = 262144, 1536, 128
