@@ -19,8 +19,6 @@ __device__ int g_status_word;
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-
 struct DeviceInfo {
     bool probed = false;
     bool supported = false;
@@ -95,10 +93,33 @@ qmm_status device_ctx(qmm_stream stream, LaunchCtx* ctx)
     if (!d.supported) return QMM_ERR_UNSUPPORTED_DEVICE;
     ctx->stream = static_cast<cudaStream_t>(stream);
     ctx->pdl = g_pdl != 0;
+    ctx->device = dev;
     ctx->num_sms = d.num_sms;
     ctx->status = d.status;
     return QMM_OK;
 }
+
+std::mutex g_smem_mutex;
+
+}  // namespace
+
+cudaError_t ensure_smem_bytes(KernelSmem& ks, const LaunchCtx& c, const void* kern, size_t smem,
+                              bool nonportable_cluster)
+{
+    std::lock_guard<std::mutex> lock(g_smem_mutex);
+    std::atomic<size_t>& have = ks.bytes[c.device];
+    if (smem <= have.load(std::memory_order_relaxed)) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (nonportable_cluster) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    have.store(smem, std::memory_order_release);
+    return cudaSuccess;
+}
+
+namespace {
 
 qmm_status launched(cudaError_t e, int32_t kernel)
 {

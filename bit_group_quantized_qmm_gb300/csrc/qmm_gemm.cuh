@@ -607,20 +607,18 @@ cudaError_t run_gemm(const LaunchCtx& c, const CUtensorMap& map, const GemmShape
     // inside the accumulator buffer (and the scale stage's sx region)
     const int first_col = EXPW == 8 ? 0 : sh.m_tile / 2;
     if (!DEBUG && first_col + MAXC > sh.d_stride) return cudaErrorInvalidValue;
-    static size_t configured = 0;
-    static int regs = 0;
-    cudaError_t e;
-    if (smem > configured) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured = smem;
-    }
+    static KernelSmem configured;
+    cudaError_t e = ensure_smem(configured, c, kern, smem);
+    if (e != cudaSuccess) return e;
+    static std::atomic<int> regs_seen{0};
+    int regs = regs_seen.load(std::memory_order_relaxed);
     if (regs == 0) {
         // the setmaxnreg split draws on the launch's 128 registers per thread
         cudaFuncAttributes fa;
         e = cudaFuncGetAttributes(&fa, kern);
         if (e != cudaSuccess) return e;
         regs = fa.numRegs;
+        regs_seen.store(regs, std::memory_order_relaxed);
     }
     if (regs * kGemmThreads != 65536) return cudaErrorInvalidConfiguration;
     int occ = 0;

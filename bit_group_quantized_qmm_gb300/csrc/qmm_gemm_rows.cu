@@ -578,21 +578,19 @@ cudaError_t run_stream(const LaunchCtx& c, int M, int N, int K, const uint8_t* b
     auto kern = gemm_rows_stream_kernel<GROUP, MR, RPT, CQ>;
     const int T = (N + 127) / 128, G = K / GROUP;
     const size_t smem = stream_smem_bytes(G, MR, GROUP, C::CB, C::NS, C::RS);
-    static size_t configured = 0;
-    static int per_sm = 0;
-    cudaError_t e;
-    if (smem > configured) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured = smem;
-        per_sm = 0;
-    }
-    int nb = per_sm;
+    static KernelSmem configured;
+    cudaError_t e = ensure_smem(configured, c, kern, smem);
+    if (e != cudaSuccess) return e;
+    // blocks per SM for this shared-memory size (the same on every supported device)
+    static std::atomic<int> per_sm{0};
+    static std::atomic<size_t> per_sm_smem{0};
+    int nb = per_sm_smem.load(std::memory_order_acquire) == smem ? per_sm.load(std::memory_order_relaxed) : 0;
     if (nb == 0) {
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, kThreads, smem);
         if (e != cudaSuccess) return e;
         if (nb < 1) return cudaErrorNotSupported;
-        per_sm = nb;
+        per_sm.store(nb, std::memory_order_relaxed);
+        per_sm_smem.store(smem, std::memory_order_release);
     }
     const int P = T < nb * c.num_sms ? T : nb * c.num_sms;
     return launch(kern, dim3(P), dim3(kThreads), smem, c, M, N, K, blob, act16, sx, Y, c.status);
@@ -616,13 +614,9 @@ cudaError_t run(const LaunchCtx& c, int M, int N, int K, const uint8_t* blob, co
     const int ng_max = (G + ks - 1) / ks;
     if (ng_max > C::NG_MAX) return cudaErrorNotSupported;   // K too large: the tensor-core path takes it
     const size_t smem = smem_bytes(ks, MR, ng_max, GROUP, C::CB);
-    static size_t configured = 0;
-    cudaError_t e;
-    if (smem > configured) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured = smem;
-    }
+    static KernelSmem configured;
+    const cudaError_t e = ensure_smem(configured, c, kern, smem);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(T, ks);
     cfg.blockDim = dim3(kThreads);

@@ -246,12 +246,9 @@ static cudaError_t launch_gemv_t(const LaunchCtx& c, int N, int K, int ksplit, c
     const int ring = ng_max < C::RING ? ng_max : C::RING;
     const size_t smem = gemv_smem_bytes(ring, C::CB, ng_max, GROUP);
     auto kern = gemv_kernel<GROUP, DEBUG, CQ>;
-    static size_t configured = 0;
-    if (smem > configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured = smem;
-    }
+    static KernelSmem configured;
+    const cudaError_t e = ensure_smem(configured, c, kern, smem);
+    if (e != cudaSuccess) return e;
     return launch(kern, dim3(T, ksplit), dim3(kGemvThreads), smem, c, N, K, ksplit, blob, a, sx, y, P, ws_part,
                   ws_count, c.status);
 }

@@ -373,15 +373,9 @@ cudaError_t run(const LaunchCtx& c, const FusedSet& set, int K, int hadamard, co
     const int ng_max = (G + ks - 1) / ks;
     if (ng_max > (GROUP == 64 ? 44 : 22)) return cudaErrorInvalidValue;   // K too large for one cluster per tile
     const size_t smem = smem_bytes(ng_max, C::CB, ng_max, GROUP);
-    static size_t configured = 0;
-    cudaError_t e;
-    if (smem > configured) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-        configured = smem;
-    }
+    static KernelSmem configured;
+    const cudaError_t e = ensure_smem(configured, c, kern, smem, /*nonportable_cluster=*/true);
+    if (e != cudaSuccess) return e;
     const float rot = hadamard ? (float)(1.0 / sqrt((double)GROUP)) : 1.0f;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(T, ks);

@@ -6,16 +6,41 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 namespace qmm {
 
+constexpr int kMaxDevices = 64;   // device ordinals the library serves
+
 struct LaunchCtx {
     cudaStream_t stream;
     bool pdl;         // launch with programmatic stream serialization
+    int device;       // current device ordinal, < kMaxDevices
     int num_sms;
     int* status;      // device error word
 };
+
+// A kernel's dynamic shared-memory limit is a per-device function attribute,
+// and CUDA sets it rather than raising it. Each launcher keeps one KernelSmem
+// per kernel instantiation (a function-local static); ensure_smem raises the
+// limit on the launch's device when the launch needs more than was set there.
+// The fast path is one atomic load; raising is serialised by a mutex, so two
+// threads never lower the limit under each other.
+struct KernelSmem {
+    std::atomic<size_t> bytes[kMaxDevices] = {};
+};
+
+cudaError_t ensure_smem_bytes(KernelSmem& ks, const LaunchCtx& c, const void* kern, size_t smem,
+                              bool nonportable_cluster);
+
+template <typename... Params>
+cudaError_t ensure_smem(KernelSmem& ks, const LaunchCtx& c, void (*kern)(Params...), size_t smem,
+                        bool nonportable_cluster = false)
+{
+    if (smem <= ks.bytes[c.device].load(std::memory_order_acquire)) return cudaSuccess;
+    return ensure_smem_bytes(ks, c, reinterpret_cast<const void*>(kern), smem, nonportable_cluster);
+}
 
 // Launch `kern` on the context's stream, with programmatic dependent launch
 // when enabled.

@@ -271,12 +271,9 @@ cudaError_t launch_rot_t(const LaunchCtx& c, const CUtensorMap& map, int M, int 
     auto kern = prep_rotate_kernel<GROUP, XDT>;
     const int stage_bytes = rot_stage_bytes(M, XDT == 0 ? 4 : 2);
     const size_t smem = rot_smem_bytes(stage_bytes);
-    static size_t configured = 0;
-    if (smem > configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured = smem;
-    }
+    static KernelSmem configured;
+    const cudaError_t e = ensure_smem(configured, c, kern, smem);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(K / 128 * kRotCluster), (unsigned)((M + kRotMB - 1) / kRotMB));
     cfg.blockDim = dim3(kRotThreads);
