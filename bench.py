@@ -12,7 +12,7 @@ The per-step weights (> 2x L2) are larger than L2, so no flush is needed.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--no-sweep]
   python bench.py --profile-case prefill_gemm:1068     (a few GEMM launches, for ncu; also prep_rotated:M,
-                                                        lm_head_gemv:1, lm_head_gemm:M)
+                                                        lm_head_gemv:1, lm_head_gemv_cq4:1, lm_head_gemm:M)
 
 The step is captured once in a CUDA graph (the kernels are launched with
 programmatic dependent launch, so each GEMV streams its weights while the
@@ -63,7 +63,7 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-cpu-all-cores", action="store_true", help="skip the all-core oracle figure")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
-    p.add_argument("--profile-case", default=None, metavar="prefill_gemm:M|prep_rotated:M|lm_head_gemv:1|lm_head_gemm:M",
+    p.add_argument("--profile-case", default=None, metavar="prefill_gemm:M|prep_rotated:M|lm_head_gemv[_cq4]:1|lm_head_gemm:M",
                    help="run one prefill GEMM shape a few times and exit (for profilers; prints one JSON line)")
     return p.parse_args()
 
@@ -622,9 +622,10 @@ def profile_case(spec):
     import torch
     import bit_group_quantized_qmm_gb300 as q
     name, _, m = spec.partition(":")
-    if name not in ("prefill_gemm", "prep_rotated", "lm_head_gemv", "lm_head_gemm") or not m.isdigit():
+    if name not in ("prefill_gemm", "prep_rotated", "lm_head_gemv", "lm_head_gemv_cq4", "lm_head_gemm") \
+            or not m.isdigit():
         raise SystemExit(f"unknown profile case {spec!r} (expected prefill_gemm:M, prep_rotated:M, "
-                         "lm_head_gemv:1 or lm_head_gemm:M)")
+                         "lm_head_gemv:1, lm_head_gemv_cq4:1 or lm_head_gemm:M)")
     if name == "lm_head_gemm":
         # the GEMM at lm_head size (K = 1536, N = 262144, group 128); M <= 8 runs
         # the dp4a kernel's streaming form
@@ -653,15 +654,23 @@ def profile_case(spec):
         print(json.dumps({"profile_case": spec, "us_per_call": us, "weight_GBps": packed.numel() / us / 1e3,
                           "kernel": q.qmm_last_kernel_id(), "device_status": q.qmm_device_status()}))
         return
-    if name == "lm_head_gemv":
-        # the plain GEMV on prepared codes at lm_head size (K = 1536, N = 262144, group 128)
+    if name in ("lm_head_gemv", "lm_head_gemv_cq4"):
+        # the plain GEMV on prepared codes at lm_head size (K = 1536, N = 262144,
+        # group 128), symmetric or codebook weights
         N, K, g = 262144, 1536, 128
+        variant = CQ4 if name.endswith("cq4") else W4A8
         dev = torch.device("cuda", torch.cuda.current_device())
-        lay = qmm_synth.Layer("lm_head", W4A8, N, K, g, g)
+        lay = qmm_synth.Layer("lm_head", variant, N, K, g, g)
         qb, sw, _ = qmm_synth.layer_weights(0, "lm_head", lay)
-        d = q.weight_desc(W4A8, N, K, g)
+        d = q.weight_desc(variant, N, K, g)
         packed = torch.empty(q.qmm_packed_size(d), dtype=torch.uint8, device=dev)
-        q.qmm_pack_weights(d, torch.from_numpy(qb).to(dev), torch.from_numpy(sw.view(np.int16)).to(dev), None, packed)
+        if variant == CQ4:
+            C, cb = qmm_synth.layer_codebook(0, "lm_head")
+            q.qmm_pack_weights_cq4(d, torch.from_numpy(qb).to(dev), C, cb,
+                                   torch.from_numpy(sw.view(np.int16)).to(dev), packed)
+        else:
+            q.qmm_pack_weights(d, torch.from_numpy(qb).to(dev), torch.from_numpy(sw.view(np.int16)).to(dev), None,
+                               packed)
         x = torch.from_numpy(qmm_synth.layer_activations(0, "lm_head/x1", lay, 1)).to(dev)
         a = torch.empty(K, dtype=torch.int8, device=dev)
         sx = torch.empty(K // g, dtype=torch.float32, device=dev)
