@@ -31,6 +31,7 @@ DeviceInfo g_devices[kMaxDevices];
 thread_local int32_t g_last_kernel = QMM_KERNEL_NONE;
 int g_pdl = 1;
 int g_a_in_smem = 0;
+int g_narrow = QMM_NARROW_AUTO;
 int g_fault = 0;   // test-only fault injection point (0: none)
 int g_rows_max = 8;
 
@@ -417,6 +418,14 @@ static qmm_status gemm_common(const qmm_weight_desc* w, const void* packed, int3
                                                static_cast<const uint16_t*>(act16), act_scale, Y);
         if (e != cudaErrorNotSupported) return launched(e, QMM_KERNEL_GEMM_ROWS);
     }
+    const bool many_tiles = (w->N + 127) / 128 >= 512;
+    if (int8_act(w->variant) && !P && M <= 32 &&
+        (g_narrow == QMM_NARROW_ALWAYS || (g_narrow == QMM_NARROW_AUTO && w->variant == QMM_W4A8 && many_tiles))) {
+        CUtensorMap nmap;
+        if (!act_tensor_map(&nmap, act16, M, w->K, (M + 7) & ~7)) return QMM_ERR_CUDA;
+        const cudaError_t e = launch_gemm_narrow(c, cq4, w->group, nmap, M, w->N, w->K, blob, act_scale, Y);
+        if (e != cudaErrorNotSupported) return launched(e, QMM_KERNEL_GEMM_NARROW);
+    }
     const bool a_smem = g_a_in_smem != 0;
     GemmShape sh = gemm_shape(M, w->N, w->K, a_smem);
     CUtensorMap map;
@@ -502,6 +511,11 @@ void qmm_set_pdl(int32_t enable) { g_pdl = enable ? 1 : 0; }
 void qmm_set_fault_injection(int32_t point) { g_fault = point == 1 ? 1 : 0; }
 
 void qmm_set_gemm_weight_operand(int32_t in_shared_memory) { g_a_in_smem = in_shared_memory ? 1 : 0; }
+
+void qmm_set_gemm_narrow(int32_t mode)
+{
+    g_narrow = mode == QMM_NARROW_OFF || mode == QMM_NARROW_ALWAYS ? mode : QMM_NARROW_AUTO;
+}
 
 void qmm_set_gemm_rows_max(int32_t max_rows) { g_rows_max = max_rows < 0 ? 0 : (max_rows > 16 ? 16 : max_rows); }
 

@@ -124,6 +124,10 @@ cudaError_t launch_gemm_w4a8(const LaunchCtx& c, int group, const CUtensorMap& m
                              const uint8_t* blob, const float* sx, float* Y, int32_t* P, bool a_in_smem);
 cudaError_t launch_gemm_cq4(const LaunchCtx& c, int group, const CUtensorMap& map, const GemmShape& sh,
                             const uint8_t* blob, const float* sx, float* Y, int32_t* P, bool a_in_smem);
+// W4A8 / CQ4 GEMM for 1 <= M <= 32 on the tensor cores with the weights in the
+// MMA's N slot. map: act_tensor_map of act16 with boxes of M rounded up to 8 rows.
+cudaError_t launch_gemm_narrow(const LaunchCtx& c, bool cq4, int group, const CUtensorMap& map, int M, int N, int K,
+                               const uint8_t* blob, const float* sx, float* Y);
 // W4A8 / CQ4 GEMM for M <= 16 on the CUDA cores; cudaErrorNotSupported when the
 // shape does not fit it (the caller then uses the tensor-core kernel).
 cudaError_t launch_gemm_rows(const LaunchCtx& c, bool cq4, int group, int M, int N, int K, const uint8_t* blob,

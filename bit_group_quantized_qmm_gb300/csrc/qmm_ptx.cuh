@@ -290,6 +290,15 @@ __device__ __forceinline__ void tmem_ld_wait64(uint32_t (&r)[64])
                  : "memory");
 }
 
+__device__ __forceinline__ void tmem_ld_wait_n(uint32_t (&r)[16])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15])
+                 :
+                 : "memory");
+}
 __device__ __forceinline__ void tmem_ld_wait_n(uint32_t (&r)[32]) { tmem_ld_wait32(r); }
 __device__ __forceinline__ void tmem_ld_wait_n(uint32_t (&r)[48])
 {

@@ -105,7 +105,8 @@ typedef enum {
     QMM_KERNEL_GEMV_FUSED_SIBLINGS = 9,
     QMM_KERNEL_GEMV_CQ4 = 10,
     QMM_KERNEL_GEMM_CQ4 = 11,
-    QMM_KERNEL_PREP_ROTATED = 12
+    QMM_KERNEL_PREP_ROTATED = 12,
+    QMM_KERNEL_GEMM_NARROW = 13
 } qmm_kernel_id;
 
 typedef void* qmm_stream; /* cudaStream_t */
@@ -382,7 +383,11 @@ qmm_status qmm_gemv_static_scratch(const qmm_weight_desc* w, const void* packed,
  * each weight read once for all rows (qmm_last_kernel_id reports
  * QMM_KERNEL_GEMM_ROWS); same inputs, same outputs within the W4A8 tolerance.
  * Shapes that kernel cannot hold (K above 1536 per 8-CTA cluster slice of
- * 24 groups of 64, or 12 of 128) stay on the tensor cores.
+ * 24 groups of 64, or 12 of 128) stay on the tensor cores. Above that limit,
+ * a W4A8 call with M <= 32 and at least 512 row tiles (N > 65408) runs the
+ * tensor-core kernel that puts the weights in the MMA's N slot, 256 weight
+ * rows per MMA (QMM_KERNEL_GEMM_NARROW; see qmm_set_gemm_narrow); it performs
+ * the same operations in the same order as the general tensor-core kernel.
  *   QMM_W4A8:   act16 = qmm_prep_act a16 [M][K] fp16 codes, act_scale = sx [M][G]
  *               Y[m][n] = sum_g sw[n][g] * sx[m][g] * P[m][n][g]
  *   QMM_CQ4:    as QMM_W4A8, with q[n][k] = C[i[n][k]], times cb_scale
@@ -450,6 +455,18 @@ void qmm_set_gemm_weight_operand(int32_t in_shared_memory);
  * cores; values above 16 are treated as 16. Default 8 (above it the tensor
  * cores are as fast or faster on the measured shapes). */
 void qmm_set_gemm_rows_max(int32_t max_rows);
+
+/* When W4A8 and CQ4 qmm_gemm calls with M <= 32 (above the CUDA-core limit)
+ * run the tensor-core kernel with the weights in the MMA's N slot
+ * (process-wide, launches after the call): QMM_NARROW_OFF never;
+ * QMM_NARROW_AUTO (default) for W4A8 with at least 512 row tiles, where it
+ * measured faster (lm_head: 0.88x to 0.96x the time of the general kernel;
+ * codebook weights and few row tiles were slower); QMM_NARROW_ALWAYS for every
+ * such call (tests). The outputs are the same bits either way; shapes whose
+ * activation scales overflow its shared memory (K / group above about 300)
+ * stay on the general kernel. */
+enum { QMM_NARROW_OFF = 0, QMM_NARROW_AUTO = 1, QMM_NARROW_ALWAYS = 2 };
+void qmm_set_gemm_narrow(int32_t mode);
 
 #ifdef __cplusplus
 }

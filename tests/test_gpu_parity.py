@@ -351,10 +351,12 @@ def test_gemm_output(torch_cuda, orc, M, N, K, group, had, operand_in_smem):
     d, packed = gc.pack(W4A8, N, K, group, qb, sw)
     _, a16, sx, _, _ = gc.prep_w4a8(x, group, had)
     q.qmm_set_gemm_weight_operand(operand_in_smem)
+    q.qmm_set_gemm_narrow(q.NARROW_OFF)   # the general tensor-core kernel (or the small-M one)
     try:
         Yg = gc.gemm(d, packed, M, a16, sx).cpu().numpy()
     finally:
         q.qmm_set_gemm_weight_operand(False)
+        q.qmm_set_gemm_narrow(q.NARROW_AUTO)
     ra, rsx, _ = orc.prep_w4a8(x, group, had)
     Y, Ym = orc.gemm_w4a8(qb, sw, ra, rsx, group)
     ok, worst = gc.within_w4a8(Yg, Y, Ym)
@@ -370,6 +372,46 @@ WIDE_N = 305 * 128 - 72
 @pytest.mark.parametrize("operand_in_smem", [False, True])
 def test_gemm_many_tiles(torch_cuda, orc, M, operand_in_smem):
     test_gemm_output(torch_cuda, orc, M, WIDE_N, 256, 64, 64, operand_in_smem)
+
+
+# M <= 32 above the small-M limit: the tensor-core kernel with the weights in
+# the MMA's N slot (256 weight rows per MMA, activations loaded into all four
+# lane quadrants). Against the oracle (every output), bit for bit against the
+# general tensor-core kernel (same operations in the same order), and a repeat.
+# Odd tile counts leave the last pair half empty; 640 tiles run several pairs
+# per persistent block.
+NARROW_CASES = [
+    (1, 200, 256, 64, 64),
+    (9, 384, 512, 64, 64),          # 3 tiles: one full pair, one half
+    (16, 256, 1536, 128, 128),
+    (17, 640 * 128 - 40, 256, 64, 64),
+    (32, 1000, 384, 128, 128),
+    (32, 130, 1536, 64, 0),
+]
+
+
+@pytest.mark.parametrize("M,N,K,group,had", NARROW_CASES)
+def test_gemm_narrow_output(torch_cuda, orc, M, N, K, group, had):
+    q = gc.lib()
+    qb, sw, x = gc.w4a8_case(16, f"narrow/{M}/{N}/{K}", N, K, group, had, M)
+    d, packed = gc.pack(W4A8, N, K, group, qb, sw)
+    _, a16, sx, _, _ = gc.prep_w4a8(x, group, had)
+    q.qmm_set_gemm_rows_max(0)
+    q.qmm_set_gemm_narrow(q.NARROW_ALWAYS)
+    try:
+        Yn = gc.gemm(d, packed, M, a16, sx, kernel=13).cpu().numpy()
+        Yn2 = gc.gemm(d, packed, M, a16, sx, kernel=13).cpu().numpy()
+        q.qmm_set_gemm_narrow(q.NARROW_OFF)
+        Yt = gc.gemm(d, packed, M, a16, sx, kernel=5).cpu().numpy()
+    finally:
+        q.qmm_set_gemm_rows_max(ROWS_DEFAULT)
+        q.qmm_set_gemm_narrow(q.NARROW_AUTO)
+    assert np.array_equal(Yn.view(np.uint32), Yn2.view(np.uint32)), "not deterministic"
+    ra, rsx, _ = orc.prep_w4a8(x, group, had)
+    Y, Ym = orc.gemm_w4a8(qb, sw, ra, rsx, group)
+    ok, worst = gc.within_w4a8(Yn, Y, Ym)
+    assert ok, f"worst error / bound = {worst}"
+    assert np.array_equal(Yn.view(np.uint32), Yt.view(np.uint32)), "differs from the general tensor-core kernel"
 
 
 def _sample_rows(N, n=48):
@@ -408,22 +450,26 @@ def test_lm_head_full_size_sampled(lm_head, orc, M):
     g = lay.group
     x = qmm_synth.layer_activations(0, f"lm_head/x{M}", lay, M)
     a, a16, sx, _, _ = gc.prep_w4a8(x, g, g)
-    Yg = gc.gemm(d, packed, M, a16, sx, kernel=8 if M <= 8 else 5).cpu().numpy()
+    Yg = gc.gemm(d, packed, M, a16, sx, kernel=8 if M <= 8 else 13).cpu().numpy()
     ra, rsx, _ = orc.prep_w4a8(x, g, g)
     rows = _sample_rows(lay.N)
     Y, Ym = orc.gemm_w4a8(qb, sw, ra, rsx, g, rows=rows)
     ok, worst = gc.within_w4a8(Yg[:, rows], Y, Ym)
     assert ok, f"GEMM worst error / bound = {worst}"
-    if M <= 16:
-        # the same call on the other kernel
-        q = gc.lib()
-        q.qmm_set_gemm_rows_max(0 if M <= 8 else 16)
+    # the same call on the other kernels that serve this M
+    q = gc.lib()
+    on, off = q.NARROW_AUTO, q.NARROW_OFF
+    others = [(0, on, 13), (0, off, 5)] if M <= 8 else [(0, off, 5)] + ([(16, on, 8)] if M <= 16 else [])
+    for rows_max, narrow, kernel in others:
+        q.qmm_set_gemm_rows_max(rows_max)
+        q.qmm_set_gemm_narrow(narrow)
         try:
-            Yt = gc.gemm(d, packed, M, a16, sx, kernel=5 if M <= 8 else 8).cpu().numpy()
+            Yt = gc.gemm(d, packed, M, a16, sx, kernel=kernel).cpu().numpy()
         finally:
             q.qmm_set_gemm_rows_max(ROWS_DEFAULT)
+            q.qmm_set_gemm_narrow(q.NARROW_AUTO)
         ok, worst = gc.within_w4a8(Yt[:, rows], Y, Ym)
-        assert ok, f"tensor-core GEMM worst error / bound = {worst}"
+        assert ok, f"kernel {kernel}: worst error / bound = {worst}"
     if M == 1:
         y = gc.gemv(d, packed, a, sx).cpu().numpy()
         ok, worst = gc.within_w4a8(y[None, rows], Y, Ym)
@@ -459,9 +505,11 @@ def test_gemm_rows_output(torch_cuda, orc, M, N, K, group, had):
         Yr2 = gc.gemm(d, packed, M, a16, sx, kernel=8).cpu().numpy()
         assert np.array_equal(Yr, Yr2)
         q.qmm_set_gemm_rows_max(0)
+        q.qmm_set_gemm_narrow(q.NARROW_OFF)
         Yt = gc.gemm(d, packed, M, a16, sx, kernel=5).cpu().numpy()
     finally:
         q.qmm_set_gemm_rows_max(ROWS_DEFAULT)
+        q.qmm_set_gemm_narrow(q.NARROW_AUTO)
     ra, rsx, _ = orc.prep_w4a8(x, group, had)
     Y, Ym = orc.gemm_w4a8(qb, sw, ra, rsx, group)
     for name, Yg in (("dp4a", Yr), ("tensor", Yt)):
@@ -504,7 +552,9 @@ def test_gemm_rows_stream_output(torch_cuda, orc, M, K, group, had):
 
 def test_gemm_rows_limit_and_fallback(torch_cuda, orc):
     """The rows limit picks the kernel; a K too long for one cluster of the
-    dp4a kernel (193 groups of 64) falls back to the tensor cores."""
+    dp4a kernel (193 groups of 64) falls back to the tensor cores: not to the
+    weights-in-N kernel (its shared memory holds every group's activation
+    scales, which 193 groups overflow) but to the general one."""
     q = gc.lib()
     M, N, K, group = 4, 128, 193 * 64, 64
     qb, sw, x = gc.w4a8_case(12, "rows/fallback", N, K, group, 0, M)

@@ -206,13 +206,26 @@ def test_gemm_output(torch_cuda, orc, M, N, K, group, had, operand_in_smem):
     Y, Ym = orc.gemm_cq4(idx, C, cb, sw, ra, rsx, group)
     q.qmm_set_gemm_weight_operand(operand_in_smem)
     q.qmm_set_gemm_rows_max(0)
+    q.qmm_set_gemm_narrow(q.NARROW_OFF)
     try:
         Yg = gc.gemm(d, packed, M, a16, sx, kernel=11).cpu().numpy()
     finally:
         q.qmm_set_gemm_weight_operand(False)
         q.qmm_set_gemm_rows_max(8)
+        q.qmm_set_gemm_narrow(q.NARROW_AUTO)
     ok, worst = gc.within_w4a8(Yg, Y, Ym)
     assert ok, f"tensor-core kernel: worst error / bound = {worst}"
+    if M <= 32 and not operand_in_smem:
+        # the weights-in-N tensor-core kernel (not chosen by default for
+        # codebook weights): the same bits
+        q.qmm_set_gemm_rows_max(0)
+        q.qmm_set_gemm_narrow(q.NARROW_ALWAYS)
+        try:
+            Yn = gc.gemm(d, packed, M, a16, sx, kernel=13).cpu().numpy()
+        finally:
+            q.qmm_set_gemm_rows_max(8)
+            q.qmm_set_gemm_narrow(q.NARROW_AUTO)
+        assert np.array_equal(Yn.view(np.uint32), Yg.view(np.uint32)), "weights-in-N kernel differs"
     if M <= 16 and not operand_in_smem:
         q.qmm_set_gemm_rows_max(16)
         try:
