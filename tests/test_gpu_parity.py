@@ -387,6 +387,7 @@ NARROW_CASES = [
     (17, 640 * 128 - 40, 256, 64, 64),
     (32, 1000, 384, 128, 128),
     (32, 130, 1536, 64, 0),
+    (12, 640 * 128 - 41, 256, 64, 64),   # N % 4 != 0: scalar stores
 ]
 
 
