@@ -16,20 +16,23 @@
 // activation rows (M = 128), so a 64-wide k-step of 256 weight rows is 4 MMAs
 // (a microbenchmark with the weight operand refilled from shared memory every
 // k-step ran them at the isolated rate, ~130 cycles each). The activation
-// tile (at most 32 rows, boxes of M rounded up to 8) is loaded four times, at
-// rows 0, 32, 64 and 96 of the operand, so every tensor-memory lane quadrant
-// holds all activation rows
-// and the rescale of a group's 256 columns spreads over the four quadrants
-// (each quadrant's two epilogue warps take 64 of the columns).
+// tile (at most 32 rows; boxes of M rounded up to 8 rows) is loaded four
+// times, at rows 0, 32, 64 and 96 of the operand, so every tensor-memory lane
+// quadrant holds all activation rows and the rescale of a group's 256 columns
+// spreads over the four quadrants (each quadrant's two epilogue warps take 64
+// of the columns).
 //
 // Per k-step: 8 expand warps decode the 256 rows' nibbles (or codebook
 // indices) into fp16 integers in the 128-byte-swizzled K-major layout of the
-// B operand; the activation producer lands four TMA boxes (64 k wide); the MMA
-// warp issues 4 MMAs into the group's
-// accumulator (256 tensor-memory columns, two buffers). Per group the
-// epilogue rescales the exact fp32 partials: acc += (P * sx) * sw, in group
-// order, the operations and order of the other tensor-core kernel. Persistent
-// over pairs of 128-row weight tiles; every wait bounded.
+// B operand; the activation producer lands the four TMA boxes (64 k wide); the
+// MMA warp issues 4 MMAs into the group's accumulator (256 tensor-memory
+// columns, two buffers). Per group the epilogue rescales the exact fp32
+// partials, acc += (P * sx) * sw in group order: the operations and order of
+// the other tensor-core kernel, so the outputs are the same bits. The
+// activation scales of every group are staged once in shared memory.
+// Persistent over pairs of 128-row weight tiles; every wait bounded. Shared
+// memory carries the fp16 weight operand twice (stored, then read by the
+// MMAs) and bounds the kernel at ~2.5x the MMA time.
 #include <cuda_fp16.h>
 
 #include "qmm.h"
