@@ -581,16 +581,16 @@ cudaError_t run_stream(const LaunchCtx& c, int M, int N, int K, const uint8_t* b
     static KernelSmem configured;
     cudaError_t e = ensure_smem(configured, c, kern, smem);
     if (e != cudaSuccess) return e;
-    // blocks per SM for this shared-memory size (the same on every supported device)
-    static std::atomic<int> per_sm{0};
-    static std::atomic<size_t> per_sm_smem{0};
-    int nb = per_sm_smem.load(std::memory_order_acquire) == smem ? per_sm.load(std::memory_order_relaxed) : 0;
+    // blocks per SM for this shared-memory size (the same on every supported
+    // device), cached as one word: shared-memory bytes << 8 | blocks
+    static std::atomic<uint64_t> occ_cache{0};
+    const uint64_t cached = occ_cache.load(std::memory_order_relaxed);
+    int nb = (cached >> 8) == (uint64_t)smem ? (int)(cached & 0xFF) : 0;
     if (nb == 0) {
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, kThreads, smem);
         if (e != cudaSuccess) return e;
         if (nb < 1) return cudaErrorNotSupported;
-        per_sm.store(nb, std::memory_order_relaxed);
-        per_sm_smem.store(smem, std::memory_order_release);
+        occ_cache.store(((uint64_t)smem << 8) | (uint64_t)(nb & 0xFF), std::memory_order_relaxed);
     }
     const int P = T < nb * c.num_sms ? T : nb * c.num_sms;
     return launch(kern, dim3(P), dim3(kThreads), smem, c, M, N, K, blob, act16, sx, Y, c.status);
