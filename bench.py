@@ -12,7 +12,8 @@ The per-step weights (> 2x L2) are larger than L2, so no flush is needed.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--no-sweep]
   python bench.py --profile-case prefill_gemm:1068     (a few GEMM launches, for ncu; also prep_rotated:M,
-                                                        lm_head_gemv:1, lm_head_gemv_cq4:1, lm_head_gemm:M)
+                                                        lm_head_gemv:1, lm_head_gemv_cq4:1, lm_head_gemm:M,
+                                                        affine_gemm:M)
 
 The step is captured once in a CUDA graph (the kernels are launched with
 programmatic dependent launch, so each GEMV streams its weights while the
@@ -63,7 +64,7 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-cpu-all-cores", action="store_true", help="skip the all-core oracle figure")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
-    p.add_argument("--profile-case", default=None, metavar="prefill_gemm:M|prep_rotated:M|lm_head_gemv[_cq4]:1|lm_head_gemm:M",
+    p.add_argument("--profile-case", default=None, metavar="prefill_gemm:M|prep_rotated:M|lm_head_gemv[_cq4]:1|lm_head_gemm:M|affine_gemm:M",
                    help="run one prefill GEMM shape a few times and exit (for profilers; prints one JSON line)")
     return p.parse_args()
 
@@ -622,10 +623,37 @@ def profile_case(spec):
     import torch
     import bit_group_quantized_qmm_gb300 as q
     name, _, m = spec.partition(":")
-    if name not in ("prefill_gemm", "prep_rotated", "lm_head_gemv", "lm_head_gemv_cq4", "lm_head_gemm") \
-            or not m.isdigit():
+    if name not in ("prefill_gemm", "prep_rotated", "lm_head_gemv", "lm_head_gemv_cq4", "lm_head_gemm",
+                    "affine_gemm") or not m.isdigit():
         raise SystemExit(f"unknown profile case {spec!r} (expected prefill_gemm:M, prep_rotated:M, "
-                         "lm_head_gemv:1, lm_head_gemv_cq4:1 or lm_head_gemm:M)")
+                         "lm_head_gemv:1, lm_head_gemv_cq4:1, lm_head_gemm:M or affine_gemm:M)")
+    if name == "affine_gemm":
+        # the affine GEMM of the fused gate_up shape (K = 5120, N = 34816, group 64, fp16 x)
+        M, N, K = int(m), 34816, 5120
+        dev = torch.device("cuda", torch.cuda.current_device())
+        lay = qmm_synth.Layer("affine_gemm", AFFINE, N, K, 64, 0)
+        qb, s, b = qmm_synth.layer_weights(0, "affine_gemm", lay)
+        d = q.weight_desc(AFFINE, N, K, 64)
+        packed = torch.empty(q.qmm_packed_size(d), dtype=torch.uint8, device=dev)
+        q.qmm_pack_weights(d, torch.from_numpy(qb).to(dev), torch.from_numpy(s.view(np.int16)).to(dev),
+                           torch.from_numpy(b.view(np.int16)).to(dev), packed)
+        x16 = torch.from_numpy(qmm_synth.layer_activations(0, f"affine_gemm/x{M}", lay, M).view(np.float16)).to(dev)
+        S = torch.empty((M, K // 64), dtype=torch.float32, device=dev)
+        Y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        q.qmm_prep_act(AFFINE, M, K, 64, 0, x16, 1, gsum=S)
+        for _ in range(2):
+            q.qmm_gemm(d, packed, M, x16, S, Y)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(3):
+            q.qmm_gemm(d, packed, M, x16, S, Y)
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / 3
+        print(json.dumps({"profile_case": spec, "us_per_call": us, "TFLOPS": 2 * M * N * K / us / 1e6,
+                          "kernel": q.qmm_last_kernel_id(), "device_status": q.qmm_device_status()}))
+        return
     if name == "lm_head_gemm":
         # the GEMM at lm_head size (K = 1536, N = 262144, group 128); M <= 8 runs
         # the dp4a kernel's streaming form
