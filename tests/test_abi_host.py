@@ -155,3 +155,15 @@ def test_no_cpu_fallback_in_product_path():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(root, f)).read()
                 assert "oracle" not in text.lower(), f
+
+
+def test_kernel_ids_match_header(q):
+    """The binding's kernel names cover exactly the qmm_kernel_id values the
+    header declares, and the narrow-kernel modes match the header's enum."""
+    import re
+    hdr = open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "..", "include", "qmm.h")).read()
+    ids = {int(v) for v in re.findall(r"QMM_KERNEL_\w+\s*=\s*(\d+)", hdr)}
+    assert ids == set(q.KERNEL_IDS), (sorted(ids), sorted(q.KERNEL_IDS))
+    modes = dict(re.findall(r"(QMM_NARROW_\w+)\s*=\s*(\d+)", hdr))
+    assert {int(v) for v in modes.values()} == {q.NARROW_OFF, q.NARROW_AUTO, q.NARROW_ALWAYS}
+    assert int(modes["QMM_NARROW_AUTO"]) == q.NARROW_AUTO
