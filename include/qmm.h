@@ -382,12 +382,14 @@ qmm_status qmm_gemv_static_scratch(const qmm_weight_desc* w, const void* packed,
  * (default 8) runs instead on the CUDA cores: exact int32 partials with dp4a,
  * each weight read once for all rows (qmm_last_kernel_id reports
  * QMM_KERNEL_GEMM_ROWS); same inputs, same outputs within the W4A8 tolerance.
- * Shapes that kernel cannot hold (K above 1536 per 8-CTA cluster slice of
- * 24 groups of 64, or 12 of 128) stay on the tensor cores. Above that limit,
- * a W4A8 call with M <= 32 and at least 512 row tiles (N > 65408) runs the
- * tensor-core kernel that puts the weights in the MMA's N slot, 256 weight
- * rows per MMA (QMM_KERNEL_GEMM_NARROW; see qmm_set_gemm_narrow); it performs
- * the same operations in the same order as the general tensor-core kernel.
+ * With at least 512 row tiles (N > 65408) that kernel streams over the tiles
+ * with all of K per block; with fewer it splits K over a cluster, and shapes
+ * it cannot hold then (K above 1536 per 8-CTA cluster slice of 24 groups of
+ * 64, or 12 of 128) go to the tensor cores. Of the calls on the tensor cores,
+ * W4A8 ones with M <= 32 and at least 512 row tiles run the kernel that puts
+ * the weights in the MMA's N slot, 256 weight rows per MMA
+ * (QMM_KERNEL_GEMM_NARROW; see qmm_set_gemm_narrow), which performs the same
+ * operations in the same order as the general tensor-core kernel.
  *   QMM_W4A8:   act16 = qmm_prep_act a16 [M][K] fp16 codes, act_scale = sx [M][G]
  *               Y[m][n] = sum_g sw[n][g] * sx[m][g] * P[m][n][g]
  *   QMM_CQ4:    as QMM_W4A8, with q[n][k] = C[i[n][k]], times cb_scale
