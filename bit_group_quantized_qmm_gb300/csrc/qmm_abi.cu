@@ -104,6 +104,12 @@ std::mutex g_smem_mutex;
 
 }  // namespace
 
+int probe_current_device()
+{
+    LaunchCtx c;
+    return (int)device_ctx(nullptr, &c);
+}
+
 cudaError_t ensure_smem_bytes(KernelSmem& ks, const LaunchCtx& c, const void* kern, size_t smem,
                               bool nonportable_cluster)
 {

@@ -78,8 +78,12 @@ extern "C" qmm_status qmm_gemv_static_scratch(const qmm_weight_desc* w, const vo
     for (const void* p : {packed, static_cast<const void*>(a), static_cast<const void*>(sx),
                           static_cast<const void*>(y)})
         if (reinterpret_cast<uintptr_t>(p) & 15u) return QMM_ERR_MISALIGNED;
+    // the device probe first: an unsupported device gets the code qmm_gemv gives
+    // it, before any CUDA call of the set-up
+    qmm_status st = static_cast<qmm_status>(probe_current_device());
+    if (st != QMM_OK) return st;
     void* scratch = nullptr;
-    qmm_status st = scratch_address(&scratch);
+    st = scratch_address(&scratch);
     if (st != QMM_OK) return st;
     // the split-K counters sit at the end of the workspace and must start at zero
     const size_t T = (size_t)(w->N + 127) / 128;

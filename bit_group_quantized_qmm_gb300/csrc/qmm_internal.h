@@ -61,6 +61,11 @@ cudaError_t launch(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, 
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
+// The library's probe of the current device (compute capability 10.3, looked
+// up once per device): 0 (QMM_OK) when it is supported, else the qmm_status
+// code every entry point returns for it.
+int probe_current_device();
+
 cudaError_t launch_pack(const LaunchCtx& c, int variant, int N, int K, int group, const uint8_t* q,
                         const uint16_t* scales, const uint16_t* biases, uint8_t* blob);
 
@@ -79,7 +84,7 @@ cudaError_t launch_prep_w4a8(const LaunchCtx& c, int M, int K, int group, int ha
 // Full-K rotation z = R x (fp32, ascending fused multiply-adds), then per-group
 // int8 quantization. K % 128 == 0, group 64 or 128.
 // r_map: qmm_abi's rotation_tensor_map of R.
-// skip_first_box: test-only fault injection (the first box of R is never
+// skip_first_box: test-only fault injection (the first stage, box of R and rows of x, is never
 // requested, so the kernel's bounded waits run out and it sets the timeout bit).
 cudaError_t launch_prep_rotated(const LaunchCtx& c, const CUtensorMap& r_map, int M, int K, int group,
                                 const void* x, int x_dtype, int8_t* a, uint16_t* a16, float* sx, int32_t* asum,

@@ -136,6 +136,7 @@ __global__ void __launch_bounds__(kRotThreads) prep_rotate_kernel(const __grid_c
     uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)kRotStages * stage_bytes);
     float* pamax = reinterpret_cast<float*>(full + kRotStages);   // [kRotMB] partial maxima
     int* psum = reinterpret_cast<int*>(pamax + kRotMB);            // [kRotMB] partial code sums
+    int* pok = psum + kRotMB;   // every stage of this CTA arrived (read by the whole cluster)
 
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int r = t & (kRotRows - 1), mm = t / kRotRows;
@@ -168,6 +169,7 @@ __global__ void __launch_bounds__(kRotThreads) prep_rotate_kernel(const __grid_c
         }
     };
     auto issue_x = [&](int c) {
+        if (skip_first_box && c == 0) return;   // injected: stage 0 gets no copies at all
         uint8_t* st = ring + (size_t)(c % kRotStages) * stage_bytes + kRotRBytes;
         const int j = lane - 16;
         if (j >= 0 && j < mrows)
@@ -218,9 +220,14 @@ __global__ void __launch_bounds__(kRotThreads) prep_rotate_kernel(const __grid_c
         // copies may still be in flight into stages that were never consumed
         const int upto = consumed >= 1 ? consumed - 1 + kRotStages : kRotStages;
         const int issued = nstage < upto ? nstage : upto;
-        for (int c = consumed; c < issued; ++c)
+        for (int c = consumed; c < issued; ++c) {
+            if (skip_first_box && c == 0) continue;   // nothing was requested for it
             mbar_wait(&full[c % kRotStages], (uint32_t)(c / kRotStages) & 1u, status, nullptr);
+        }
     }
+    // the cluster's CTAs combine their partial maxima and code sums: none of
+    // them writes anything unless every CTA of the cluster saw all its stages
+    if (t == 0) *pok = ok;
 
     // ---- group amax: partial maxima of this CTA's 16 outputs per row
     const bool valid = mm < mrows;
@@ -229,6 +236,7 @@ __global__ void __launch_bounds__(kRotThreads) prep_rotate_kernel(const __grid_c
     for (int o = kRotRows / 2; o > 0; o >>= 1) pa = fmaxf(pa, __shfl_xor_sync(0xffffffffu, pa, o));
     if (r == 0) pamax[mm] = pa;
     cluster_sync_all();
+    for (uint32_t j = 0; j < kRotCluster; ++j) ok &= ld_shared_cluster_s32(map_shared_rank(smem_u32(pok), j));
     const uint32_t g_first = rank / CPG * CPG;
     float amax = 0.f;
 #pragma unroll

@@ -437,11 +437,12 @@ void qmm_set_pdl(int32_t enable);
 
 /*
  * Test-only fault injection (process-wide; 0 = off, the default). Point 1: the
- * next qmm_prep_act_rotated launches expect the first TMA box of R but never
- * request it, so every CTA's bounded wait for it runs out (about 2 s), the
- * kernel sets the timeout bit of the device error word and returns without
- * writing its outputs; qmm_device_status then reports QMM_ERR_TIMEOUT and the
- * context stays usable. Other values turn injection off. (The pages have no
+ * next qmm_prep_act_rotated launches expect their first stage (the TMA box of R
+ * and the rows of x) but never request it, so every CTA's bounded wait for it
+ * runs out (one wait limit, about 2 s), the kernel sets the timeout bit of the
+ * device error word and returns without writing its outputs (no CTA of a
+ * cluster writes once any of them timed out); qmm_device_status then reports
+ * QMM_ERR_TIMEOUT and the context stays usable. Other values turn injection off. (The pages have no
  * counterpart: it exercises the failure detection of the bounded waits.)
  */
 void qmm_set_fault_injection(int32_t point);

@@ -16,3 +16,13 @@ def pytest_configure(config):
 def orc():
     import oracle
     return oracle.default()
+
+
+@pytest.fixture(autouse=True)
+def _guards_intact():
+    """After every test: the guard regions around the outputs the GPU helpers
+    allocated (tests/gpu_cases.py) still hold their patterns."""
+    yield
+    mod = sys.modules.get("tests.gpu_cases")
+    if mod is not None and mod._live:
+        mod.assert_guards_intact()

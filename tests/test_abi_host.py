@@ -167,3 +167,19 @@ def test_kernel_ids_match_header(q):
     modes = dict(re.findall(r"(QMM_NARROW_\w+)\s*=\s*(\d+)", hdr))
     assert {int(v) for v in modes.values()} == {q.NARROW_OFF, q.NARROW_AUTO, q.NARROW_ALWAYS}
     assert int(modes["QMM_NARROW_AUTO"]) == q.NARROW_AUTO
+
+
+def test_static_scratch_probes_the_device_first(q):
+    """qmm_gemv_static_scratch validates its arguments on the host and then
+    probes the device before any other CUDA call: without a supported device
+    (this host has none) a valid call returns QMM_ERR_UNSUPPORTED_DEVICE, the
+    code qmm_gemv gives, not QMM_ERR_CUDA from the scratch set-up."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    L = q.library()
+    A = 1 << 20   # aligned, never dereferenced
+    d = q.weight_desc(0, 1536, 6144, 64)   # a split-K shape: the scratch path
+    assert q.qmm_gemv_workspace_size(d) > 0
+    assert L.qmm_gemv_static_scratch(ctypes.byref(d), A, A, A, A, None) == 3
+    assert L.qmm_gemv(ctypes.byref(d), A, A, A, A, A, q.qmm_gemv_workspace_size(d), None) == 3

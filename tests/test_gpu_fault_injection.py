@@ -1,10 +1,13 @@
 """Failure detection of the bounded waits, on the GPU, without a fault.
 
-With injection point 1 the full-K rotation prepass expects the first TMA box
-of R but never requests it: every CTA's bounded wait for it runs out (about
-2 s), the kernel records the timeout in the device error word and returns
-without writing its outputs; its copies in flight are drained and all CTAs
-of each cluster still meet at the cluster barriers, so nothing hangs. The
+With injection point 1 the full-K rotation prepass expects the first stage
+(the TMA box of R and the rows of x) but never requests it: every CTA's
+bounded wait for it runs out (one wait limit, about 2 s), the kernel records
+the timeout in the device error word and returns without writing its outputs;
+its other copies in flight are drained, the stage that was never requested is
+not waited for again, all CTAs of each cluster still meet at the cluster
+barriers, and no CTA writes once any CTA of its cluster has timed out, so
+nothing hangs and nothing is written. The
 host then reads QMM_ERR_TIMEOUT, and the same call without injection runs on
 the same context and matches the oracle.
 """

@@ -143,8 +143,8 @@ def test_prep_affine_group_sums_bit_exact(torch_cuda, orc, M, K, x_dtype):
     x = qmm_synth.normal(5, f"aff/{M}/{K}", M * K).astype(np.float32).reshape(M, K)
     xin, xval = _prep_input(x, x_dtype)
     G = K // 64
-    S = torch.empty((M, G), dtype=torch.float32, device=dev)
-    x16 = torch.empty((M, K), dtype=torch.float16, device=dev) if x_dtype != 1 else None
+    S = gc.guarded((M, G), torch.float32)
+    x16 = gc.guarded((M, K), torch.float16) if x_dtype != 1 else None
     q.qmm_prep_act(AFFINE, M, K, 64, 0, xin.to(dev), x_dtype, gsum=S, x16=x16)
     assert q.qmm_last_kernel_id() == 3
     ref = orc.group_sums_affine(xval)
@@ -160,7 +160,7 @@ def test_prep_affine_tree_fixture(torch_cuda):
     q = gc.lib()
     cases = oracle_pins.read_cases("group_sum_tree.txt")
     x = np.array([c["chunk"] for c in cases], dtype=np.float32).reshape(len(cases), 64)
-    S = torch.empty((len(cases), 1), dtype=torch.float32, device=gc.dev())
+    S = gc.guarded((len(cases), 1), torch.float32)
     q.qmm_prep_act(AFFINE, len(cases), 64, 64, 0, torch.from_numpy(x).to(gc.dev()), 0, gsum=S)
     expect = np.array([float(c["expect"]) for c in cases], dtype=np.float32)
     assert np.array_equal(S.cpu().numpy()[:, 0], expect)
@@ -215,9 +215,9 @@ def test_gemv_fused(torch_cuda, orc, N, K, group, had, outl, x_dtype):
     d, packed = gc.pack(W4A8, N, K, group, qb, sw)
     xin, xval = _prep_input(x, x_dtype)
     dev = gc.dev()
-    y = torch.full((N,), float("nan"), dtype=torch.float32, device=dev)
-    a = torch.empty(K, dtype=torch.int8, device=dev)
-    sx = torch.empty(K // group, dtype=torch.float32, device=dev)
+    y = gc.guarded((N,), torch.float32, float("nan"))
+    a = gc.guarded(K, torch.int8)
+    sx = gc.guarded(K // group, torch.float32)
     q.qmm_gemv_fused(d, packed, xin.to(dev), x_dtype, had, y, a, sx)
     assert q.qmm_last_kernel_id() == 7
     ra, rsx, _ = orc.prep_w4a8(xval, group, had)
@@ -254,10 +254,10 @@ def test_gemv_fused_siblings(torch_cuda, orc, Ns, K, group, had):
         d, packed = gc.pack(W4A8, N, K, group, qb, sw)
         descs.append(d)
         packs.append(packed)
-        ys.append(torch.full((N,), float("nan"), dtype=torch.float32, device=dev))
+        ys.append(gc.guarded((N,), torch.float32, float("nan")))
         refs.append((qb, sw))
-    a = torch.empty(K, dtype=torch.int8, device=dev)
-    sx = torch.empty(K // group, dtype=torch.float32, device=dev)
+    a = gc.guarded(K, torch.int8)
+    sx = gc.guarded(K // group, torch.float32)
     xt = gc.t(x[0].astype(np.float32))
     q.qmm_gemv_fused_siblings(descs, packs, xt, 0, had, ys, a, sx)
     assert q.qmm_last_kernel_id() == 9
@@ -294,11 +294,11 @@ def test_pack_then_consume_same_stream(torch_cuda, orc):
     torch.cuda.synchronize()
 
     def fresh():
-        return torch.full((size,), 0xFF, dtype=torch.uint8, device=gc.dev())
+        return gc.guarded((size,), torch.uint8, 0xFF)
 
     # fused GEMV (row 0 of x)
     blob = fresh()
-    y = torch.full((N,), float("nan"), dtype=torch.float32, device=gc.dev())
+    y = gc.guarded((N,), torch.float32, float("nan"))
     q.qmm_pack_weights(d, qt, st, None, blob)
     q.qmm_gemv_fused(d, blob, xt[0], 0, g, y)
     ok, worst = gc.within_w4a8(y.cpu().numpy()[None, rows], Y[:1], Ym[:1])
@@ -306,7 +306,7 @@ def test_pack_then_consume_same_stream(torch_cuda, orc):
     # GEMM on the CUDA cores (M = 2) and on the tensor cores (M = 64)
     for M, kernel in ((2, 8), (64, 5)):
         blob = fresh()
-        Yg = torch.full((M, N), float("nan"), dtype=torch.float32, device=gc.dev())
+        Yg = gc.guarded((M, N), torch.float32, float("nan"))
         q.qmm_pack_weights(d, qt, st, None, blob)
         q.qmm_gemm(d, blob, M, a16[:M], sx[:M], Yg)
         assert q.qmm_last_kernel_id() == kernel
@@ -591,7 +591,7 @@ def _affine_run(M, N, K, seed, name, zero_sums=False):
     x16 = qmm_synth.layer_activations(seed, name, lay, M)
     d, packed = gc.pack(AFFINE, N, K, 64, qb, s, b)
     xt = gc.t(x16).view(torch.float16)
-    S = torch.empty((M, K // 64), dtype=torch.float32, device=gc.dev())
+    S = gc.guarded((M, K // 64), torch.float32)
     q.qmm_prep_act(AFFINE, M, K, 64, 0, xt, 1, gsum=S)
     if zero_sums:
         S.zero_()

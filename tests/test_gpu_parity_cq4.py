@@ -114,9 +114,9 @@ def test_gemv_fused(torch_cuda, orc, N, K, group, had, outl, x_dtype):
         xt = xt.to(torch.float16)
     xval = xt.float().numpy()
     dev = gc.dev()
-    y = torch.full((N,), float("nan"), dtype=torch.float32, device=dev)
-    a = torch.empty(K, dtype=torch.int8, device=dev)
-    sx = torch.empty(K // group, dtype=torch.float32, device=dev)
+    y = gc.guarded((N,), torch.float32, float("nan"))
+    a = gc.guarded(K, torch.int8)
+    sx = gc.guarded(K // group, torch.float32)
     q.qmm_gemv_fused(d, packed, xt.to(dev), x_dtype, had, y, a, sx)
     assert q.qmm_last_kernel_id() == 7
     ra, rsx, _ = orc.prep_w4a8(xval, group, had)
@@ -149,7 +149,7 @@ def test_gemv_fused_siblings(torch_cuda, orc, Ns, K, group, had):
         d, packed = gc.pack_cq4(N, K, group, idx, C, cb, sw)
         descs.append(d)
         packs.append(packed)
-        ys.append(torch.full((N,), float("nan"), dtype=torch.float32, device=dev))
+        ys.append(gc.guarded((N,), torch.float32, float("nan")))
         refs.append((idx, sw, C, cb))
     xt = gc.t(x[0].astype(np.float32))
     q.qmm_gemv_fused_siblings(descs, packs, xt, 0, had, ys)

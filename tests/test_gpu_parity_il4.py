@@ -56,7 +56,7 @@ def _pack_il4(variant, N, K, group, ck, qb, s, b, C, cb):
     import torch
     q = gc.lib()
     d = q.weight_desc(variant, N, K, group)
-    packed = torch.full((q.qmm_packed_size(d),), 0xA5, dtype=torch.uint8, device=gc.dev())
+    packed = gc.guarded((q.qmm_packed_size(d),), torch.uint8, 0xA5)
     q.qmm_pack_weights_interleaved4(d, ck, gc.t(_panels(qb, ck)), gc.t(_panels(s, None)),
                                     None if b is None else gc.t(_panels(b, None)), packed, codebook=C,
                                     cb_scale=cb)
@@ -122,6 +122,6 @@ def test_pack_interleaved4_control_layout_is_detected(torch_cuda):
     import torch
     q = gc.lib()
     d = q.weight_desc(W4A8, N, K, group)
-    packed = torch.empty(q.qmm_packed_size(d), dtype=torch.uint8, device=gc.dev())
+    packed = gc.guarded(q.qmm_packed_size(d), torch.uint8)
     q.qmm_pack_weights_interleaved4(d, 16, gc.t(_panels(qb, 32)), gc.t(_panels(s, None)), None, packed)
     assert not np.array_equal(packed.cpu().numpy(), _pack_rows(W4A8, N, K, group, qb, s, b, C, cb))

@@ -52,10 +52,10 @@ def prep_rotated(R, xin, M, K, group, x_dtype):
     q = gc.lib()
     dev = gc.dev()
     G = K // group
-    a = torch.full((M, K), 99, dtype=torch.int8, device=dev)
-    a16 = torch.full((M, K), 99.0, dtype=torch.float16, device=dev)
-    sx = torch.full((M, G), float("nan"), dtype=torch.float32, device=dev)
-    asum = torch.full((M, G), -1, dtype=torch.int32, device=dev)
+    a = gc.guarded((M, K), torch.int8, 99)
+    a16 = gc.guarded((M, K), torch.float16, 99.0)
+    sx = gc.guarded((M, G), torch.float32, float("nan"))
+    asum = gc.guarded((M, G), torch.int32, -1)
     q.qmm_prep_act_rotated(M, K, group, gc.t(R), xin.to(dev), x_dtype, a=a, a16=a16, sx=sx, asum=asum)
     assert q.qmm_last_kernel_id() == 12
     return a, a16, sx, asum

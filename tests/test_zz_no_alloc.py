@@ -46,7 +46,7 @@ def test_static_scratch_matches_workspace_gemv_twice(torch_cuda, orc, N, K, grou
     ra, rsx, _ = orc.prep_w4a8(x, group, had)
     Y, Ym = orc.gemm_w4a8(qb, sw, ra, rsx, group)
     for call in range(2):
-        y = torch.full((N,), float("nan"), dtype=torch.float32, device=gc.dev())
+        y = gc.guarded((N,), torch.float32, float("nan"))
         # through the C ABI directly
         st = q.library().qmm_gemv_static_scratch(ctypes.byref(d), packed.data_ptr(), a.data_ptr(),
                                                  sx.data_ptr(), y.data_ptr(),
