@@ -64,6 +64,8 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-cpu-all-cores", action="store_true", help="skip the all-core oracle figure")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--peaks", action="store_true",
+                   help="compile and run the FP32 / mma.sync peak microbenchmark and exit (one JSON line)")
     p.add_argument("--profile-case", default=None, metavar="prefill_gemm:M|prep_rotated:M|lm_head_gemv[_cq4]:1|lm_head_gemm:M|affine_gemm:M",
                    help="run one prefill GEMM shape a few times and exit (for profilers; prints one JSON line)")
     return p.parse_args()
@@ -412,19 +414,146 @@ def run_reference(args, rank, world):
 
 # ------------------------------------------------------------------ sweep of the other workloads
 
-def sweep(world):
+# Peak of the legacy warp-level int8 MMA (mma.sync.m16n8k32.s8, int32
+# accumulators) on this GPU, measured with `python bench.py --peaks`: 252 MACs
+# per clock per SM (the tcgen05 kind::f16 MMA the GEMM issues does 4096). The
+# sweep reports every GEMM's TOPS against it beside the bf16 figure.
+MMA_SYNC_S8_MAC_PER_CLK_SM = 252.0
+
+
+def s8_peak_tops(sm_mhz=None):
+    """mma.sync s8 peak in TOPS at the given SM clock (default: the measured maximum)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    mhz = sm_mhz
+    if mhz is None:
+        mhz = 2070.0
+        if os.path.exists(path):
+            with open(path) as f:
+                mhz = float(json.load(f).get("sm_max_mhz", mhz))
+    return 2.0 * MMA_SYNC_S8_MAC_PER_CLK_SM * 152 * mhz * 1e6 / 1e12
+
+
+def ab_time(fns, calls, rounds=6, iters=10):
+    """Alternating best-of timing: one CUDA graph per function, replayed
+    `iters` times per round; the rounds alternate the order (A B, B A, A B,
+    ...) so that a drift of the clock or of the other users hits every
+    function alike. Per function: the best round's time per call, the median,
+    the spread ((worst - best) / best) and the number of rounds."""
+    graphs = {k: capture(f) for k, f in fns.items()}
+    keys = list(fns)
+    samples = {k: [] for k in keys}
+    for r in range(rounds):
+        for k in (keys if r % 2 == 0 else keys[::-1]):
+            samples[k].append(time_graph(graphs[k], iters, 2, 1) / iters / calls[k])
+    out = {}
+    for k, v in samples.items():
+        best = min(v)
+        out[k] = {"us_per_call": best * 1e6, "us_median": statistics.median(v) * 1e6,
+                  "spread": (max(v) - best) / best, "rounds": rounds}
+    del graphs
+    return out
+
+
+def eager_us(fn, calls, reps=3):
+    """Time per call of eager (not captured) calls: CUDA events around `calls`
+    back-to-back calls from Python, best of `reps` (host launch cost included)."""
+    import torch
+    best = float("inf")
+    fn()
+    torch.cuda.synchronize()
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1) * 1e3 / calls)
+    return best
+
+
+# --- oracle tasks (the CPU baseline beside every sweep row)
+
+def _oracle_run(task):
+    """One pass of a row's sampled oracle work; returns seconds."""
+    import oracle
+    orc = oracle.default()
+    t0 = time.perf_counter()
+    kind = task["kind"]
+    if kind == "w4a8":
+        a, sx, _ = orc.prep_w4a8(task["x"], task["group"], task["had"])
+        for qb, sw in task["mats"]:
+            orc.gemm_w4a8(qb, sw, a, sx, task["group"])
+    elif kind == "affine":
+        orc.gemm_affine(task["qb"], task["s"], task["b"], task["x16"])
+    elif kind == "rotated_cq4":
+        a, sx, _, _ = orc.prep_rotated(task["R"], task["x"], 128)
+        orc.gemm_cq4(task["idx"], task["C"], task["cb"], task["sw"], a, sx, 128)
+    return time.perf_counter() - t0
+
+
+def _oracle_loop(args):
+    task, seconds = args
+    n, t0 = 0, time.perf_counter()
+    while True:
+        _oracle_run(task)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return n, el
+
+
+def oracle_baselines(rows, pool, seconds=0.6):
+    """For every (row, task): the oracle's sampled work timed single-threaded
+    in this process and, in parallel, in one spawned process per host core.
+    The task's `bytes` / `ops` are the weight bytes and operations of the
+    sampled work; `full_bytes` those of the whole call."""
+    ncores = os.cpu_count() or 1
+    for row, task in rows:
+        n1, el1 = _oracle_loop((task, seconds))
+        rate1 = task["bytes"] * n1 / el1
+        base = {"kind": "oracle", "cores": 1, "sample": task["sample"],
+                "weight_GBps": rate1 / 1e9,
+                "us_per_call_est": task["full_bytes"] / rate1 * 1e6}
+        if task.get("ops"):
+            base["GOPS"] = task["ops"] * n1 / el1 / 1e9
+        if pool is not None:
+            res = pool.map(_oracle_loop, [(task, seconds)] * ncores)
+            el = max(r[1] for r in res)
+            nall = sum(r[0] for r in res)
+            allc = {"cores": ncores, "weight_GBps": task["bytes"] * nall / el / 1e9}
+            if task.get("ops"):
+                allc["GOPS"] = task["ops"] * nall / el / 1e9
+            base["all_cores"] = allc
+        gpu_gbps = row.get("weight_GBps")
+        if gpu_gbps:
+            base["gpu_speedup_vs_1_core"] = gpu_gbps / base["weight_GBps"]
+            if "all_cores" in base:
+                base["gpu_speedup_vs_all_cores"] = gpu_gbps / base["all_cores"]["weight_GBps"]
+        row["cpu_baseline"] = base
+
+
+def _sample_rows(N, n=64):
+    return np.unique(np.linspace(0, N - 1, n).astype(np.int64))
+
+
+def sweep(world, cpu=True):
     """Extra figures for the other workloads (not the headline): GEMV at
     K = N = 1024, sibling GEMVs (q | k | v) in one launch vs three, prefill
-    GEMM TOPS vs M, affine GEMM, lm_head sweep. Each call rotates over enough
-    weight copies to exceed L2 twice."""
+    GEMM TOPS vs M, affine GEMM, lm_head sweep, orthogonal lm_head. Each call
+    rotates over enough weight copies to exceed L2 twice. Every row is timed
+    by alternating best-of rounds (with its spread), once more as eager calls,
+    and beside the oracle on a row-sampled slice of the same shape (one core
+    and all host cores)."""
     import torch
     import bit_group_quantized_qmm_gb300 as q
     dev = torch.device("cuda", torch.cuda.current_device())
     out = {}
     pool_bytes = 320 << 20
+    tasks = []   # (row dict, oracle task)
 
-    def pack_pool(variant, N, K, group, name):
-        lay = qmm_synth.Layer(name, variant, N, K, group, group if variant == W4A8 else 0)
+    def pack_pool(variant, N, K, group, name, had=None):
+        lay = qmm_synth.Layer(name, variant, N, K, group,
+                              (group if variant == W4A8 else 0) if had is None else had)
         qb, s, b = qmm_synth.layer_weights(0, name, lay)
         d = q.weight_desc(variant, N, K, group)
         size = q.qmm_packed_size(d)
@@ -433,14 +562,20 @@ def sweep(world):
         q.qmm_pack_weights(d, torch.from_numpy(qb).to(dev), torch.from_numpy(s.view(np.int16)).to(dev),
                            None if b is None else torch.from_numpy(b.view(np.int16)).to(dev), first)
         pool = [first] + [first.clone() for _ in range(copies - 1)]
-        return lay, d, pool, size
+        return lay, d, pool, size, (qb, s, b)
 
-    def timed(fn, iters=20, warm=3):
-        g = capture(fn)
-        return time_graph(g, iters, warm, 1) / iters
+    def w4a8_task(hostw, x, group, had, N, K, M, label, mats=None):
+        rows = _sample_rows(N)
+        qb, sw, _ = hostw
+        mats = mats or [(qb[rows], sw[rows])]
+        nr = sum(m[0].shape[0] for m in mats)
+        per_row = K // 2 + 2 * (K // group)
+        return {"kind": "w4a8", "x": np.ascontiguousarray(x), "group": group, "had": had, "mats": mats,
+                "bytes": nr * per_row, "ops": 2 * M * nr * K, "full_bytes": N * per_row,
+                "sample": f"{label}: prepass of all {M} activation rows + {nr} of {N} output rows"}
 
     # K = N = 1024 GEMV
-    lay, d, pool, size = pack_pool(W4A8, 1024, 1024, 64, "gemv_k1024_n1024")
+    lay, d, pool, size, hostw = pack_pool(W4A8, 1024, 1024, 64, "gemv_k1024_n1024", had=0)
     x = torch.from_numpy(qmm_synth.layer_activations(0, "gemv_k1024_n1024", lay, 1)).to(dev)
     a = torch.empty(1024, dtype=torch.int8, device=dev)
     sx = torch.empty(16, dtype=torch.float32, device=dev)
@@ -455,43 +590,62 @@ def sweep(world):
     def fused_pool():   # quantization of x included
         for p in pool:
             q.qmm_gemv_fused(d, p, x[0], 0, 0, y)
-    t = timed(gemv_pool) / len(pool)
-    tf = timed(fused_pool) / len(pool)
-    out["gemv_k1024_n1024"] = {"us_per_call": t * 1e6, "weight_GBps": size / t / 1e9,
-                               "fused_us_per_call": tf * 1e6, "fused_weight_GBps": size / tf / 1e9}
+    n = len(pool)
+    t = ab_time({"gemv": gemv_pool, "fused": fused_pool}, {"gemv": n, "fused": n})
+    row = dict(t["gemv"])
+    row["weight_GBps"] = size / (row["us_per_call"] * 1e-6) / 1e9
+    row["eager_us_per_call"] = eager_us(gemv_pool, n)
+    row["fused"] = dict(t["fused"], weight_GBps=size / (t["fused"]["us_per_call"] * 1e-6) / 1e9,
+                        eager_us_per_call=eager_us(fused_pool, n))
+    out["gemv_k1024_n1024"] = row
+    tasks.append((row, w4a8_task(hostw, x.cpu().numpy(), 64, 0, 1024, 1024, 1, "K = N = 1024")))
     del pool
 
     # sibling GEMVs sharing x (q | k | v of one layer, K = 1536): one launch vs three
     Ns, K = (2048, 512, 512), 1536
     sib = []
     for i, N in enumerate(Ns):
-        lay_i, d_i, pool_i, size_i = pack_pool(W4A8, N, K, 64, f"siblings/{i}")
-        sib.append((d_i, pool_i, size_i))
+        lay_i, d_i, pool_i, size_i, host_i = pack_pool(W4A8, N, K, 64, f"siblings/{i}")
+        sib.append((d_i, pool_i, size_i, host_i))
     ncopy = min(len(p[1]) for p in sib)
-    x = torch.from_numpy(qmm_synth.layer_activations(0, "siblings/x", lay_i, 1)).to(dev)[0].contiguous()
+    xs_np = qmm_synth.layer_activations(0, "siblings/x", lay_i, 1)
+    x = torch.from_numpy(xs_np).to(dev)[0].contiguous()
     ys = [torch.empty(N, dtype=torch.float32, device=dev) for N in Ns]
     descs = [p[0] for p in sib]
     set_bytes = sum(p[2] for p in sib)
 
     def separate():
         for c in range(ncopy):
-            for (d_i, pool_i, _), y_i in zip(sib, ys):
+            for (d_i, pool_i, _, _), y_i in zip(sib, ys):
                 q.qmm_gemv_fused(d_i, pool_i[c], x, 0, 64, y_i)
 
     def together():
         for c in range(ncopy):
             q.qmm_gemv_fused_siblings(descs, [p[1][c] for p in sib], x, 0, 64, ys)
-    t_sep = timed(separate) / ncopy
-    t_tog = timed(together) / ncopy
-    out["siblings_qkv"] = {"separate_us": t_sep * 1e6, "one_launch_us": t_tog * 1e6,
-                           "weight_GBps_one_launch": set_bytes / t_tog / 1e9}
+    t = ab_time({"separate": separate, "together": together}, {"separate": ncopy, "together": ncopy})
+    row = {"one_launch_us": t["together"]["us_per_call"], "separate_us": t["separate"]["us_per_call"],
+           "one_launch_spread": t["together"]["spread"], "separate_spread": t["separate"]["spread"],
+           "rounds": t["together"]["rounds"],
+           "weight_GBps": set_bytes / (t["together"]["us_per_call"] * 1e-6) / 1e9,
+           "eager_one_launch_us": eager_us(together, ncopy), "eager_separate_us": eager_us(separate, ncopy)}
+    out["siblings_qkv"] = row
+    mats = []
+    for (_, _, _, (qb_i, sw_i, _)), N in zip(sib, Ns):
+        r_i = _sample_rows(N, 22)
+        mats.append((qb_i[r_i], sw_i[r_i]))
+    per_row = K // 2 + 2 * (K // 64)
+    nr = sum(m[0].shape[0] for m in mats)
+    tasks.append((row, {"kind": "w4a8", "x": np.ascontiguousarray(xs_np), "group": 64, "had": 64, "mats": mats,
+                        "bytes": nr * per_row, "ops": 2 * nr * K, "full_bytes": sum(Ns) * per_row,
+                        "sample": f"q|k|v: one prepass + {nr} of {sum(Ns)} output rows"}))
     del sib
 
     # prefill GEMM K=1536 N=12288 vs M
-    lay, d, pool, size = pack_pool(W4A8, 12288, 1536, 64, "prefill_gemm")
+    lay, d, pool, size, hostw = pack_pool(W4A8, 12288, 1536, 64, "prefill_gemm")
     res = {}
     for M in (16, 64, 128, 512, 1068):
-        x = torch.from_numpy(qmm_synth.layer_activations(0, f"prefill_gemm/x{M}", lay, M)).to(dev)
+        x_np = qmm_synth.layer_activations(0, f"prefill_gemm/x{M}", lay, M)
+        x = torch.from_numpy(x_np).to(dev)
         a16 = torch.empty((M, 1536), dtype=torch.float16, device=dev)
         sxm = torch.empty((M, 24), dtype=torch.float32, device=dev)
         Y = torch.empty((M, 12288), dtype=torch.float32, device=dev)
@@ -501,17 +655,21 @@ def sweep(world):
         def gemm_pool():
             for p in use:
                 q.qmm_gemm(d, p, M, a16, sxm, Y)
-        t = timed(gemm_pool) / len(use)
-        res[str(M)] = {"us_per_call": t * 1e6, "TOPS": 2 * M * 12288 * 1536 / t / 1e12,
-                       "weight_GBps": size / t / 1e9}
+        row = dict(ab_time({"g": gemm_pool}, {"g": len(use)})["g"])
+        tsec = row["us_per_call"] * 1e-6
+        row.update({"TOPS": 2 * M * 12288 * 1536 / tsec / 1e12, "weight_GBps": size / tsec / 1e9,
+                    "eager_us_per_call": eager_us(gemm_pool, len(use)), "kernel": q.qmm_last_kernel_id()})
+        res[str(M)] = row
+        tasks.append((row, w4a8_task(hostw, x_np, 64, 64, 12288, 1536, M, f"prefill M = {M}")))
     out["prefill_gemm"] = res
     del pool
 
     # affine GEMM K=5120 N=34816
-    lay, d, pool, size = pack_pool(AFFINE, 34816, 5120, 64, "affine_gemm")
+    lay, d, pool, size, (qb_a, s_a, b_a) = pack_pool(AFFINE, 34816, 5120, 64, "affine_gemm")
     res = {}
     for M in (64, 65, 128):
-        x16 = torch.from_numpy(qmm_synth.layer_activations(0, f"affine_gemm/x{M}", lay, M).view(np.float16)).to(dev)
+        x16_np = qmm_synth.layer_activations(0, f"affine_gemm/x{M}", lay, M)
+        x16 = torch.from_numpy(x16_np.view(np.float16)).to(dev)
         S = torch.empty((M, 80), dtype=torch.float32, device=dev)
         Y = torch.empty((M, 34816), dtype=torch.float32, device=dev)
         q.qmm_prep_act(AFFINE, M, 5120, 64, 0, x16, 1, gsum=S)
@@ -519,17 +677,37 @@ def sweep(world):
         def aff_pool():
             for p in pool:
                 q.qmm_gemm(d, p, M, x16, S, Y)
-        t = timed(aff_pool) / len(pool)
-        res[str(M)] = {"us_per_call": t * 1e6, "TFLOPS": 2 * M * 34816 * 5120 / t / 1e12,
-                       "weight_GBps": size / t / 1e9}
+        row = dict(ab_time({"g": aff_pool}, {"g": len(pool)}, iters=4)["g"])
+        tsec = row["us_per_call"] * 1e-6
+        row.update({"TFLOPS": 2 * M * 34816 * 5120 / tsec / 1e12, "weight_GBps": size / tsec / 1e9,
+                    "eager_us_per_call": eager_us(aff_pool, len(pool)), "kernel": q.qmm_last_kernel_id()})
+        # the element-wise error beside the norm-wise tolerance, on sampled columns
+        rows = _sample_rows(34816, 48)
+        import oracle
+        Yr, Ym = oracle.default().gemm_affine(qb_a, s_a, b_a, x16_np, rows=rows.astype(np.int32))
+        Yg = Y[:, torch.from_numpy(rows).to(dev)].double().cpu().numpy()
+        err = np.abs(Yg - Yr)
+        floor = 1e-3 * float(np.abs(Yr).max())
+        big = np.abs(Yr) > floor
+        row["max_rel_err_elementwise"] = float((err[big] / np.abs(Yr[big])).max())
+        row["rel_err_floor"] = floor
+        row["max_err_over_normwise_bound"] = float((err / (2e-3 * Ym)).max())
+        res[str(M)] = row
+        nr = rows.size
+        per_row = 5120 // 2 + 4 * 80
+        tasks.append((row, {"kind": "affine", "qb": qb_a[rows], "s": s_a[rows], "b": b_a[rows],
+                            "x16": np.ascontiguousarray(x16_np), "bytes": nr * per_row, "ops": 2 * M * nr * 5120,
+                            "full_bytes": 34816 * per_row,
+                            "sample": f"affine M = {M}: group sums + {nr} of 34816 output rows"}))
     out["affine_gemm"] = res
     del pool
 
     # lm_head sweep K=1536 N=262144 group 128
-    lay, d, pool, size = pack_pool(W4A8, 262144, 1536, 128, "lm_head")
+    lay, d, pool, size, hostw = pack_pool(W4A8, 262144, 1536, 128, "lm_head")
     res = {}
     for M in (1, 2, 4, 8, 16, 32):
-        x = torch.from_numpy(qmm_synth.layer_activations(0, f"lm_head/x{M}", lay, M)).to(dev)
+        x_np = qmm_synth.layer_activations(0, f"lm_head/x{M}", lay, M)
+        x = torch.from_numpy(x_np).to(dev)
         a = torch.empty((M, 1536), dtype=torch.int8, device=dev)
         a16 = torch.empty((M, 1536), dtype=torch.float16, device=dev)
         sxm = torch.empty((M, 12), dtype=torch.float32, device=dev)
@@ -540,17 +718,27 @@ def sweep(world):
         def gemm_pool():
             for p in pool:
                 q.qmm_gemm(d, p, M, a16, sxm, Y)
-        t = timed(gemm_pool) / len(pool)
-        entry["gemm"] = {"us_per_call": t * 1e6, "weight_GBps": size / t / 1e9}
+        fns, calls = {"gemm": gemm_pool}, {"gemm": len(pool)}
         if M == 1:
             ws1 = torch.zeros(max(16, q.qmm_gemv_workspace_size(d)), dtype=torch.uint8, device=dev)
 
             def gemv_pool2():
                 for p in pool:
                     q.qmm_gemv(d, p, a, sxm, Y, ws1, ws1.numel())
-            t = timed(gemv_pool2) / len(pool)
-            entry["gemv"] = {"us_per_call": t * 1e6, "weight_GBps": size / t / 1e9}
+            fns["gemv"], calls["gemv"] = gemv_pool2, len(pool)
+        t = ab_time(fns, calls, iters=4)
+        for k in fns:
+            r_ = dict(t[k])
+            r_["weight_GBps"] = size / (r_["us_per_call"] * 1e-6) / 1e9
+            r_["eager_us_per_call"] = eager_us(fns[k], calls[k])
+            if k == "gemm":
+                fns[k]()
+                r_["kernel"] = q.qmm_last_kernel_id()
+                r_["TOPS"] = 2 * M * 262144 * 1536 / (r_["us_per_call"] * 1e-6) / 1e12
+            entry[k] = r_
         res[str(M)] = entry
+        tasks.append((entry["gemv" if M == 1 else "gemm"],
+                      w4a8_task(hostw, x_np, 128, 128, 262144, 1536, M, f"lm_head M = {M}")))
     out["lm_head"] = res
     del pool
 
@@ -568,10 +756,12 @@ def sweep(world):
     q.qmm_pack_weights_cq4(d, torch.from_numpy(idx).to(dev), C, cb, torch.from_numpy(sw.view(np.int16)).to(dev),
                            first)
     pool = [first] + [first.clone() for _ in range(max(1, math.ceil(pool_bytes / size)) - 1)]
-    R = torch.from_numpy(qmm_synth.orthogonal_f32(0, "lm_head_orth/R", K)).to(dev)
+    R_np = qmm_synth.orthogonal_f32(0, "lm_head_orth/R", K)
+    R = torch.from_numpy(R_np).to(dev)
     res = {}
     for M in (1, 8):
-        x = torch.from_numpy(qmm_synth.layer_activations(0, f"lm_head_orth/x{M}", lay, M)).to(dev)
+        x_np = qmm_synth.layer_activations(0, f"lm_head_orth/x{M}", lay, M)
+        x = torch.from_numpy(x_np).to(dev)
         a = torch.empty((M, K), dtype=torch.int8, device=dev)
         a16 = torch.empty((M, K), dtype=torch.float16, device=dev)
         sxm = torch.empty((M, K // 128), dtype=torch.float32, device=dev)
@@ -589,31 +779,206 @@ def sweep(world):
                     q.qmm_gemv(d, p, a, sxm, Y, ws1, ws1.numel())
                 else:
                     q.qmm_gemm(d, p, M, a16, sxm, Y)
-        tp = timed(prep_only) / len(pool)
-        t = timed(prep_and_matmul) / len(pool)
-        res[str(M)] = {"prep_rotated_us": tp * 1e6, "us_per_call": t * 1e6, "weight_GBps": size / t / 1e9,
-                       "rotation_GBps": K * K * 4 / tp / 1e9}
+        t = ab_time({"prep": prep_only, "call": prep_and_matmul}, {"prep": len(pool), "call": len(pool)}, iters=4)
+        row = dict(t["call"])
+        row.update({"prep_rotated_us": t["prep"]["us_per_call"], "prep_rotated_spread": t["prep"]["spread"],
+                    "weight_GBps": size / (row["us_per_call"] * 1e-6) / 1e9,
+                    "rotation_GBps": K * K * 4 / (t["prep"]["us_per_call"] * 1e-6) / 1e9,
+                    "eager_us_per_call": eager_us(prep_and_matmul, len(pool))})
+        res[str(M)] = row
+        rows = _sample_rows(N)
+        per_row = K // 2 + 2 * (K // 128)
+        tasks.append((row, {"kind": "rotated_cq4", "R": R_np, "x": np.ascontiguousarray(x_np), "idx": idx[rows],
+                            "C": C, "cb": cb, "sw": sw[rows], "bytes": rows.size * per_row,
+                            "ops": 2 * M * rows.size * K, "full_bytes": N * per_row,
+                            "sample": f"orthogonal lm_head M = {M}: full-K rotation of x + {rows.size} of {N} "
+                                      f"output rows"}))
     out["lm_head_orth"] = res
     del pool
     torch.cuda.empty_cache()
+    if cpu:
+        import multiprocessing as mp
+        with mp.get_context("spawn").Pool(os.cpu_count() or 1) as cpu_pool:
+            oracle_baselines(tasks, cpu_pool)
     _add_fractions(out)
     return out
 
 
 def _add_fractions(node):
-    """Beside every figure of the sweep, its fraction of the measured peaks:
-    weight bytes per second over the copy bandwidth, TOPS / TFLOPS over the
-    dense bf16 rate (the rate of the kind::f16 MMAs the GEMM issues)."""
+    """Beside every figure of the sweep, its fraction of the peaks: weight
+    bytes per second over the measured copy bandwidth; TOPS / TFLOPS over the
+    measured dense bf16 rate (the rate of the kind::f16 MMAs the GEMM issues)
+    and over the mma.sync s8 peak (the int8 warp MMA, measured on this GPU)."""
     hbm, tflops, _ = measured_peaks()
+    s8 = s8_peak_tops()
     if isinstance(node, dict):
         for k in list(node):
             v = node[k]
-            if k.endswith("weight_GBps"):
+            if k.endswith("weight_GBps") and isinstance(v, (int, float)):
                 node[k.replace("weight_GBps", "frac_copy_bw")] = v / hbm
             elif k in ("TOPS", "TFLOPS"):
                 node["frac_bf16_peak"] = v / tflops
-            else:
+                node["frac_s8_peak"] = v / s8
+            elif k != "cpu_baseline":
                 _add_fractions(v)
+
+
+# ------------------------------------------------------------------ per-projection figures of the headline
+
+def projection_rows(model):
+    """Per projection of the decode step: one fused launch per layer of that
+    projection alone, over enough weight copies to exceed L2 twice, the four
+    projections timed by alternating best-of rounds. Algorithmic bytes per
+    launch: packed nibbles and scales, fp32 x in, fp32 y out."""
+    q = model.q
+    fns, calls, nbytes, keep = {}, {}, {}, []
+    for name, N, K in PROJ:
+        ps = [p for p in model.projs if p["name"] == name]
+        blobs = [p["packed"] for p in ps]
+        size = q.qmm_packed_size(ps[0]["d"])
+        while len(blobs) * size < (256 << 20):
+            blobs = blobs + [b.clone() for b in blobs[:len(ps)]]
+        keep.append(blobs)
+        d = ps[0]["d"]
+        x = model.x[ps[0]["x_off"]:ps[0]["x_off"] + K]
+        y = model.y[ps[0]["y_off"]:ps[0]["y_off"] + N]
+
+        def f(blobs=blobs, d=d, x=x, y=y):
+            for b in blobs:
+                q.qmm_gemv_fused(d, b, x, 0, GROUP, y)
+        fns[name], calls[name], nbytes[name] = f, len(blobs), size
+    t = ab_time(fns, calls, rounds=6, iters=20)
+    hbm, _, _ = measured_peaks()
+    out = {}
+    for name, N, K in PROJ:
+        r = t[name]
+        alg = nbytes[name] + 4 * K + 4 * N
+        gbps = alg / (r["us_per_call"] * 1e-6) / 1e9
+        out[name] = {"N": N, "K": K, "us_per_launch": r["us_per_call"], "us_median": r["us_median"],
+                     "spread": r["spread"], "rounds": r["rounds"], "algorithmic_bytes": alg, "GBps": gbps,
+                     "frac_copy_bw": gbps / hbm, "copies": calls[name]}
+    return out
+
+
+# ------------------------------------------------------------------ peaks of the non-tensor-memory units
+
+PEAKS_CU = r'''
+// FP32 FMA (scalar and packed pairs) and legacy warp-MMA (mma.sync) rates:
+// one CTA per SM, clock64 per CTA, the slowest CTA counts; the warp-MMA rates
+// are the best over 4, 8 and 16 warps per SM.
+#include <cstdio>
+#include <cstdint>
+#include <cuda_runtime.h>
+__global__ void __launch_bounds__(1024, 1) fp32(int iters, int packed, long long* cyc, float* sink)
+{
+    float a[16];
+    for (int i = 0; i < 16; ++i) a[i] = threadIdx.x * 1e-7f + i;
+    const float b = 0.999f, c = 1e-6f;
+    __syncthreads();
+    const long long t0 = clock64();
+    if (!packed) {
+        for (int it = 0; it < iters; ++it)
+#pragma unroll
+            for (int i = 0; i < 16; ++i) asm volatile("fma.rn.f32 %0, %0, %1, %2;" : "+f"(a[i]) : "f"(b), "f"(c));
+    } else {
+        unsigned long long p[8], bb, cc;
+        for (int i = 0; i < 8; ++i) asm("mov.b64 %0, {%1, %2};" : "=l"(p[i]) : "f"(a[2 * i]), "f"(a[2 * i + 1]));
+        asm("mov.b64 %0, {%1, %1};" : "=l"(bb) : "f"(b));
+        asm("mov.b64 %0, {%1, %1};" : "=l"(cc) : "f"(c));
+        for (int it = 0; it < iters; ++it)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) asm volatile("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(p[i]) : "l"(bb), "l"(cc));
+        for (int i = 0; i < 8; ++i) asm("mov.b64 {%0, %1}, %2;" : "=f"(a[2 * i]), "=f"(a[2 * i + 1]) : "l"(p[i]));
+    }
+    __syncthreads();
+    const long long t1 = clock64();
+    float s = 0.f;
+    for (int i = 0; i < 16; ++i) s += a[i];
+    if (s == 12345.f) sink[threadIdx.x] = s;
+    if (threadIdx.x == 0) cyc[blockIdx.x] = t1 - t0;
+}
+__global__ void __launch_bounds__(512, 1) mmas(int iters, int mode, long long* cyc, int* sink)
+{
+    uint32_t a0 = threadIdx.x, a1 = a0 * 3, a2 = a0 * 5, a3 = a0 * 7, b0 = a0 * 11, b1 = a0 * 13;
+    uint32_t d[8][4];
+    for (int i = 0; i < 8; ++i)
+        for (int j = 0; j < 4; ++j) d[i][j] = 0;
+    if (mode == 1) { a0 &= 0x3C003C00u; a1 &= 0x3C003C00u; a2 &= 0x3C003C00u; a3 &= 0x3C003C00u; b0 &= 0x3C003C00u; b1 &= 0x3C003C00u; }
+    __syncthreads();
+    const long long t0 = clock64();
+    for (int it = 0; it < iters; ++it)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (mode == 0)
+                asm volatile("mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                             : "+r"(d[i][0]), "+r"(d[i][1]), "+r"(d[i][2]), "+r"(d[i][3])
+                             : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+            else
+                asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                             : "+r"(d[i][0]), "+r"(d[i][1]), "+r"(d[i][2]), "+r"(d[i][3])
+                             : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+        }
+    __syncthreads();
+    const long long t1 = clock64();
+    int s = 0;
+    for (int i = 0; i < 8; ++i)
+        for (int j = 0; j < 4; ++j) s += (int)d[i][j];
+    if (s == 12345) sink[threadIdx.x] = s;
+    if (threadIdx.x == 0) cyc[blockIdx.x] = t1 - t0;
+}
+static long long slowest(long long* dcyc, int n)
+{
+    long long h[1024], mx = 0;
+    cudaMemcpy(h, dcyc, 8 * n, cudaMemcpyDeviceToHost);
+    for (int i = 0; i < n; ++i) mx = h[i] > mx ? h[i] : mx;
+    return mx;
+}
+int main()
+{
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0);
+    long long* cyc; float* fs; int* is;
+    cudaMalloc(&cyc, 8 * 1024); cudaMalloc(&fs, 4 * 1024); cudaMalloc(&is, 4 * 1024);
+    double best[4] = {0, 0, 0, 0};
+    for (int rep = 0; rep < 3; ++rep) {
+        for (int packed = 0; packed < 2; ++packed) {
+            fp32<<<sms, 1024>>>(4096, packed, cyc, fs);
+            if (cudaDeviceSynchronize() != cudaSuccess) return 1;
+            const double r = 1024.0 * 4096 * 16 / slowest(cyc, sms);
+            if (r > best[packed]) best[packed] = r;
+        }
+        for (int mode = 0; mode < 2; ++mode)
+            for (int threads = 128; threads <= 512; threads *= 2) {
+                mmas<<<sms, threads>>>(1024, mode, cyc, is);
+                if (cudaDeviceSynchronize() != cudaSuccess) return 1;
+                const double r = (threads / 32) * 1024.0 * 8 * (mode == 0 ? 16 * 8 * 32 : 16 * 8 * 16) / slowest(cyc, sms);
+                if (r > best[2 + mode]) best[2 + mode] = r;
+            }
+    }
+    printf("{\"sms\": %d, \"fma_f32_lane_ops_per_clk_sm\": %.1f, \"fma_f32x2_lane_ops_per_clk_sm\": %.1f, "
+           "\"mma_sync_s8_mac_per_clk_sm\": %.1f, \"mma_sync_f16_mac_per_clk_sm\": %.1f}\n",
+           sms, best[0], best[1], best[2], best[3]);
+    return 0;
+}
+'''
+
+
+def run_peaks():
+    """Compile and run the FP32 / mma.sync microbenchmark; print its JSON line
+    with the s8 peak in TOPS at the measured maximum SM clock."""
+    import shutil
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    with tempfile.TemporaryDirectory() as tmp:
+        src = os.path.join(tmp, "peaks.cu")
+        exe = os.path.join(tmp, "peaks")
+        with open(src, "w") as f:
+            f.write(PEAKS_CU)
+        subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-o", exe, src], check=True)
+        res = subprocess.run([exe], capture_output=True, text=True, check=True)
+    d = json.loads(res.stdout.strip().splitlines()[-1])
+    d["mma_sync_s8_tops_at_max_clock"] = 2.0 * d["mma_sync_s8_mac_per_clk_sm"] * d["sms"] * 2070e6 / 1e12
+    d["tcgen05_kind_f16_mac_per_clk_sm_nominal"] = 4096
+    print(json.dumps(d), flush=True)
 
 
 def profile_case(spec):
@@ -770,6 +1135,9 @@ def profile_case(spec):
 def main():
     args = parse_args()
     rank, world, local = dist_env()
+    if args.peaks:
+        run_peaks()
+        return
     if args.profile_case:
         import torch
         torch.cuda.set_device(local)
@@ -839,6 +1207,8 @@ def main():
     barrier(world)
     t_e2e = max_over_ranks(t_e2e, world)
 
+    per_projection = projection_rows(model) if rank == 0 and not args.no_sweep else None
+
     total_weight = sum_over_ranks(model.weight_bytes * args.steps, world)
     value = total_weight / t_step / 1e9
     e2e_value = sum_over_ranks(model.weight_bytes * e2e_steps, world) / t_e2e / 1e9
@@ -849,7 +1219,7 @@ def main():
 
     sweep_out = None
     if not args.no_sweep and rank == 0:
-        sweep_out = sweep(1 if world == 1 else world)
+        sweep_out = sweep(1 if world == 1 else world, cpu=not args.no_cpu_baseline)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -902,6 +1272,7 @@ def main():
                 "avg_launch_us": gemv_launch_s * 1e6,
                 "frac_of_8TBps": achieved / 8000.0,
             },
+            "per_projection": per_projection,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": model.h2d_bytes,
                     "d2h_bytes_per_step": model.d2h_bytes, "steps": e2e_steps,

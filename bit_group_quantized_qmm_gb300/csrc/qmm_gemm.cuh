@@ -621,10 +621,17 @@ cudaError_t run_gemm(const LaunchCtx& c, const CUtensorMap& map, const GemmShape
         regs_seen.store(regs, std::memory_order_relaxed);
     }
     if (regs * kGemmThreads != 65536) return cudaErrorInvalidConfiguration;
-    int occ = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kGemmThreads, smem);
-    if (e != cudaSuccess) return e;
-    if (occ < 1) return cudaErrorInvalidConfiguration;
+    // blocks per SM for this shared-memory size (the same on every supported
+    // device), asked once and cached as one word: shared-memory bytes << 8 | blocks
+    static std::atomic<uint64_t> occ_cache{0};
+    const uint64_t cached = occ_cache.load(std::memory_order_relaxed);
+    int occ = (cached >> 8) == (uint64_t)smem ? (int)(cached & 0xFF) : 0;
+    if (occ == 0) {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kGemmThreads, smem);
+        if (e != cudaSuccess) return e;
+        if (occ < 1) return cudaErrorInvalidConfiguration;
+        occ_cache.store(((uint64_t)smem << 8) | (uint64_t)(occ & 0xFF), std::memory_order_relaxed);
+    }
     int per_sm = occ;
     if (per_sm * sh.tmem_cols > 512) per_sm = 512 / sh.tmem_cols;
     const int grid = sh.num_tiles < c.num_sms * per_sm ? sh.num_tiles : c.num_sms * per_sm;

@@ -44,3 +44,39 @@ def test_sweep_fractions_use_the_measured_peaks():
     assert abs(node["a"]["frac_bf16_peak"] - 0.25) < 1e-12
     assert abs(node["b"]["1"]["gemv"]["frac_copy_bw"] - 1.0) < 1e-12
     assert abs(node["b"]["fused_frac_copy_bw"] - 0.25) < 1e-12
+
+
+def test_sweep_fractions_include_the_s8_peak():
+    node = {"a": {"TOPS": bench.s8_peak_tops()}, "cpu_baseline": {"weight_GBps": 1.0}}
+    bench._add_fractions(node)
+    assert abs(node["a"]["frac_s8_peak"] - 1.0) < 1e-12
+    assert "frac_copy_bw" not in node["cpu_baseline"]   # the oracle's own figures stay as they are
+
+
+def test_s8_peak_from_the_measured_rate():
+    # 252 MACs per clock per SM, 2 operations per MAC, 152 SMs, at 2070 MHz
+    assert abs(bench.s8_peak_tops(2070.0) - 2 * 252 * 152 * 2070e6 / 1e12) < 1e-9
+
+
+def test_oracle_baseline_of_a_sweep_row():
+    """A sweep row's CPU baseline: the oracle's sampled work timed on one core,
+    the rate per weight byte, the estimate for the whole call, the speed-up."""
+    import numpy as np
+    import qmm_synth
+    N, K, g = 256, 256, 64
+    lay = qmm_synth.Layer("bench_host", 0, N, K, g, g)
+    qb, sw, _ = qmm_synth.layer_weights(0, "bench_host", lay)
+    x = qmm_synth.layer_activations(0, "bench_host", lay, 2)
+    rows = bench._sample_rows(N, 16)
+    per_row = K // 2 + 2 * (K // g)
+    task = {"kind": "w4a8", "x": x, "group": g, "had": g, "mats": [(qb[rows], sw[rows])],
+            "bytes": rows.size * per_row, "ops": 2 * 2 * rows.size * K, "full_bytes": N * per_row,
+            "sample": "test"}
+    row = {"weight_GBps": 100.0}
+    bench.oracle_baselines([(row, task)], None, seconds=0.05)
+    base = row["cpu_baseline"]
+    assert base["kind"] == "oracle" and base["cores"] == 1 and base["sample"] == "test"
+    assert base["weight_GBps"] > 0 and base["GOPS"] > 0
+    assert abs(base["us_per_call_est"] - N * per_row / (base["weight_GBps"] * 1e9) * 1e6) < 1e-6
+    assert abs(base["gpu_speedup_vs_1_core"] - 100.0 / base["weight_GBps"]) < 1e-9
+    assert np.isfinite(base["us_per_call_est"])
