@@ -12,6 +12,9 @@ reproduces z exactly). The codes of qmm_prep_act, of the fused decode GEMV's
 prepass and of the full-K rotation prepass (with an identity and a signed
 permutation as the rotation, which move values exactly) must equal the
 oracle's bit for bit, and the tie positions must round to the even neighbour.
+The largest tie is +-126.5: a tie at the clamp edge (+-127.5) cannot occur,
+since every |v| is at most amax = 127 s, so |v / s| never exceeds 127 by more
+than the division's rounding.
 """
 
 import numpy as np
