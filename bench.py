@@ -524,12 +524,22 @@ def oracle_baselines(rows, pool, seconds=0.6):
             if task.get("ops"):
                 allc["GOPS"] = task["ops"] * nall / el / 1e9
             base["all_cores"] = allc
+        if "all_cores" in base:
+            base["all_cores"]["us_per_call_est"] = task["full_bytes"] / (base["all_cores"]["weight_GBps"] * 1e9) * 1e6
         gpu_gbps = row.get("weight_GBps")
         if gpu_gbps:
             base["gpu_speedup_vs_1_core"] = gpu_gbps / base["weight_GBps"]
             if "all_cores" in base:
                 base["gpu_speedup_vs_all_cores"] = gpu_gbps / base["all_cores"]["weight_GBps"]
         row["cpu_baseline"] = base
+        # the same figures flat on the row, beside the GPU's
+        row["oracle_us"] = base["us_per_call_est"]
+        row["oracle_GBps"] = base["weight_GBps"]
+        row["oracle_cores"] = 1
+        if "all_cores" in base:
+            row["oracle_all_cores_us"] = base["all_cores"]["us_per_call_est"]
+            row["oracle_all_cores_GBps"] = base["all_cores"]["weight_GBps"]
+            row["oracle_all_cores"] = base["all_cores"]["cores"]
 
 
 def _sample_rows(N, n=64):

@@ -80,3 +80,6 @@ def test_oracle_baseline_of_a_sweep_row():
     assert abs(base["us_per_call_est"] - N * per_row / (base["weight_GBps"] * 1e9) * 1e6) < 1e-6
     assert abs(base["gpu_speedup_vs_1_core"] - 100.0 / base["weight_GBps"]) < 1e-9
     assert np.isfinite(base["us_per_call_est"])
+    # the same figures flat on the row
+    assert row["oracle_us"] == base["us_per_call_est"] and row["oracle_GBps"] == base["weight_GBps"]
+    assert row["oracle_cores"] == 1 and "oracle_all_cores" not in row
