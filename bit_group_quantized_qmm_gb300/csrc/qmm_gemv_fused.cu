@@ -266,9 +266,11 @@ __global__ void __launch_bounds__(kThreads)
         // ---------------------------------------------------------- phase B
         const int r = tid & 127, h = tid >> 7;
         float acc = 0.f;
+        // one group's exact partial as four independent dp4a chains (one per
+        // 32-bit word of a piece; integer sums, so the order is free)
         auto partial = [&](int i) {
             const uint8_t* c = stages + (size_t)i * C::CB;
-            int dp = 0;
+            int d0 = 0, d1 = 0, d2 = 0, d3 = 0;
 #pragma unroll
             for (int p = 0; p < C::PP; ++p) {
                 const uint4 w = *reinterpret_cast<const uint4*>(c + p * 2048 + r * 16);
@@ -277,28 +279,29 @@ __global__ void __launch_bounds__(kThreads)
                 if (CQ) {
                     uint32_t lo, hi;
                     cq4_expand(book, w.x, lo, hi);
-                    dp = __dp4a((int)lo, (int)a0.x, dp);
-                    dp = __dp4a((int)hi, (int)a0.y, dp);
+                    d0 = __dp4a((int)lo, (int)a0.x, d0);
+                    d0 = __dp4a((int)hi, (int)a0.y, d0);
                     cq4_expand(book, w.y, lo, hi);
-                    dp = __dp4a((int)lo, (int)a0.z, dp);
-                    dp = __dp4a((int)hi, (int)a0.w, dp);
+                    d1 = __dp4a((int)lo, (int)a0.z, d1);
+                    d1 = __dp4a((int)hi, (int)a0.w, d1);
                     cq4_expand(book, w.z, lo, hi);
-                    dp = __dp4a((int)lo, (int)a1.x, dp);
-                    dp = __dp4a((int)hi, (int)a1.y, dp);
+                    d2 = __dp4a((int)lo, (int)a1.x, d2);
+                    d2 = __dp4a((int)hi, (int)a1.y, d2);
                     cq4_expand(book, w.w, lo, hi);
-                    dp = __dp4a((int)lo, (int)a1.z, dp);
-                    dp = __dp4a((int)hi, (int)a1.w, dp);
+                    d3 = __dp4a((int)lo, (int)a1.z, d3);
+                    d3 = __dp4a((int)hi, (int)a1.w, d3);
                 } else {
-                    dp = __dp4a(nib_lo16(w.x), (int)a0.x, dp);
-                    dp = __dp4a(nib_hi16(w.x), (int)a0.y, dp);
-                    dp = __dp4a(nib_lo16(w.y), (int)a0.z, dp);
-                    dp = __dp4a(nib_hi16(w.y), (int)a0.w, dp);
-                    dp = __dp4a(nib_lo16(w.z), (int)a1.x, dp);
-                    dp = __dp4a(nib_hi16(w.z), (int)a1.y, dp);
-                    dp = __dp4a(nib_lo16(w.w), (int)a1.z, dp);
-                    dp = __dp4a(nib_hi16(w.w), (int)a1.w, dp);
+                    d0 = __dp4a(nib_lo16(w.x), (int)a0.x, d0);
+                    d0 = __dp4a(nib_hi16(w.x), (int)a0.y, d0);
+                    d1 = __dp4a(nib_lo16(w.y), (int)a0.z, d1);
+                    d1 = __dp4a(nib_hi16(w.y), (int)a0.w, d1);
+                    d2 = __dp4a(nib_lo16(w.z), (int)a1.x, d2);
+                    d2 = __dp4a(nib_hi16(w.z), (int)a1.y, d2);
+                    d3 = __dp4a(nib_lo16(w.w), (int)a1.z, d3);
+                    d3 = __dp4a(nib_hi16(w.w), (int)a1.w, d3);
                 }
             }
+            const int dp = (d0 + d1) + (d2 + d3);
             return CQ ? dp : dp >> 4;   // symmetric: every product carried a factor 16
         };
         // two groups per step (independent dp4a chains), added in group order
