@@ -415,10 +415,10 @@ def run_reference(args, rank, world):
 # ------------------------------------------------------------------ sweep of the other workloads
 
 # Peak of the legacy warp-level int8 MMA (mma.sync.m16n8k32.s8, int32
-# accumulators) on this GPU, measured with `python bench.py --peaks`: 252 MACs
+# accumulators) on this GPU, measured with `python bench.py --peaks`: 223 MACs
 # per clock per SM (the tcgen05 kind::f16 MMA the GEMM issues does 4096). The
 # sweep reports every GEMM's TOPS against it beside the bf16 figure.
-MMA_SYNC_S8_MAC_PER_CLK_SM = 252.0
+MMA_SYNC_S8_MAC_PER_CLK_SM = 223.0
 
 
 def s8_peak_tops(sm_mhz=None):

@@ -54,8 +54,8 @@ def test_sweep_fractions_include_the_s8_peak():
 
 
 def test_s8_peak_from_the_measured_rate():
-    # 252 MACs per clock per SM, 2 operations per MAC, 152 SMs, at 2070 MHz
-    assert abs(bench.s8_peak_tops(2070.0) - 2 * 252 * 152 * 2070e6 / 1e12) < 1e-9
+    # 223 MACs per clock per SM, 2 operations per MAC, 152 SMs, at 2070 MHz
+    assert abs(bench.s8_peak_tops(2070.0) - 2 * 223 * 152 * 2070e6 / 1e12) < 1e-9
 
 
 def test_oracle_baseline_of_a_sweep_row():
