@@ -14,7 +14,10 @@ import os
 import re
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libqmm_gb300.so")
+# QMM_CHECKED_LIBRARY=1 loads the test-only checked variant (same kernels with
+# internal range checks recorded in the device error word; see build.py)
+LIB_PATH = os.path.join(HERE, "libqmm_gb300_checked.so" if os.environ.get("QMM_CHECKED_LIBRARY") == "1"
+                        else "libqmm_gb300.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "qmm.h")
 
 QMM_W4A8 = 0
@@ -43,7 +46,7 @@ class qmm_weight_desc(ctypes.Structure):
 
 def _load():
     if not os.path.exists(LIB_PATH):
-        raise ImportError(f"libqmm_gb300.so not built ({LIB_PATH}); run __graft_entry__.build()")
+        raise ImportError(f"{os.path.basename(LIB_PATH)} not built ({LIB_PATH}); run __graft_entry__.build()")
     L = ctypes.CDLL(LIB_PATH)
     P, I32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
     D = ctypes.POINTER(qmm_weight_desc)

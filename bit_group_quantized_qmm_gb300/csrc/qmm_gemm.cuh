@@ -249,6 +249,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = sh.K / GROUP;
+    const size_t n_chunks = (size_t)((sh.N + 127) / 128) * G;   // chunks in the blob
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < RS; ++i) {
@@ -298,6 +299,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             ok = false;
                             break;
                         }
+                        // the chunk lies inside the blob
+                        if (!in_range((size_t)(tile / sh.mt_count) * G + g < n_chunks, status)) {
+                            *abort = 1;
+                            ok = false;
+                            break;
+                        }
                         mbar_arrive_expect_tx(&raw_full[rs], C::CB);
                         bulk_g2s(raw + (size_t)rs * C::CB, src + (size_t)g * C::CB, C::CB, &raw_full[rs]);
                         ++issued;
@@ -314,7 +321,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const uint32_t idesc = idesc_f16_f32(128, m_tile);
                 int ks = 0, db = 0;
                 uint32_t kph = 0, dph = 0;
-                bool ok = true;
+                // accumulators below the weight-operand stages, stages inside
+                // the allocation
+                bool ok = in_range(DS * sh.d_stride <= (int)a_col0 && m_tile <= sh.d_stride &&
+                                       (!A_TMEM || (int)a_col0 + 32 * KS <= sh.tmem_cols),
+                                   status);
+                if (!ok) *abort = 1;
                 for (int tile = blockIdx.x; ok && tile < sh.num_tiles; tile += gridDim.x) {
                     for (int g = 0; ok && g < G; ++g) {
                         if (!mbar_wait(&d_empty[db], dph ^ 1u, status, abort)) {
@@ -371,6 +383,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     // asynchronous copies: the slot's barrier completes when every
                     // lane's copies have landed
+                    if (!in_range((size_t)nt * G + g < n_chunks, status)) {
+                        *abort = 1;
+                        ok = false;
+                        break;
+                    }
                     uint8_t* st = scs + (size_t)xs * ssb;
                     const uint8_t* ws = wsrc + (size_t)g * C::CB;
 #pragma unroll
@@ -505,7 +522,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0;
         int db = 0, xs = 0;
         uint32_t dph = 0, xph = 0;
-        bool ok = true;
+        // the columns read per group lie inside the accumulator buffer and the
+        // scale stage's activation-scale region (the raw-partials hook reads
+        // only live columns)
+        bool ok = in_range(DEBUG || c0 + MAXC <= sh.d_stride, status);
+        if (!ok) *abort = 1;
         const float out_scale =
             VARIANT == 2 ? *reinterpret_cast<const float*>(blob + cq4_trailer_offset(sh.N, sh.K, GROUP) + 16) : 1.f;
         pdl_wait();   // outputs may still be read by the previous kernel

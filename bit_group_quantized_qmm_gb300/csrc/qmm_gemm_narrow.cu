@@ -172,6 +172,12 @@ __global__ void __launch_bounds__(kNwThreads, 1)
                         ok = false;
                         break;
                     }
+                    // both chunks lie inside the blob
+                    if (!in_range((size_t)(2 * tp + (two ? 1 : 0)) * G + g < (size_t)T * G, status)) {
+                        *abort = 1;
+                        ok = false;
+                        break;
+                    }
                     uint8_t* dst = wst + (size_t)ws * 2 * C::CB;
                     mbar_arrive_expect_tx(&w_full[ws], (uint32_t)(two ? 2 * C::CB : C::CB));
                     bulk_g2s(dst, src0 + (size_t)g * C::CB, C::CB, &w_full[ws]);
@@ -338,7 +344,10 @@ __global__ void __launch_bounds__(kNwThreads, 1)
             VARIANT == 2 ? *reinterpret_cast<const float*>(blob + cq4_trailer_offset(N, K, GROUP) + 16) : 1.f;
         int db = 0, xs = 0;
         uint32_t dph = 0, xph = 0;
-        bool ok = true;
+        // the 32 columns read from either accumulator buffer lie inside the
+        // 512-column allocation
+        bool ok = in_range((kNwDS - 1) * kNwRows + c0 + 32 <= 512, status);
+        if (!ok) *abort = 1;
         pdl_wait();   // outputs may still be read by the previous kernel
         for (int tp = blockIdx.x; ok && tp < TP; tp += gridDim.x) {
             unsigned long long acc[16];

@@ -133,12 +133,17 @@ __global__ void __launch_bounds__(kThreads)
         // producer: the whole slice, before the dependency wait
         if (lane == 0) {
             const uint8_t* src = blob + ((size_t)t * G + g0) * C::CB;
+            const size_t n_chunks = (size_t)((N + 127) / 128) * G;
             for (int i = 0; i < ng; ++i) {
+                // the chunk lies inside the blob (a skipped chunk leaves its
+                // consumers to their bounded waits)
+                if (!in_range((size_t)t * G + g0 + i < n_chunks, status)) continue;
                 mbar_arrive_expect_tx(&full[i], C::CB);
                 bulk_g2s(stages + (size_t)i * C::CB, src + (size_t)i * C::CB, C::CB, &full[i]);
             }
             // the CTA must not exit with copies in flight
-            for (int i = 0; i < ng; ++i) mbar_wait(&full[i], 0, status, nullptr);
+            for (int i = 0; i < ng; ++i)
+                if (!QMM_CHECKS || (size_t)t * G + g0 + i < n_chunks) mbar_wait(&full[i], 0, status, nullptr);
         }
         __syncwarp();
         return;
@@ -375,6 +380,10 @@ __global__ void __launch_bounds__(kThreads)
                         const int ga = G * q / NS, gz = G * (q + 1) / NS;
                         if (stop || ga + i >= gz) continue;
                         if (n[q] >= (uint32_t)RS && !mbar_wait(&empty[q * RS + st[q]], ph[q], status, abort)) {
+                            stop = true;
+                            continue;
+                        }
+                        if (!in_range((size_t)t * G + ga + i < (size_t)T * G, status)) {
                             stop = true;
                             continue;
                         }

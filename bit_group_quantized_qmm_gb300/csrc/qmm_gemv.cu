@@ -104,14 +104,18 @@ __global__ void __launch_bounds__(kGemvThreads)
         // copies start before the dependency wait
         if (lane == 0) {
             const uint8_t* src = blob + ((size_t)t * G + g0) * C::CB;
+            int issued = 0;
             for (int i = 0; i < ng; ++i) {
                 const int st = i % ring;
                 if (i >= ring && !mbar_wait(&empty[st], ((i / ring) - 1) & 1, status, abort)) break;
+                // the chunk lies inside the blob
+                if (!in_range((size_t)t * G + g0 + i < (size_t)((N + 127) / 128) * G, status)) break;
                 mbar_arrive_expect_tx(&full[st], C::CB);
                 bulk_g2s(stages + (size_t)st * C::CB, src + (size_t)i * C::CB, C::CB, &full[st]);
+                ++issued;
             }
             // the CTA must not exit with copies in flight: wait for the last ones
-            for (int i = ng - ring > 0 ? ng - ring : 0; i < ng; ++i)
+            for (int i = issued - ring > 0 ? issued - ring : 0; i < issued; ++i)
                 mbar_wait(&full[i % ring], (i / ring) & 1, status, nullptr);
         }
         return;

@@ -142,11 +142,16 @@ __global__ void __launch_bounds__(kThreads)
         if (lane == 0) {
             const uint8_t* src = blob + ((size_t)t * G + g0) * C::CB;
             for (int i = 0; i < ng; ++i) {
+                // the chunk lies inside the blob (a skipped chunk is never
+                // waited for below: its consumers' bounded waits run out)
+                if (!in_range((size_t)t * G + g0 + i < (size_t)((N + 127) / 128) * G, status)) continue;
                 mbar_arrive_expect_tx(&full[i], C::CB);
                 bulk_g2s(stages + (size_t)i * C::CB, src + (size_t)i * C::CB, C::CB, &full[i]);
             }
             // the CTA must not exit with copies in flight
-            for (int i = 0; i < ng; ++i) mbar_wait(&full[i], 0, status, nullptr);
+            for (int i = 0; i < ng; ++i)
+                if (!QMM_CHECKS || (size_t)t * G + g0 + i < (size_t)((N + 127) / 128) * G)
+                    mbar_wait(&full[i], 0, status, nullptr);
         }
         __syncwarp();
     } else {

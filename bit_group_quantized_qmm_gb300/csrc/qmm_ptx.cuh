@@ -12,6 +12,14 @@ namespace qmm {
 
 // Device error word bits (read back by qmm_device_status).
 constexpr int kErrTimeout = 1;
+// Checked builds (QMM_CHECKS=1: the test-only library variant): an internal
+// index range that fails its check sets kErrBounds in the device error word
+// and the access is skipped (a skipped copy leaves its consumer to a bounded
+// wait). Normal builds compile the checks away.
+#ifndef QMM_CHECKS
+#define QMM_CHECKS 0
+#endif
+constexpr int kErrBounds = 2;
 
 // A bounded wait gives up after this many SM clock cycles.
 constexpr long long kWaitLimitCycles = 4000000000ll;
@@ -34,6 +42,17 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 // Allow the next grid in the stream to be scheduled.
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// True when `ok`; otherwise (checked builds only) records kErrBounds and
+// returns false.
+__device__ __forceinline__ bool in_range(bool ok, int* status)
+{
+    if (QMM_CHECKS && !ok) {
+        if (status) atomicOr(status, kErrBounds);
+        return false;
+    }
+    return true;
+}
 
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
