@@ -82,6 +82,11 @@ struct GemmCfg {
     static constexpr int KS_TMEM = NARROW ? 8 : 4;   // k-step stages, weight operand in tensor memory
     static constexpr int KS_SMEM = 4;                // k-step stages, weight operand in shared memory
     static constexpr int DS = MAXC <= 48 ? 4 : 3;    // accumulator buffers
+    // Narrow tiles relay the accumulator-buffer wait through the expand warps:
+    // there the MMA-issuing thread's loop is the critical path (two mbarrier
+    // waits, four MMAs and two commits per group, each wait ~150 cycles of
+    // that thread), while the expand warps have slack.
+    static constexpr bool RELAY = NARROW;
     // epilogue columns per tensor-memory round trip: the whole group
     static constexpr int EB = MAXC;
     static constexpr int XS = 16;                    // scale stages
@@ -329,7 +334,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if (!ok) *abort = 1;
                 for (int tile = blockIdx.x; ok && tile < sh.num_tiles; tile += gridDim.x) {
                     for (int g = 0; ok && g < G; ++g) {
-                        if (!mbar_wait(&d_empty[db], dph ^ 1u, status, abort)) {
+                        // the group's accumulator buffer has been drained (with the
+                        // relay, the first k-step's barrier below implies it)
+                        if (!C::RELAY && !mbar_wait(&d_empty[db], dph ^ 1u, status, abort)) {
                             ok = false;
                             break;
                         }
@@ -438,8 +445,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int set = warp >> 2;         // with two sets, set s takes the groups g % 2 == s
         Cq4Book book = {};
         if (VARIANT == 2) book = cq4_load(blob + cq4_trailer_offset(sh.N, sh.K, GROUP), 0x80808080u);
-        int rs = 0, ks = 0, turn = 0;
-        uint32_t rph = 0, kph = 0;
+        int rs = 0, ks = 0, turn = 0, db = 0;
+        uint32_t rph = 0, kph = 0, dph = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < sh.num_tiles; tile += gridDim.x) {
             for (int g = 0; ok && g < G; ++g) {
@@ -450,6 +457,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                         for (int j = 0; j < KSG; ++j) ring_next<KS>(ks, kph);
                         ring_next<RS>(rs, rph);
+                        ring_next<DS>(db, dph);
                         continue;
                     }
                 }
@@ -504,11 +512,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                 make_uint4(hv[4 * c], hv[4 * c + 1], hv[4 * c + 2], hv[4 * c + 3]);
                         fence_proxy_async_smem();
                     }
+                    // relay: the group's first k-step is released to the MMA warp
+                    // only once the epilogue has drained the group's accumulator
+                    // buffer (one lane of the set's first warp waits)
+                    if (C::RELAY && j == 0 && wq == 0 && lane == 0 && !mbar_wait(&d_empty[db], dph ^ 1u, status, abort))
+                        ok = false;
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&k_full[ks]);
                     ring_next<KS>(ks, kph);
                 }
                 ring_next<RS>(rs, rph);
+                ring_next<DS>(db, dph);
             }
         }
     } else {
