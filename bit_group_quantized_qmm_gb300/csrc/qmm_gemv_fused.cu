@@ -37,11 +37,22 @@ namespace {
 
 constexpr int kComputeThreads = 256;
 constexpr int kThreads = kComputeThreads + 32;   // + producer warp
-// CTAs a launch aims at (K-slices per tile = ceil(kTargetCtas / tiles), at most
-// one 16-CTA cluster): about 1.3 per SM. Measured on the Gemma-shaped decode
-// projections (K-slices of gate_up / down / q / o = 3 / 16 / 13 / 16): 0.380
-// ms per 32-layer step against 0.426 ms at 2 per SM (4 / 16 / 16 / 16).
+// Launch shape, measured on the 32-layer Gemma-shaped decode step (ms per
+// step, alternating best-of rounds). K-slices per tile: ceil(kTargetCtas /
+// tiles), at most one 16-CTA cluster (about 1.3 CTAs per SM: 0.380 against
+// 0.426 at 2 per SM), raised so that a CTA holds at most kMaxGroupsPerCta
+// groups as long as the grid stays within kCtasPerSm resident CTAs per SM;
+// and when the whole grid fits that way, each CTA takes at least
+// kMinSmemPerCta of shared memory, so that no SM holds more than kCtasPerSm of
+// them (the block scheduler otherwise stacked up to 5 gate_up CTAs on an SM
+// whose weight copies then landed last). K-slices of gate_up / down / q / o
+// become 4 / 16 / 13 / 16 (from 3 / 16 / 13 / 16): 0.367 against 0.382; the
+// shared-memory floor alone 0.378, the gate_up split alone 0.391, 5 or 6
+// gate_up slices 0.42 (more CTAs than fit), a floor of 76 KB (2 per SM) 0.43.
 constexpr int kTargetCtas = 200;
+constexpr int kMaxGroupsPerCta = 6;
+constexpr int kCtasPerSm = 3;
+constexpr size_t kMinSmemPerCta = 60 * 1024;   // 4 x (60 + 1) KB exceeds an SM's 228 KB
 constexpr int kMaxCluster = 16;
 constexpr int kMaxNg = 48;                          // chunks a CTA may hold
 // parts (16 x 512 B), red (512 B), flags (16 B), kMaxNg barriers, padded to 128 B
@@ -355,13 +366,15 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
-// K-slices per tile: about kTargetCtas CTAs over the grid, at most 16 (one
-// cluster), and few enough groups per CTA for its shared memory (44 chunks of
-// group 64, 22 of group 128).
-int fused_ksplit(int T, int K, int group)
+// K-slices per tile (see kTargetCtas), at most 16 (one cluster), and few
+// enough groups per CTA for its shared memory (44 chunks of group 64, 22 of
+// group 128).
+int fused_ksplit(int T, int K, int group, int num_sms)
 {
     const int G = K / group;
     int ks = (kTargetCtas + T - 1) / T;
+    const int by_groups = (G + kMaxGroupsPerCta - 1) / kMaxGroupsPerCta;
+    if (by_groups > ks && (long long)T * by_groups <= (long long)kCtasPerSm * num_sms) ks = by_groups;
     if (ks > G) ks = G;
     if (ks > kMaxCluster) ks = kMaxCluster;
     if (ks < 1) ks = 1;
@@ -377,10 +390,11 @@ cudaError_t run(const LaunchCtx& c, const FusedSet& set, int K, int hadamard, co
     using C = Cfg<GROUP>;
     auto kern = gemv_fused_kernel<GROUP, XDT, EPL, CQ>;
     const int G = K / GROUP, T = set.tile0[set.count];
-    const int ks = fused_ksplit(T, K, GROUP);
+    const int ks = fused_ksplit(T, K, GROUP, c.num_sms);
     const int ng_max = (G + ks - 1) / ks;
     if (ng_max > (GROUP == 64 ? 44 : 22)) return cudaErrorInvalidValue;   // K too large for one cluster per tile
-    const size_t smem = smem_bytes(ng_max, C::CB, ng_max, GROUP);
+    size_t smem = smem_bytes(ng_max, C::CB, ng_max, GROUP);
+    if ((long long)T * ks <= (long long)kCtasPerSm * c.num_sms && smem < kMinSmemPerCta) smem = kMinSmemPerCta;
     static KernelSmem configured;
     const cudaError_t e = ensure_smem(configured, c, kern, smem, /*nonportable_cluster=*/true);
     if (e != cudaSuccess) return e;
@@ -421,7 +435,7 @@ cudaError_t run_group(const LaunchCtx& c, const FusedSet& set, int K, int group,
                       int x_dtype, int8_t* a_out, float* sx_out)
 {
     // short slices (at most 16 groups per CTA) quantize with a warp per group
-    const int ks = fused_ksplit(set.tile0[set.count], K, group);
+    const int ks = fused_ksplit(set.tile0[set.count], K, group, c.num_sms);
     const bool short_slice = (K / group + ks - 1) / ks <= 16;
     if (group == 64)
         return short_slice ? run_dtype<64, 2, CQ>(c, set, K, hadamard, x, x_dtype, a_out, sx_out)
