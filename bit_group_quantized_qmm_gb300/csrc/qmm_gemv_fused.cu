@@ -46,13 +46,14 @@ constexpr int kThreads = kComputeThreads + 32;   // + producer warp
 // kMinSmemPerCta of shared memory, so that no SM holds more than kCtasPerSm of
 // them (the block scheduler otherwise stacked up to 5 gate_up CTAs on an SM
 // whose weight copies then landed last). K-slices of gate_up / down / q / o
-// become 4 / 16 / 13 / 16 (from 3 / 16 / 13 / 16): 0.367 against 0.382; the
-// shared-memory floor alone 0.378, the gate_up split alone 0.391, 5 or 6
-// gate_up slices 0.42 (more CTAs than fit), a floor of 76 KB (2 per SM) 0.43.
+// become 4 / 16 / 13 / 16 (from 3 / 16 / 13 / 16): 0.361 against 0.382 with
+// at most 4 CTAs per SM, 0.366 with at most 3, 0.394 with at most 5; at most
+// 5 or 4 groups per CTA 0.373 / 0.374, the split alone 0.391, a floor allowing
+// only 2 per SM 0.43.
 constexpr int kTargetCtas = 200;
 constexpr int kMaxGroupsPerCta = 6;
-constexpr int kCtasPerSm = 3;
-constexpr size_t kMinSmemPerCta = 60 * 1024;   // 4 x (60 + 1) KB exceeds an SM's 228 KB
+constexpr int kCtasPerSm = 4;
+constexpr size_t kMinSmemPerCta = 45 * 1024;   // 5 x (45 + 1) KB exceeds an SM's 228 KB
 constexpr int kMaxCluster = 16;
 constexpr int kMaxNg = 48;                          // chunks a CTA may hold
 // parts (16 x 512 B), red (512 B), flags (16 B), kMaxNg barriers, padded to 128 B
