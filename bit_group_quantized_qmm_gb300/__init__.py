@@ -27,7 +27,8 @@ QMM_DTYPE_F32, QMM_DTYPE_F16, QMM_DTYPE_BF16 = 0, 1, 2
 QMM_PATH_GEMV, QMM_PATH_GEMM = 0, 1
 KERNEL_IDS = {0: "none", 1: "pack", 2: "prep_w4a8", 3: "prep_affine", 4: "gemv_w4a8", 5: "gemm_w4a8",
               6: "gemm_affine", 7: "gemv_fused", 8: "gemm_rows", 9: "gemv_fused_siblings", 10: "gemv_cq4",
-              11: "gemm_cq4", 12: "prep_rotated", 13: "gemm_narrow"}
+              11: "gemm_cq4", 12: "prep_rotated", 13: "gemm_narrow",
+              14: "gemm_narrow_e4m3"}
 
 STATUS = {0: "QMM_OK", 1: "QMM_ERR_INVALID_ARG", 2: "QMM_ERR_UNSUPPORTED_SHAPE", 3: "QMM_ERR_UNSUPPORTED_DEVICE",
           4: "QMM_ERR_MISALIGNED", 5: "QMM_ERR_CUDA", 6: "QMM_ERR_TIMEOUT", 7: "QMM_ERR_WORKSPACE"}
@@ -247,7 +248,7 @@ def qmm_set_gemm_weight_operand(in_shared_memory: bool):
     _L.qmm_set_gemm_weight_operand(1 if in_shared_memory else 0)
 
 
-NARROW_OFF, NARROW_AUTO, NARROW_ALWAYS = 0, 1, 2
+NARROW_OFF, NARROW_AUTO, NARROW_ALWAYS, NARROW_F16 = 0, 1, 2, 3
 
 
 def qmm_set_gemm_narrow(mode: int):

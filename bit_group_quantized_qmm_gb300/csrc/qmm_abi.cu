@@ -456,8 +456,15 @@ static qmm_status gemm_common(const qmm_weight_desc* w, const void* packed, int3
         if (e != cudaErrorNotSupported) return launched(e, QMM_KERNEL_GEMM_ROWS);
     }
     const bool many_tiles = (w->N + 127) / 128 >= 512;
+    if (w->variant == QMM_W4A8 && !P && M <= 16 && w->group == 128 &&
+        (g_narrow == QMM_NARROW_ALWAYS || (g_narrow == QMM_NARROW_AUTO && many_tiles))) {
+        const cudaError_t e = launch_gemm_narrow_e4m3(c, M, w->N, w->K, blob, static_cast<const uint16_t*>(act16),
+                                                      act_scale, Y);
+        if (e != cudaErrorNotSupported) return launched(e, QMM_KERNEL_GEMM_NARROW_E4M3);
+    }
     if (int8_act(w->variant) && !P && M <= 32 &&
-        (g_narrow == QMM_NARROW_ALWAYS || (g_narrow == QMM_NARROW_AUTO && w->variant == QMM_W4A8 && many_tiles))) {
+        (g_narrow == QMM_NARROW_ALWAYS || g_narrow == QMM_NARROW_F16 ||
+         (g_narrow == QMM_NARROW_AUTO && w->variant == QMM_W4A8 && many_tiles))) {
         CUtensorMap nmap;
         if (!act_tensor_map(&nmap, act16, M, w->K, (M + 7) & ~7)) return QMM_ERR_CUDA;
         const cudaError_t e = launch_gemm_narrow(c, cq4, w->group, nmap, M, w->N, w->K, blob, act_scale, Y);
@@ -551,7 +558,8 @@ void qmm_set_gemm_weight_operand(int32_t in_shared_memory) { g_a_in_smem = in_sh
 
 void qmm_set_gemm_narrow(int32_t mode)
 {
-    g_narrow = mode == QMM_NARROW_OFF || mode == QMM_NARROW_ALWAYS ? mode : QMM_NARROW_AUTO;
+    g_narrow = mode == QMM_NARROW_OFF || mode == QMM_NARROW_ALWAYS || mode == QMM_NARROW_F16 ? mode
+                                                                                          : QMM_NARROW_AUTO;
 }
 
 void qmm_set_gemm_rows_max(int32_t max_rows) { g_rows_max = max_rows < 0 ? 0 : (max_rows > 16 ? 16 : max_rows); }

@@ -133,6 +133,11 @@ cudaError_t launch_gemm_cq4(const LaunchCtx& c, int group, const CUtensorMap& ma
 // MMA's N slot. map: act_tensor_map of act16 with boxes of M rounded up to 8 rows.
 cudaError_t launch_gemm_narrow(const LaunchCtx& c, bool cq4, int group, const CUtensorMap& map, int M, int N, int K,
                                const uint8_t* blob, const float* sx, float* Y);
+// W4A8 GEMM for M <= 16, group 128, on the tensor cores with the weights in the
+// MMA's N slot and e4m3 operands; cudaErrorNotSupported when K is too long for
+// its shared memory (the caller then uses the fp16 form).
+cudaError_t launch_gemm_narrow_e4m3(const LaunchCtx& c, int M, int N, int K, const uint8_t* blob,
+                                    const uint16_t* act16, const float* sx, float* Y);
 // W4A8 / CQ4 GEMM for M <= 16 on the CUDA cores; cudaErrorNotSupported when the
 // shape does not fit it (the caller then uses the tensor-core kernel).
 cudaError_t launch_gemm_rows(const LaunchCtx& c, bool cq4, int group, int M, int N, int K, const uint8_t* blob,

@@ -235,6 +235,19 @@ __device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uin
         : "memory");
 }
 
+// D (tensor memory) [+]= A x B, both shared-memory descriptors, kind::f8f6f4.
+// With format fields 0 in the instruction descriptor (idesc_f16_f32's
+// encoding) A and B are e4m3, 32 elements (32 bytes) of K per instruction.
+__device__ __forceinline__ void mma_e4m3_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16: fp16 A and B, both
 // K-major, fp32 accumulator, shape M x N (x K = 16).
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N)

@@ -106,7 +106,8 @@ typedef enum {
     QMM_KERNEL_GEMV_CQ4 = 10,
     QMM_KERNEL_GEMM_CQ4 = 11,
     QMM_KERNEL_PREP_ROTATED = 12,
-    QMM_KERNEL_GEMM_NARROW = 13
+    QMM_KERNEL_GEMM_NARROW = 13,
+    QMM_KERNEL_GEMM_NARROW_E4M3 = 14
 } qmm_kernel_id;
 
 typedef void* qmm_stream; /* cudaStream_t */
@@ -389,7 +390,13 @@ qmm_status qmm_gemv_static_scratch(const qmm_weight_desc* w, const void* packed,
  * W4A8 ones with M <= 32 and at least 512 row tiles run the kernel that puts
  * the weights in the MMA's N slot, 256 weight rows per MMA
  * (QMM_KERNEL_GEMM_NARROW; see qmm_set_gemm_narrow), which performs the same
- * operations in the same order as the general tensor-core kernel.
+ * operations in the same order as the general tensor-core kernel. Those with
+ * M <= 16 and group 128 (K at most 1792) run its e4m3 form
+ * (QMM_KERNEL_GEMM_NARROW_E4M3): weight nibbles u = q + 8 and the two planes of
+ * each activation code (16 floor(a/16) and a mod 16) are exact e4m3 numbers,
+ * the kind::f8f6f4 MMA sums their products exactly, and the raw partial is
+ * recovered as P = sum a u - 8 sum a; the rescale that follows is the general
+ * kernel's, so the outputs are the same bits.
  *   QMM_W4A8:   act16 = qmm_prep_act a16 [M][K] fp16 codes, act_scale = sx [M][G]
  *               Y[m][n] = sum_g sw[n][g] * sx[m][g] * P[m][n][g]
  *   QMM_CQ4:    as QMM_W4A8, with q[n][k] = C[i[n][k]], times cb_scale
@@ -463,12 +470,15 @@ void qmm_set_gemm_rows_max(int32_t max_rows);
  * run the tensor-core kernel with the weights in the MMA's N slot
  * (process-wide, launches after the call): QMM_NARROW_OFF never;
  * QMM_NARROW_AUTO (default) for W4A8 with at least 512 row tiles, where it
- * measured faster (lm_head: 0.88x to 0.96x the time of the general kernel;
- * codebook weights and few row tiles were slower); QMM_NARROW_ALWAYS for every
- * such call (tests). The outputs are the same bits either way; shapes whose
- * activation scales overflow its shared memory (K / group above about 300)
+ * measured faster (lm_head: 0.88x to 0.96x the time of the general kernel in
+ * its fp16 form; codebook weights and few row tiles were slower);
+ * QMM_NARROW_ALWAYS for every such call (tests); QMM_NARROW_F16 for every such
+ * call, always in the fp16 form. Under AUTO and ALWAYS, W4A8 calls with
+ * M <= 16 and group 128 take the e4m3 form when K fits its shared memory. The
+ * outputs are the same bits whichever kernel runs; shapes whose activation
+ * scales overflow the fp16 form's shared memory (K / group above about 300)
  * stay on the general kernel. */
-enum { QMM_NARROW_OFF = 0, QMM_NARROW_AUTO = 1, QMM_NARROW_ALWAYS = 2 };
+enum { QMM_NARROW_OFF = 0, QMM_NARROW_AUTO = 1, QMM_NARROW_ALWAYS = 2, QMM_NARROW_F16 = 3 };
 void qmm_set_gemm_narrow(int32_t mode);
 
 #ifdef __cplusplus

@@ -130,8 +130,9 @@ def gemv(d, packed, a, sx, workspace=True):
 
 def gemm(d, packed, M, act16, act_scale, kernel=None):
     """qmm_gemm into a NaN-filled Y; checks which kernel ran (W4A8: the
-    tensor-core kernel 5, its weights-in-N form 13 (M <= 32) or the CUDA-core
-    small-M kernel 8; CQ4: 11, 13 or 8; affine: 6)."""
+    tensor-core kernel 5, its weights-in-N form 13 (M <= 32) or 14 (e4m3,
+    M <= 16, group 128), or the CUDA-core small-M kernel 8; CQ4: 11, 13 or 8;
+    affine: 6)."""
     import torch
     q = lib()
     Y = guarded((M, d.N), torch.float32, float("nan"))
@@ -141,7 +142,7 @@ def gemm(d, packed, M, act16, act_scale, kernel=None):
     if kernel is not None:
         assert kid == kernel, kid
     else:
-        assert kid in {W4A8: (5, 8, 13), CQ4: (11, 8, 13), AFFINE: (6,)}[d.variant], kid
+        assert kid in {W4A8: (5, 8, 13, 14), CQ4: (11, 8, 13), AFFINE: (6,)}[d.variant], kid
     return Y
 
 

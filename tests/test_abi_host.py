@@ -165,7 +165,7 @@ def test_kernel_ids_match_header(q):
     ids = {int(v) for v in re.findall(r"QMM_KERNEL_\w+\s*=\s*(\d+)", hdr)}
     assert ids == set(q.KERNEL_IDS), (sorted(ids), sorted(q.KERNEL_IDS))
     modes = dict(re.findall(r"(QMM_NARROW_\w+)\s*=\s*(\d+)", hdr))
-    assert {int(v) for v in modes.values()} == {q.NARROW_OFF, q.NARROW_AUTO, q.NARROW_ALWAYS}
+    assert {int(v) for v in modes.values()} == {q.NARROW_OFF, q.NARROW_AUTO, q.NARROW_ALWAYS, q.NARROW_F16}
     assert int(modes["QMM_NARROW_AUTO"]) == q.NARROW_AUTO
 
 

@@ -8,9 +8,9 @@ accumulator buffer and scale stage) and record a failure in the device error
 word instead of making the access. A child process loads it
 (QMM_CHECKED_LIBRARY=1) and runs a set of small calls that reach every kernel
 family: pack, both prepasses, the plain and fused GEMVs (and siblings), the
-tensor-core GEMM with the weight operand in tensor and in shared memory,
-its weights-in-N form, the CUDA-core small-M GEMM, the raw-partials hook, the
-affine GEMM and codebook weights. Every call must leave the error word at
+tensor-core GEMM with the weight operand in tensor and in shared memory, its
+weights-in-N forms (fp16 and e4m3), the CUDA-core small-M GEMM, the
+raw-partials hook, the affine GEMM and codebook weights. Every call must leave the error word at
 zero, and every output must equal the product library's, bit for bit (the
 checks change no arithmetic).
 """
@@ -81,6 +81,12 @@ def run_cases(out_path):
     _, a16b, sxb, _, _ = gc.prep_w4a8(x2, g2, g2)
     Y = gc.gemm(d2, packed2, M2, a16b, sxb, kernel=5)
     done("gemm_g128", Y)
+    q.qmm_set_gemm_narrow(q.NARROW_ALWAYS)
+    try:
+        Y = gc.gemm(d2, packed2, 16, a16b[0:16], sxb[0:16], kernel=14)   # e4m3 operands, weights in N
+        done("gemm_narrow_e4m3", Y)
+    finally:
+        q.qmm_set_gemm_narrow(q.NARROW_AUTO)
     # siblings
     ys = [gc.guarded((n,), torch.float32, float("nan")) for n in (N, N2)]
     qb3, sw3, _ = gc.w4a8_case(93, "checked/sib", N2, K, g, g, 1)

@@ -398,7 +398,7 @@ def test_gemm_narrow_output(torch_cuda, orc, M, N, K, group, had):
     d, packed = gc.pack(W4A8, N, K, group, qb, sw)
     _, a16, sx, _, _ = gc.prep_w4a8(x, group, had)
     q.qmm_set_gemm_rows_max(0)
-    q.qmm_set_gemm_narrow(q.NARROW_ALWAYS)
+    q.qmm_set_gemm_narrow(q.NARROW_F16)
     try:
         Yn = gc.gemm(d, packed, M, a16, sx, kernel=13).cpu().numpy()
         Yn2 = gc.gemm(d, packed, M, a16, sx, kernel=13).cpu().numpy()
@@ -413,6 +413,86 @@ def test_gemm_narrow_output(torch_cuda, orc, M, N, K, group, had):
     ok, worst = gc.within_w4a8(Yn, Y, Ym)
     assert ok, f"worst error / bound = {worst}"
     assert np.array_equal(Yn.view(np.uint32), Yt.view(np.uint32)), "differs from the general tensor-core kernel"
+
+
+# M <= 16, group 128: the e4m3 form of the weights-in-N kernel (kind::f8f6f4
+# MMAs on the nibbles u = q + 8 and the two planes of each activation code).
+# Every output against the oracle; bit for bit against the fp16 form and the
+# general tensor-core kernel (the partials are the same exact integers and the
+# rescale is the same operations); a repeat. Ragged and odd tile counts, N % 4
+# != 0 (scalar stores), rows M..15 unused, no rotation, K of 12 and 14 groups
+# (the longest it holds) and one group.
+E4M3_CASES = [
+    (1, 200, 256, 128, 128),
+    (9, 384, 512, 128, 128),            # 3 tiles: one full pair, one half
+    (16, 256, 1536, 128, 128),
+    (16, 640 * 128 - 40, 256, 128, 0),  # 320 pairs over the persistent blocks
+    (12, 640 * 128 - 41, 256, 128, 128),
+    (5, 1000, 384, 128, 128),
+    (16, 300, 1792, 128, 128),
+    (3, 130, 128, 128, 128),
+]
+
+
+@pytest.mark.parametrize("M,N,K,group,had", E4M3_CASES)
+def test_gemm_narrow_e4m3_output(torch_cuda, orc, M, N, K, group, had):
+    q = gc.lib()
+    qb, sw, x = gc.w4a8_case(17, f"narrow_e4m3/{M}/{N}/{K}", N, K, group, had, M)
+    d, packed = gc.pack(W4A8, N, K, group, qb, sw)
+    _, a16, sx, _, _ = gc.prep_w4a8(x, group, had)
+    q.qmm_set_gemm_rows_max(0)
+    q.qmm_set_gemm_narrow(q.NARROW_ALWAYS)
+    try:
+        Ye = gc.gemm(d, packed, M, a16, sx, kernel=14).cpu().numpy()
+        Ye2 = gc.gemm(d, packed, M, a16, sx, kernel=14).cpu().numpy()
+        q.qmm_set_gemm_narrow(q.NARROW_F16)
+        Yn = gc.gemm(d, packed, M, a16, sx, kernel=13).cpu().numpy()
+        q.qmm_set_gemm_narrow(q.NARROW_OFF)
+        Yt = gc.gemm(d, packed, M, a16, sx, kernel=5).cpu().numpy()
+    finally:
+        q.qmm_set_gemm_rows_max(ROWS_DEFAULT)
+        q.qmm_set_gemm_narrow(q.NARROW_AUTO)
+    assert np.array_equal(Ye.view(np.uint32), Ye2.view(np.uint32)), "not deterministic"
+    ra, rsx, _ = orc.prep_w4a8(x, group, had)
+    Y, Ym = orc.gemm_w4a8(qb, sw, ra, rsx, group)
+    ok, worst = gc.within_w4a8(Ye, Y, Ym)
+    assert ok, f"worst error / bound = {worst}"
+    assert np.array_equal(Ye.view(np.uint32), Yn.view(np.uint32)), "differs from the fp16 form"
+    assert np.array_equal(Ye.view(np.uint32), Yt.view(np.uint32)), "differs from the general tensor-core kernel"
+
+
+def test_gemm_narrow_e4m3_extreme_codes(torch_cuda):
+    """Codes at the ends of both ranges: weights q = -8 and 7 (u = 0 and 15),
+    activation codes -127, 127, -1, 0, 1, 15, 16, -16, -17 (every hi/lo split
+    edge); bit for bit against the general tensor-core kernel."""
+    import torch
+    q = gc.lib()
+    N, K, g, M = 512, 256, 128, 16
+    rng = np.random.default_rng(5)
+    qv = rng.choice(np.array([-8, 7, 0, -1, 1], np.int8), size=(N, K))
+    nib = (qv & 15).astype(np.uint8)
+    qbytes = (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)   # low nibble = even k
+    sw = rng.uniform(0.005, 0.02, size=(N, K // g)).astype(np.float16)
+    d, packed = gc.pack(W4A8, N, K, g, qbytes, sw.view(np.uint16))
+    codes = rng.choice(np.array([-127, 127, -1, 0, 1, 15, 16, -16, -17], np.float16), size=(M, K))
+    a16 = gc.t(codes)
+    sx = gc.t(rng.uniform(0.5, 2.0, size=(M, K // g)).astype(np.float32))
+    q.qmm_set_gemm_narrow(q.NARROW_ALWAYS)
+    q.qmm_set_gemm_rows_max(0)
+    try:
+        Ye = gc.gemm(d, packed, M, a16, sx, kernel=14).cpu().numpy()
+        q.qmm_set_gemm_narrow(q.NARROW_OFF)
+        Yt = gc.gemm(d, packed, M, a16, sx, kernel=5).cpu().numpy()
+    finally:
+        q.qmm_set_gemm_rows_max(ROWS_DEFAULT)
+        q.qmm_set_gemm_narrow(q.NARROW_AUTO)
+    assert np.array_equal(Ye.view(np.uint32), Yt.view(np.uint32))
+    # and against the definition: sum_g sw sx sum_k q a, in fp64
+    P = np.einsum("mgk,ngk->mng", codes.astype(np.float64).reshape(M, K // g, g),
+                  qv.astype(np.float64).reshape(N, K // g, g))
+    ref = np.einsum("mng,ng,mg->mn", P, sw.astype(np.float64), sx.cpu().numpy().astype(np.float64))
+    bound = 1e-5 * np.einsum("mng,ng,mg->mn", np.abs(P), sw.astype(np.float64), sx.cpu().numpy().astype(np.float64)) + 1e-6
+    assert np.all(np.abs(Ye - ref) <= bound)
 
 
 def _sample_rows(N, n=48):
@@ -451,7 +531,7 @@ def test_lm_head_full_size_sampled(lm_head, orc, M):
     g = lay.group
     x = qmm_synth.layer_activations(0, f"lm_head/x{M}", lay, M)
     a, a16, sx, _, _ = gc.prep_w4a8(x, g, g)
-    Yg = gc.gemm(d, packed, M, a16, sx, kernel=8 if M <= 8 else 13).cpu().numpy()
+    Yg = gc.gemm(d, packed, M, a16, sx, kernel=8 if M <= 8 else (14 if M <= 16 else 13)).cpu().numpy()
     ra, rsx, _ = orc.prep_w4a8(x, g, g)
     rows = _sample_rows(lay.N)
     Y, Ym = orc.gemm_w4a8(qb, sw, ra, rsx, g, rows=rows)
@@ -459,8 +539,9 @@ def test_lm_head_full_size_sampled(lm_head, orc, M):
     assert ok, f"GEMM worst error / bound = {worst}"
     # the same call on the other kernels that serve this M
     q = gc.lib()
-    on, off = q.NARROW_AUTO, q.NARROW_OFF
-    others = [(0, on, 13), (0, off, 5)] if M <= 8 else [(0, off, 5)] + ([(16, on, 8)] if M <= 16 else [])
+    on, off, f16 = q.NARROW_AUTO, q.NARROW_OFF, q.NARROW_F16
+    others = [(0, on, 14), (0, f16, 13), (0, off, 5)] if M <= 8 else \
+        [(0, off, 5)] + ([(16, on, 8), (0, f16, 13)] if M <= 16 else [])
     for rows_max, narrow, kernel in others:
         q.qmm_set_gemm_rows_max(rows_max)
         q.qmm_set_gemm_narrow(narrow)
