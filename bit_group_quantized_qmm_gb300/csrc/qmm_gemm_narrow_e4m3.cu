@@ -69,6 +69,7 @@ constexpr int kE8BStage = kE8Rows * 128;      // weight operand: 256 rows x 128 
 constexpr int kE8Plane = 32 * 128;            // one group's hi and lo rows
 constexpr int kE8XB = kE8Rows * 4;            // scale stage: sw of the 256 rows
 constexpr int kE8RA = 2, kE8RB = 3, kE8RW = 2, kE8RX = 4, kE8DS = 2;
+constexpr int kE8Prefetch = 6;               // groups ahead of the bulk copies, into L2
 constexpr int kE8Bars = 2 * kE8RW + 2 * kE8RA + 2 * kE8RB + 2 * kE8RX + 2 * kE8DS + 2;
 
 size_t e8_smem_bytes(int G)
@@ -225,6 +226,17 @@ __global__ void __launch_bounds__(kE8Threads, 1)
                     mbar_arrive_expect_tx(&w_full[ws], (uint32_t)(two ? 2 * kE8CB : kE8CB));
                     bulk_g2s(dst, src0 + (size_t)g * kE8CB, kE8CB, &w_full[ws]);
                     if (two) bulk_g2s(dst + kE8CB, src0 + (size_t)(G + g) * kE8CB, kE8CB, &w_full[ws]);
+                    // the chunks kE8Prefetch groups ahead into L2: one block per SM
+                    // holds only kE8RW chunk pairs in shared memory, too few bytes
+                    // in flight to cover HBM latency at full bandwidth
+                    {
+                        const int ahead = issued + kE8Prefetch, tpa = (int)blockIdx.x + (ahead / G) * (int)gridDim.x;
+                        if (tpa < TP) {
+                            const uint8_t* srca = blob + (size_t)(2 * tpa) * G * kE8CB + (size_t)(ahead % G) * kE8CB;
+                            bulk_prefetch_l2(srca, kE8CB);
+                            if (2 * tpa + 1 < T) bulk_prefetch_l2(srca + (size_t)G * kE8CB, kE8CB);
+                        }
+                    }
                     ++issued;
                     ring_next<kE8RW>(ws, wph);
                 }
