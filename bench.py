@@ -13,7 +13,7 @@ The per-step weights (> 2x L2) are larger than L2, so no flush is needed.
   python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--no-sweep]
   python bench.py --profile-case prefill_gemm:1068     (a few GEMM launches, for ncu; also prep_rotated:M,
                                                         lm_head_gemv:1, lm_head_gemv_cq4:1, lm_head_gemm:M,
-                                                        affine_gemm:M)
+                                                        lm_head_gemm_f16:M, affine_gemm:M)
 
 The step is captured once in a CUDA graph (the kernels are launched with
 programmatic dependent launch, so each GEMV streams its weights while the
@@ -66,7 +66,7 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--peaks", action="store_true",
                    help="compile and run the FP32 / mma.sync peak microbenchmark and exit (one JSON line)")
-    p.add_argument("--profile-case", default=None, metavar="prefill_gemm:M|prep_rotated:M|lm_head_gemv[_cq4]:1|lm_head_gemm:M|affine_gemm:M",
+    p.add_argument("--profile-case", default=None, metavar="prefill_gemm:M|prep_rotated:M|lm_head_gemv[_cq4]:1|lm_head_gemm[_f16]:M|affine_gemm:M",
                    help="run one prefill GEMM shape a few times and exit (for profilers; prints one JSON line)")
     return p.parse_args()
 
@@ -999,9 +999,13 @@ def profile_case(spec):
     import bit_group_quantized_qmm_gb300 as q
     name, _, m = spec.partition(":")
     if name not in ("prefill_gemm", "prep_rotated", "lm_head_gemv", "lm_head_gemv_cq4", "lm_head_gemm",
-                    "affine_gemm") or not m.isdigit():
+                    "lm_head_gemm_f16", "affine_gemm") or not m.isdigit():
         raise SystemExit(f"unknown profile case {spec!r} (expected prefill_gemm:M, prep_rotated:M, "
-                         "lm_head_gemv:1, lm_head_gemv_cq4:1, lm_head_gemm:M or affine_gemm:M)")
+                         "lm_head_gemv:1, lm_head_gemv_cq4:1, lm_head_gemm[_f16]:M or affine_gemm:M)")
+    if name == "lm_head_gemm_f16":
+        # the same GEMM with the weights-in-N kernel held to its fp16 form (M 9..32)
+        q.qmm_set_gemm_narrow(q.NARROW_F16)
+        name = "lm_head_gemm"
     if name == "affine_gemm":
         # the affine GEMM of the fused gate_up shape (K = 5120, N = 34816, group 64, fp16 x)
         M, N, K = int(m), 34816, 5120
