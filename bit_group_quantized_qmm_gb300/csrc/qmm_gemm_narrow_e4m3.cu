@@ -298,18 +298,29 @@ __global__ void __launch_bounds__(kE8Threads, 1)
                 }
                 // piece p (16 bytes) of the row holds k = 32 p .. 32 p + 31, word
                 // i of it k = 32 p + 8 i .. + 7; its 8 output bytes land at 32 p + 8 i
-                uint32_t o[32];
+                // the row's 16 words, and the first step of their lookup, which
+                // needs every loaded value: only then is the chunk released, so
+                // that the producer can refill the stage while the lookups run
+                // (with two chunk stages, the refill's latency paces the kernel)
+                uint32_t w[16], xw[16];
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
                     const uint4 v = *reinterpret_cast<const uint4*>(ch + p * 2048 + r * 16);
-                    expand_word_e4m3(v.x, o[8 * p + 0], o[8 * p + 1]);
-                    expand_word_e4m3(v.y, o[8 * p + 2], o[8 * p + 3]);
-                    expand_word_e4m3(v.z, o[8 * p + 4], o[8 * p + 5]);
-                    expand_word_e4m3(v.w, o[8 * p + 6], o[8 * p + 7]);
+                    w[4 * p] = v.x;
+                    w[4 * p + 1] = v.y;
+                    w[4 * p + 2] = v.z;
+                    w[4 * p + 3] = v.w;
                 }
-                // the chunk's words are all in registers
+#pragma unroll
+                for (int i = 0; i < 16; ++i) xw[i] = w[i] ^ 0x88888888u;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&w_empty[ws]);
+                uint32_t o[32];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    o[2 * i] = e4m3_u4(w[i], xw[i]);
+                    o[2 * i + 1] = e4m3_u4(w[i] >> 16, xw[i] >> 16);
+                }
                 uint8_t* row = bst + (size_t)bs * kE8BStage + (size_t)t * 128;
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
