@@ -313,6 +313,11 @@ __global__ void __launch_bounds__(kE8Threads, 1)
                 }
 #pragma unroll
                 for (int i = 0; i < 16; ++i) xw[i] = w[i] ^ 0x88888888u;
+                // the release must follow the loads: an ordered asm statement
+                // that takes every loaded value keeps the arrive after them
+                asm volatile("" ::"r"(xw[0]), "r"(xw[1]), "r"(xw[2]), "r"(xw[3]), "r"(xw[4]), "r"(xw[5]), "r"(xw[6]),
+                             "r"(xw[7]), "r"(xw[8]), "r"(xw[9]), "r"(xw[10]), "r"(xw[11]), "r"(xw[12]), "r"(xw[13]),
+                             "r"(xw[14]), "r"(xw[15]));
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&w_empty[ws]);
                 uint32_t o[32];
