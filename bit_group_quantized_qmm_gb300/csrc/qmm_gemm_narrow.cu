@@ -295,6 +295,16 @@ __global__ void __launch_bounds__(kNwThreads, 1)
                     }
                     const uint4 p0 = *reinterpret_cast<const uint4*>(ch + (2 * j) * 2048 + r * 16);
                     const uint4 p1 = *reinterpret_cast<const uint4*>(ch + (2 * j + 1) * 2048 + r * 16);
+                    if (j == KSG - 1) {
+                        // the chunk's last words are loaded: release it before the
+                        // expansion, so that the producer refills the stage meanwhile
+                        // (an ordered asm statement taking every loaded word keeps
+                        // the arrive after the loads)
+                        asm volatile("" ::"r"(p0.x), "r"(p0.y), "r"(p0.z), "r"(p0.w), "r"(p1.x), "r"(p1.y), "r"(p1.z),
+                                     "r"(p1.w));
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&w_empty[ws]);
+                    }
                     uint32_t hv[32];
                     if (VARIANT == 2) {
                         expand_word_cq4(book, p0.x, hv + 0);
@@ -314,11 +324,6 @@ __global__ void __launch_bounds__(kNwThreads, 1)
                         expand_word<8>(p1.y, hv + 20);
                         expand_word<8>(p1.z, hv + 24);
                         expand_word<8>(p1.w, hv + 28);
-                    }
-                    if (j == KSG - 1) {
-                        // the chunk's words are all in registers
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&w_empty[ws]);
                     }
                     uint8_t* row = bst + (size_t)bs * kNwBStage + (size_t)t * 128;
 #pragma unroll
