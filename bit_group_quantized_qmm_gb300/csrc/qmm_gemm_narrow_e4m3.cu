@@ -45,6 +45,13 @@
 // expanded weights: within each 8-k block, k = 0, 2, 4, 6, 1, 3, 5, 7. That is
 // the order of the nibble slots in a packed word.
 //
+// The packed weights arrive by bulk copies of chunk pairs into a two-stage
+// ring (all the shared memory the operand stages and the planes leave), so a
+// chunk's refill can start only when its previous use releases it, and the
+// refill's latency paces the groups. The expand warps therefore release a
+// chunk as soon as its words are in registers, before the lookups, and the
+// producer prefetches the chunks six groups ahead into L2.
+//
 // Persistent over pairs of 128-row weight tiles; every wait bounded.
 #include <cuda_fp16.h>
 
