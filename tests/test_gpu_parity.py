@@ -461,6 +461,27 @@ def test_gemm_narrow_e4m3_output(torch_cuda, orc, M, N, K, group, had):
     assert np.array_equal(Ye.view(np.uint32), Yt.view(np.uint32)), "differs from the general tensor-core kernel"
 
 
+def test_gemm_narrow_e4m3_falls_back_on_long_k(torch_cuda, orc):
+    """K = 1920 (15 groups of 128) leaves the e4m3 form's shared memory too
+    small for its activation planes: the call runs the fp16 form (kernel 13)
+    and is still right."""
+    q = gc.lib()
+    M, N, K, g = 16, 640 * 128, 1920, 128
+    qb, sw, x = gc.w4a8_case(18, "narrow_e4m3/long_k", N, K, g, g, M)
+    d, packed = gc.pack(W4A8, N, K, g, qb, sw)
+    _, a16, sx, _, _ = gc.prep_w4a8(x, g, g)
+    q.qmm_set_gemm_rows_max(0)
+    try:
+        Yg = gc.gemm(d, packed, M, a16, sx, kernel=13).cpu().numpy()   # NARROW_AUTO, 640 row tiles
+    finally:
+        q.qmm_set_gemm_rows_max(ROWS_DEFAULT)
+    ra, rsx, _ = orc.prep_w4a8(x, g, g)
+    rows = _sample_rows(N)
+    Y, Ym = orc.gemm_w4a8(qb, sw, ra, rsx, g, rows=rows)
+    ok, worst = gc.within_w4a8(Yg[:, rows], Y, Ym)
+    assert ok, f"worst error / bound = {worst}"
+
+
 def test_gemm_narrow_e4m3_extreme_codes(torch_cuda):
     """Codes at the ends of both ranges: weights q = -8 and 7 (u = 0 and 15),
     activation codes -127, 127, -1, 0, 1, 15, 16, -16, -17 (every hi/lo split
@@ -525,7 +546,7 @@ def lm_head(torch_cuda):
     return lay, qb, sw, d, packed
 
 
-@pytest.mark.parametrize("M", [1, 2, 4, 8, 16, 32])
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 12, 16, 32])
 def test_lm_head_full_size_sampled(lm_head, orc, M):
     lay, qb, sw, d, packed = lm_head
     g = lay.group
